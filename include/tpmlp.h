@@ -1,0 +1,188 @@
+/*
+ * tpmlp - the Megatron tensor-parallel Transformer MLP block on one GB300
+ * (sm_103a), with all p shards on one device.
+ *
+ * The block (sources are web pages on Megatron tensor parallelism):
+ *   - column-parallel first layer: A [h, f] is split along its output columns
+ *     into p shards A_i [h, f/p]; every shard sees the whole input X and
+ *     computes H_i = X A_i + b1_i, Y_i = GeLU(H_i) with no communication
+ *     ("列并行" article, sections 切分原理 / 数学基础 / MLP 应用;
+ *      "Megatron 专家面试题 Level 2", M025);
+ *   - row-parallel second layer: B [f, h] is split along its input rows into
+ *     B_i [f/p, h]; shard i computes the full-shape partial Z_i = Y_i B_i and
+ *     the block returns Z = sum_i Z_i + b2 (Level 2, M026 and M027;
+ *     "分布式并行训练全景", 考点 2).  The pages place that sum in an
+ *     All-Reduce; here it is the row GEMM's own K loop, accumulated in fp32
+ *     tensor memory across all shards, followed by one bf16 store;
+ *   - backward: dA_i = X^T dH_i and dB_i = Y_i^T dZ stay local, dX is the sum
+ *     of the shard contributions dH_i A_i^T (Level 2, M025 追问 and M026).
+ *
+ * Conventions shared by every entry point
+ *   Layout.  Activations are [s, b, h] row-major; token (s_idx, b_idx) is row
+ *     m = s_idx * b + b_idx of an [M, h] matrix, M = s * b.  Shard tensors are
+ *     stored shard-contiguous: A_sh [p][h][f/p], B_sh [p][f/p][h] (the same
+ *     bytes as B [f, h] row-major), b1_sh [p][f/p] (the same bytes as b1 [f]),
+ *     Y_sh / H_sh / dH [p][M][f/p].  All matrices are row-major.
+ *   Memory.  Every pointer is caller-owned device memory (for example
+ *     allocated by PyTorch).  The library never allocates, frees or
+ *     synchronises inside these calls; workspaces are passed in with the sizes
+ *     stated.  Calls are stream ordered and asynchronous: they return after
+ *     the kernels are enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).
+ *   Validation.  Arguments are checked on the host before anything is
+ *     enqueued, in this order: NULL pointers (TPMLP_ERR_NULL), shapes
+ *     (TPMLP_ERR_SHAPE: s, b >= 0; h, ffn, p >= 1; sizes below 2^31 rows),
+ *     divisibility (TPMLP_ERR_DIVISIBILITY: ffn % p, and h % p where stated),
+ *     dtype (TPMLP_ERR_DTYPE), alignment (TPMLP_ERR_ALIGNMENT: every pointer
+ *     16-byte aligned and every row pitch a multiple of 16 bytes, i.e. h and
+ *     ffn/p multiples of 8 for bf16, of 4 for fp32), aliasing
+ *     (TPMLP_ERR_ALIAS: no output overlaps an input or another output), then
+ *     the device (TPMLP_ERR_ARCH unless compute capability 10.3).  An empty
+ *     batch (s * b == 0) is valid and enqueues nothing.  There is no CPU
+ *     fallback.
+ *   Errors.  A failed launch returns TPMLP_ERR_CUDA.  Kernels never trap: a
+ *     device-side wait that runs past its time limit records a status word
+ *     and returns; tpmlp_device_status() reports it as TPMLP_ERR_TIMEOUT.
+ *     tpmlp_last_error() gives a thread-local message for the last failure.
+ *   Numerics.  bf16 inputs, fp32 accumulation in tensor memory, bf16 outputs
+ *     (rounded to nearest even); fp32 inputs run on fp32 FMA (no TF32).
+ */
+#ifndef TPMLP_H
+#define TPMLP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TPMLP_OK = 0,
+    TPMLP_ERR_NULL = 1,
+    TPMLP_ERR_SHAPE = 2,
+    TPMLP_ERR_DIVISIBILITY = 3,
+    TPMLP_ERR_DTYPE = 4,
+    TPMLP_ERR_ALIGNMENT = 5,
+    TPMLP_ERR_ALIAS = 6,
+    TPMLP_ERR_ARCH = 7,
+    TPMLP_ERR_CUDA = 8,
+    TPMLP_ERR_TIMEOUT = 9,
+    TPMLP_ERR_DEVICE = 10
+} tpmlp_status;
+
+typedef enum { TPMLP_BF16 = 0, TPMLP_F32 = 1 } tpmlp_dtype;
+
+typedef enum { TPMLP_ACT_NONE = 0, TPMLP_ACT_GELU_ERF = 1 } tpmlp_act;
+
+/*
+ * Column-parallel layer for all p shards in one launch
+ * ("列并行" article, 数学基础 and MLP 应用; Level 2, M025):
+ *   H_i = X A_i + b1_i,   Y_i = act(H_i),   act = GeLU(z) = z * Phi(z) (erf form) or identity.
+ *   X     [M, h]            dt
+ *   A_sh  [p][h][ffn/p]     dt
+ *   b1_sh [p][ffn/p]        dt, may be NULL (no bias)
+ *   Y_sh  [p][M][ffn/p]     dt, output
+ *   H_sh  [p][M][ffn/p]     dt, optional output of the pre-activation (NULL = not saved)
+ * Requires ffn % p == 0.
+ */
+tpmlp_status tpmlp_column_fwd(const void* X, const void* A_sh, const void* b1_sh, void* Y_sh, void* H_sh,
+                              int64_t s, int64_t b, int64_t h, int64_t ffn, int p,
+                              tpmlp_dtype dt, tpmlp_act act, void* stream);
+
+/*
+ * Row-parallel layer with the shard sum on device
+ * (Level 2, M026; "分布式并行训练全景", 考点 2: Z = Z_1 + Z_2 + ...):
+ *   Z = sum_i Y_i B_i + b2     (b2 added once, after the sum)
+ *   Y_sh [p][M][ffn/p] dt;  B_sh [p][ffn/p][h] dt;  b2 [h] dt or NULL;  Z [M, h] dt, output.
+ * Requires ffn % p == 0.
+ */
+tpmlp_status tpmlp_row_fwd(const void* Y_sh, const void* B_sh, const void* b2, void* Z,
+                           int64_t s, int64_t b, int64_t h, int64_t ffn, int p,
+                           tpmlp_dtype dt, void* stream);
+
+/*
+ * The MLP block forward: column (GeLU, erf form) then row, as two launches
+ * ("列并行" article, MLP 应用: no gather between the layers, one sum at the end).
+ *   Y_ws  [p][M][ffn/p] dt  caller workspace, holds Y on return (needed by the backward)
+ *   H_sh  [p][M][ffn/p] dt  optional pre-activation save for the backward (NULL = not saved)
+ *   other arguments as in tpmlp_column_fwd / tpmlp_row_fwd.
+ * Requires ffn % p == 0 and h % p == 0.
+ */
+tpmlp_status tpmlp_mlp_fwd(const void* X, const void* A_sh, const void* b1_sh, const void* B_sh, const void* b2,
+                           void* Z, void* Y_ws, void* H_sh,
+                           int64_t s, int64_t b, int64_t h, int64_t ffn, int p,
+                           tpmlp_dtype dt, void* stream);
+
+/*
+ * The MLP block backward from dZ (Level 2, M025 追问 and M026; chain rule):
+ *   dY_i = dZ B_i^T,  dH_i = dY_i * GeLU'(H_i),  GeLU'(z) = Phi(z) + z phi(z)
+ *   dB_i = Y_i^T dZ,  dA_i = X^T dH_i,  db1_i = 1^T dH_i,  db2 = 1^T dZ   (local)
+ *   dX   = sum_i dH_i A_i^T                                                (summed on device)
+ * Inputs:  X [M,h], A_sh, B_sh, H_sh and Y_sh from the forward, dZ [M,h]   (all dt)
+ * Outputs: dX [M,h] dt;  dA_sh [p][h][ffn/p], dB_sh [p][ffn/p][h], db1_sh [p][ffn/p] (or NULL),
+ *          db2 [h] (or NULL), all grad_dt (fp32 recommended for bf16 inputs).
+ * Workspace: dH_ws [p][M][ffn/p] dt, holds dH on return.
+ * Requires ffn % p == 0 and h % p == 0; grad_dt must be TPMLP_F32 when dt is TPMLP_F32.
+ */
+tpmlp_status tpmlp_mlp_bwd(const void* X, const void* A_sh, const void* B_sh, const void* H_sh, const void* Y_sh,
+                           const void* dZ, void* dX, void* dA_sh, void* dB_sh, void* db1_sh, void* db2,
+                           void* dH_ws, int64_t s, int64_t b, int64_t h, int64_t ffn, int p,
+                           tpmlp_dtype dt, tpmlp_dtype grad_dt, void* stream);
+
+/*
+ * Column shard layout ("列并行" article, 切分原理: W = [W(1) || ... || W(p)];
+ * the article's NumPy demo uses np.split(W, p, axis=1)):
+ *   W_sh[i][r][c] = W[r][i * cols/p + c],   W [rows, cols] dt,  W_sh [p][rows][cols/p] dt.
+ * Requires cols % p == 0 and (cols/p) a multiple of 8 (bf16) / 4 (fp32). Bit-exact copy.
+ */
+tpmlp_status tpmlp_shard_columns(const void* W, void* W_sh, int64_t rows, int64_t cols, int p,
+                                 tpmlp_dtype dt, void* stream);
+
+/* The inverse of tpmlp_shard_columns: W[r][i * cols/p + c] = W_sh[i][r][c]. */
+tpmlp_status tpmlp_unshard_columns(const void* W_sh, void* W, int64_t rows, int64_t cols, int p,
+                                   tpmlp_dtype dt, void* stream);
+
+/*
+ * Per-head interleave of a packed QKV projection ("Tencent Hunyuan AI Infra
+ * interview", answer on QKV: interleave the packed matrix so that each head's
+ * Q, K and V land on the same card; Level 2, M028: QKV column parallel by heads).
+ *   W_qkv [rows, 3h] = [Q | K | V] (each h wide, head g at columns g*d..g*d+d-1, d = h/n_heads)
+ *   W_out [rows, 3h] head-major: dst column (3g + t) d + e = src column t h + g d + e, t in {0,1,2}.
+ * After it, a p-way column split gives rank r the heads r n/p .. (r+1) n/p - 1 with their Q, K, V.
+ * inverse != 0 applies the inverse permutation.  Requires n_heads % p == 0 and h % n_heads == 0.
+ * Bit-exact copy.
+ */
+tpmlp_status tpmlp_qkv_interleave(const void* W_qkv, void* W_out, int64_t rows, int64_t h, int64_t n_heads,
+                                  int p, tpmlp_dtype dt, int inverse, void* stream);
+
+/* Host-only: the source column of destination column dst_col of tpmlp_qkv_interleave (-1 on bad args). */
+int64_t tpmlp_qkv_src_col(int64_t dst_col, int64_t h, int64_t n_heads);
+
+/*
+ * Synchronises `stream`, then reads and clears this device's status word.
+ * TPMLP_OK, TPMLP_ERR_TIMEOUT (a device-side wait gave up), TPMLP_ERR_DEVICE (another
+ * recorded device error) or TPMLP_ERR_CUDA.
+ */
+tpmlp_status tpmlp_device_status(void* stream);
+
+/*
+ * Test hook for the bounded waits: launches one warp that waits on a barrier
+ * nothing completes, with a limit of timeout_us microseconds (1 .. 1000000).
+ * The wait gives up, records TPMLP_ERR_TIMEOUT in the status word and returns.
+ */
+tpmlp_status tpmlp_debug_wait_timeout(uint32_t timeout_us, void* stream);
+
+/* Human-readable name of a status code. */
+const char* tpmlp_status_string(tpmlp_status st);
+
+/* Thread-local description of the last failure in this thread ("" if none). */
+const char* tpmlp_last_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int tpmlp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPMLP_H */

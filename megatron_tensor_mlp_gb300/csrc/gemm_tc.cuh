@@ -1,0 +1,373 @@
+// Persistent, warp-specialised bf16 GEMM on the 5th-generation tensor cores
+// (tcgen05.mma, fp32 accumulators in tensor memory), fed by TMA, with the
+// fused epilogues of the tensor-parallel MLP block.
+//
+//   D_s[M,N] = A_s[M,K] B_s[K,N]           (batched over shards s), or
+//   D  [M,N] = sum_s A_s[M,K] B_s[K,N]     (shard sum inside the K loop)
+//
+// CTA layout (384 threads, one CTA per SM, persistent over output tiles):
+//   warp 0        TMA producer: fills a STAGES-deep ring of (A, B) tiles
+//   warp 1        TMEM allocator + MMA issuer (one thread): 4 x (128x256x16)
+//                 UMMAs per 64-wide K block into one of two 256-column
+//                 fp32 accumulators (double buffered across tiles)
+//   warps 2-3     idle
+//   warps 4-11    epilogue: tcgen05.ld 32 columns at a time, fused
+//                 bias / GeLU / GeLU' / conversion, vectorised global stores;
+//                 warp w reads TMEM lanes 32*(w%4).. and column half (w-4)/4.
+//
+// Shared-memory operand layouts are the canonical 128-byte-swizzled ones:
+//   K-major tile  : rows of 64 K-elements (128 B), 8-row atoms of 1 KiB,
+//                   stride-dimension offset 1 KiB; the K step of one UMMA
+//                   (16 elements = 32 B) advances the start address.
+//   MN-major tile : 64-element MN chunks (128 B) x BK K-rows, one TMA box
+//                   per chunk; leading-dimension offset = chunk pitch
+//                   (BK * 128 B), stride-dimension offset = 8 K-rows (1 KiB);
+//                   the K step advances the start address by 16 rows (2 KiB).
+#pragma once
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tpmlp {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_TILE_BYTES = BM * BK * 2;  // 16 KiB
+constexpr int B_TILE_BYTES = BN * BK * 2;  // 32 KiB
+constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
+constexpr int MN_CHUNK_BYTES = BK * 128;   // one 64-wide MN chunk of an MN-major tile
+constexpr int NUM_THREADS = 384;
+constexpr int FIRST_EPI_WARP = 4;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr uint32_t TMEM_COLS = 512;        // two 256-column fp32 accumulators
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + BAR_BYTES;
+
+#ifndef TPMLP_MN_LBO_BYTES
+#define TPMLP_MN_LBO_BYTES MN_CHUNK_BYTES
+#endif
+#ifndef TPMLP_MN_SBO_BYTES
+#define TPMLP_MN_SBO_BYTES 1024
+#endif
+
+struct KArgs {
+    int M, N, K;
+    int n_shards, sum_shards, a_batched, b_batched;
+    int m_blocks, n_blocks, batch, num_tiles, kb_per_shard, k_iters, group_m;
+    int act, out_f32;
+    void* out; long long out_ld, out_ss;
+    void* out2; long long out2_ld, out2_ss;
+    const void* bias; long long bias_ss;
+    const void* aux; long long aux_ld, aux_ss;
+    uint32_t* status;
+    unsigned long long timeout_ns;
+};
+
+__device__ __forceinline__ void decode_tile(const KArgs& p, int t, int& mb, int& nb, int& shard) {
+    const int n_total = p.batch * p.n_blocks;
+    const int per_group = p.group_m * n_total;
+    const int g = t / per_group;
+    const int first_m = g * p.group_m;
+    const int gm = min(p.m_blocks - first_m, p.group_m);
+    const int r = t - g * per_group;
+    mb = first_m + r % gm;
+    const int nbg = r / gm;
+    shard = nbg / p.n_blocks;
+    nb = nbg - shard * p.n_blocks;
+}
+
+__device__ __forceinline__ float gelu_erf(float x) {
+    return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+}
+__device__ __forceinline__ float gelu_erf_grad(float x) {
+    return 0.5f * (1.0f + erff(x * 0.70710678118654752f)) + x * 0.39894228040143268f * expf(-0.5f * x * x);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* f) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// Store 32 values (nvalid is a multiple of 8) as bf16.
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v, int nvalid) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        if (g * 8 < nvalid) {
+            uint4 u;
+            u.x = pack_bf16x2(v[g * 8 + 0], v[g * 8 + 1]);
+            u.y = pack_bf16x2(v[g * 8 + 2], v[g * 8 + 3]);
+            u.z = pack_bf16x2(v[g * 8 + 4], v[g * 8 + 5]);
+            u.w = pack_bf16x2(v[g * 8 + 6], v[g * 8 + 7]);
+            *reinterpret_cast<uint4*>(dst + g * 8) = u;
+        }
+    }
+}
+__device__ __forceinline__ void store_f32x32(float* dst, const float* v, int nvalid) {
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        if (g * 4 < nvalid) {
+            *reinterpret_cast<float4*>(dst + g * 4) = make_float4(v[g * 4], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]);
+        }
+    }
+}
+
+template <int EPI>
+__device__ __forceinline__ void epilogue_chunk(const KArgs& p, const uint32_t (&r)[32], int gm, int gn0, int shard) {
+    if (gm >= p.M) return;
+    const int nvalid = p.N - gn0;
+    if (nvalid <= 0) return;
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+    if constexpr (EPI == EPI_BIAS_ACT) {
+        if (p.bias != nullptr) {
+            const __nv_bfloat16* bp = static_cast<const __nv_bfloat16*>(p.bias) + shard * p.bias_ss + gn0;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                if (g * 8 < nvalid) {
+                    float bf[8];
+                    unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(bp + g * 8)), bf);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[g * 8 + i] += bf[i];
+                }
+            }
+        }
+        if (p.out2 != nullptr) {
+            __nv_bfloat16* d2 = static_cast<__nv_bfloat16*>(p.out2) + shard * p.out2_ss + (long long)gm * p.out2_ld + gn0;
+            store_bf16x32(d2, v, nvalid);
+        }
+        if (p.act == TPMLP_ACT_GELU_ERF) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
+        }
+        __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.out) + shard * p.out_ss + (long long)gm * p.out_ld + gn0;
+        store_bf16x32(d, v, nvalid);
+    } else if constexpr (EPI == EPI_DGELU) {
+        const __nv_bfloat16* hp =
+            static_cast<const __nv_bfloat16*>(p.aux) + shard * p.aux_ss + (long long)gm * p.aux_ld + gn0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            if (g * 8 < nvalid) {
+                float hv[8];
+                unpack_bf16x8(*reinterpret_cast<const uint4*>(hp + g * 8), hv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[g * 8 + i] *= gelu_erf_grad(hv[i]);
+            }
+        }
+        __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.out) + shard * p.out_ss + (long long)gm * p.out_ld + gn0;
+        store_bf16x32(d, v, nvalid);
+    } else {
+        if (p.out_f32) {
+            float* d = static_cast<float*>(p.out) + shard * p.out_ss + (long long)gm * p.out_ld + gn0;
+            store_f32x32(d, v, nvalid);
+        } else {
+            __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.out) + shard * p.out_ss + (long long)gm * p.out_ld + gn0;
+            store_bf16x32(d, v, nvalid);
+        }
+    }
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * A_TILE_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull + a, 1);
+            mbar_init(tempty + a, NUM_EPI_WARPS);
+        }
+        mbar_init(drain, 1);
+        fence_mbarrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------------ producer
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0;        // bit s: stage s has been armed at least once
+            uint32_t last_parity = 0;  // bit s: parity of the phase last armed on stage s
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+                int mb, nb, shard;
+                decode_tile(p, t, mb, nb, shard);
+                for (int it = 0; it < p.k_iters; ++it) {
+                    int ks, kb;
+                    if (p.sum_shards) {
+                        ks = it / p.kb_per_shard;
+                        kb = it - ks * p.kb_per_shard;
+                    } else {
+                        ks = shard;
+                        kb = it;
+                    }
+                    const int sa = p.sum_shards ? ks : (p.a_batched ? shard : 0);
+                    const int sb = p.sum_shards ? ks : (p.b_batched ? shard : 0);
+                    if (!mbar_wait_bounded(empty + stage, phase ^ 1u, p.status, p.timeout_ns, kWhereProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full + stage, STAGE_BYTES);
+                    armed |= 1u << stage;
+                    last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                    uint8_t* a_dst = sA + stage * A_TILE_BYTES;
+                    uint8_t* b_dst = sB + stage * B_TILE_BYTES;
+                    const int k0 = kb * BK;
+                    if constexpr (!A_MN) {
+                        tma_load_3d(a_dst, &tmA, full + stage, k0, mb * BM, sa);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < BM / 64; ++c)
+                            tma_load_3d(a_dst + c * MN_CHUNK_BYTES, &tmA, full + stage, mb * BM + c * 64, k0, sa);
+                    }
+                    if constexpr (!B_MN) {
+                        tma_load_3d(b_dst, &tmB, full + stage, k0, nb * BN, sb);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < BN / 64; ++c)
+                            tma_load_3d(b_dst + c * MN_CHUNK_BYTES, &tmB, full + stage, nb * BN + c * 64, k0, sb);
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Let every copy already issued land before the CTA can exit.
+                for (int s = 0; s < STAGES; ++s)
+                    if (armed & (1u << s))
+                        mbar_wait_bounded(full + s, (last_parity >> s) & 1u, p.status, p.timeout_ns, kWhereDrain,
+                                          /*watch_status=*/false);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------------------ MMA issuer
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int lt = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++lt) {
+                const int acc = lt & 1;
+                const uint32_t acc_phase = (lt >> 1) & 1;
+                if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, p.status, p.timeout_ns, kWhereMma)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int it = 0; it < p.k_iters; ++it) {
+                    if (!mbar_wait_bounded(full + stage, phase, p.status, p.timeout_ns, kWhereMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(sA + stage * A_TILE_BYTES);
+                    const uint32_t b_base = smem_u32(sB + stage * B_TILE_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        uint64_t adesc, bdesc;
+                        if constexpr (!A_MN) adesc = sdesc_sw128(a_base + kk * 32, 16, 1024);
+                        else adesc = sdesc_sw128(a_base + kk * 2048, TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES);
+                        if constexpr (!B_MN) bdesc = sdesc_sw128(b_base + kk * 32, 16, 1024);
+                        else bdesc = sdesc_sw128(b_base + kk * 2048, TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES);
+                        umma_f16(d_tmem, adesc, bdesc, idesc, (it | kk) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(empty + stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) umma_commit(tfull + acc);
+            }
+            // Every UMMA issued by this thread has completed once `drain` flips.
+            umma_commit(drain);
+            mbar_wait_bounded(drain, 0, p.status, p.timeout_ns, kWhereDrain, /*watch_status=*/false);
+        }
+    } else if (warp >= FIRST_EPI_WARP) {
+        // ---------------------------------------------------------------- epilogue
+        const int q = warp & 3;                        // TMEM lane quarter of this warp
+        const int half = (warp - FIRST_EPI_WARP) >> 2;  // column half of the tile
+        int lt = 0;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++lt) {
+            const int acc = lt & 1;
+            const uint32_t acc_phase = (lt >> 1) & 1;
+            int okw = 0;
+            if (lane == 0) okw = mbar_wait_bounded(tfull + acc, acc_phase, p.status, p.timeout_ns, kWhereEpilogue);
+            okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+            if (!okw) break;
+            tc_fence_after();
+            int mb, nb, shard;
+            decode_tile(p, t, mb, nb, shard);
+            const int gm = mb * BM + q * 32 + lane;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                const int col = half * 128 + c * 32;
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_row + col, r);
+                tmem_ld_wait();
+                epilogue_chunk<EPI>(p, r, gm, nb * BN + col, shard);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty + acc);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace tc
+}  // namespace tpmlp

@@ -1,0 +1,72 @@
+// Internal interfaces between the C-ABI front end (tpmlp_api.cu) and the
+// kernel translation units.  Not part of the public header.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/tpmlp.h"
+
+namespace tpmlp {
+
+// Epilogue kinds of the GEMM kernels.
+enum EpiKind : int {
+    EPI_BIAS_ACT = 0,  // out = act(acc + bias[n]); optional out2 = acc + bias (pre-activation)
+    EPI_DGELU = 1,     // out = acc * GeLU'(aux[m][n])
+    EPI_STORE = 2,     // out = acc (fp32 or bf16)
+};
+
+// One operand of D[M,N] = sum_k A[M,K] B[K,N], batched over shards.
+//   Element (row r, col c) of a [rows, cols] row-major slice of shard s lives at
+//   ptr + s * ss + r * ld + c  (element units).
+//   For A: "K-major" means the slice is [M][K] (K contiguous), "MN-major" [K][M].
+//   For B: "K-major" means the slice is [N][K], "MN-major" [K][N].
+struct Operand {
+    const void* ptr;
+    int64_t ld;       // row pitch (elements)
+    int64_t ss;       // shard stride (elements)
+    int64_t shards;   // number of shards stored (1 = not sharded)
+    bool mn_major;
+};
+
+// Everything the GEMM kernels need besides the two operands.
+struct GemmSpec {
+    int64_t M, N, K;     // per-shard GEMM sizes
+    int64_t n_shards;    // batch count (batched) or K-chunk count (sum_shards)
+    bool sum_shards;     // true: D = sum_s A_s B_s in one accumulator; false: D_s = A_s B_s
+    bool a_batched, b_batched;  // batched mode: operand follows the tile's shard (else shard 0)
+    int epi;             // EpiKind
+    int act;             // tpmlp_act (EPI_BIAS_ACT)
+    bool out_f32;        // output element type (bf16 otherwise)
+    void* out; int64_t out_ld, out_ss;
+    void* out2; int64_t out2_ld, out2_ss;         // pre-activation save (EPI_BIAS_ACT), may be null
+    const void* bias; int64_t bias_ss;            // [shard][N] of the input dtype, may be null
+    const void* aux; int64_t aux_ld, aux_ss;      // EPI_DGELU: H
+};
+
+struct DeviceInfo {
+    int device;
+    int sm_count;
+    int cc_major, cc_minor;
+    uint32_t* status;  // device address of this device's status word
+};
+
+// Per-device cached properties; nullptr (with last error set) on failure.
+const DeviceInfo* device_info();
+
+void set_error(const char* fmt, ...);
+
+// Kernel launchers (all return TPMLP_OK or TPMLP_ERR_CUDA with the message set).
+tpmlp_status launch_tc_gemm(const Operand& a, const Operand& b, const GemmSpec& g, const DeviceInfo& dev,
+                            cudaStream_t st);
+tpmlp_status launch_simt_gemm(const Operand& a, const Operand& b, const GemmSpec& g, const DeviceInfo& dev,
+                              cudaStream_t st);
+// out[s][n] = sum_m in[s][m][n]; in bf16 or f32 (in_f32), out f32 or bf16 (out_f32)
+tpmlp_status launch_colsum(const void* in, bool in_f32, int64_t shards, int64_t M, int64_t N, void* out,
+                           bool out_f32, cudaStream_t st);
+tpmlp_status launch_shard_columns(const void* src, void* dst, int64_t rows, int64_t cols, int p, int esize,
+                                  bool inverse, cudaStream_t st);
+tpmlp_status launch_qkv_interleave(const void* src, void* dst, int64_t rows, int64_t h, int64_t n_heads,
+                                   int esize, bool inverse, cudaStream_t st);
+tpmlp_status launch_debug_wait(uint32_t timeout_us, uint32_t* status, cudaStream_t st);
+
+}  // namespace tpmlp

@@ -1,0 +1,271 @@
+// fp32 FMA GEMM (the fp32 path: no TF32, so results stay within fp32 rounding),
+// column sums for the bias gradients, bit-exact layout copies and the
+// bounded-wait test hook.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tpmlp {
+namespace {
+
+// ------------------------------------------------------------------ fp32 GEMM
+struct SimtArgs {
+    int M, N, K, n_shards, sum_shards, a_batched, b_batched;
+    const float* a; long long a_ld, a_ss; int a_mn;
+    const float* b; long long b_ld, b_ss; int b_mn;
+    int epi, act;
+    float* out; long long out_ld, out_ss;
+    float* out2; long long out2_ld, out2_ss;
+    const float* bias; long long bias_ss;
+    const float* aux; long long aux_ld, aux_ss;
+};
+
+constexpr int ST = 64, SK = 16;
+
+__device__ __forceinline__ float gelu_f(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
+__device__ __forceinline__ float gelu_grad_f(float x) {
+    return 0.5f * (1.0f + erff(x * 0.70710678118654752f)) + x * 0.39894228040143268f * expf(-0.5f * x * x);
+}
+
+__global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtArgs p) {
+    __shared__ float sa[SK][ST + 1];
+    __shared__ float sb[SK][ST + 1];
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int n0 = blockIdx.x * ST, m0 = blockIdx.y * ST;
+    const int shard = p.sum_shards ? 0 : blockIdx.z;
+    float acc[4][4] = {};
+    const int n_k_shards = p.sum_shards ? p.n_shards : 1;
+    for (int ksh = 0; ksh < n_k_shards; ++ksh) {
+        const int sa_idx = p.sum_shards ? ksh : (p.a_batched ? shard : 0);
+        const int sb_idx = p.sum_shards ? ksh : (p.b_batched ? shard : 0);
+        const float* A = p.a + sa_idx * p.a_ss;
+        const float* B = p.b + sb_idx * p.b_ss;
+        for (int k0 = 0; k0 < p.K; k0 += SK) {
+            for (int i = threadIdx.x; i < SK * ST; i += 256) {
+                const int kk = i / ST, mm = i % ST;
+                const int gm = m0 + mm, gk = k0 + kk;
+                float va = 0.f;
+                if (gm < p.M && gk < p.K) va = p.a_mn ? A[(long long)gk * p.a_ld + gm] : A[(long long)gm * p.a_ld + gk];
+                sa[kk][mm] = va;
+                const int gn = n0 + mm;
+                float vb = 0.f;
+                if (gn < p.N && gk < p.K) vb = p.b_mn ? B[(long long)gk * p.b_ld + gn] : B[(long long)gn * p.b_ld + gk];
+                sb[kk][mm] = vb;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int kk = 0; kk < SK; ++kk) {
+                float ra[4], rb[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) ra[i] = sa[kk][ty * 4 + i];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) rb[j] = sb[kk][tx * 4 + j];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(ra[i], rb[j], acc[i][j]);
+            }
+            __syncthreads();
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int gm = m0 + ty * 4 + i;
+        if (gm >= p.M) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int gn = n0 + tx * 4 + j;
+            if (gn >= p.N) continue;
+            float v = acc[i][j];
+            if (p.epi == EPI_BIAS_ACT) {
+                if (p.bias) v += p.bias[shard * p.bias_ss + gn];
+                if (p.out2) p.out2[shard * p.out2_ss + (long long)gm * p.out2_ld + gn] = v;
+                if (p.act == TPMLP_ACT_GELU_ERF) v = gelu_f(v);
+            } else if (p.epi == EPI_DGELU) {
+                v *= gelu_grad_f(p.aux[shard * p.aux_ss + (long long)gm * p.aux_ld + gn]);
+            }
+            p.out[shard * p.out_ss + (long long)gm * p.out_ld + gn] = v;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ column sums
+// out[s][n] = sum_m in[s][m][n], rows summed in a fixed order (deterministic).
+template <bool IN_F32, bool OUT_F32>
+__global__ void __launch_bounds__(256) colsum_kernel(const void* in, long long M, long long N, void* out) {
+    __shared__ float part[8][64];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const long long s = blockIdx.y;
+    const long long c = (long long)blockIdx.x * 64 + tx * 2;
+    float a0 = 0.f, a1 = 0.f;
+    if (c < N) {
+        for (long long m = ty; m < M; m += 8) {
+            const long long off = (s * M + m) * N + c;
+            if (IN_F32) {
+                const float2 v = *reinterpret_cast<const float2*>(static_cast<const float*>(in) + off);
+                a0 += v.x;
+                a1 += v.y;
+            } else {
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(in) + off);
+                a0 += __uint_as_float(w << 16);
+                a1 += __uint_as_float(w & 0xFFFF0000u);
+            }
+        }
+    }
+    part[ty][tx * 2] = a0;
+    part[ty][tx * 2 + 1] = a1;
+    __syncthreads();
+    if (ty == 0 && c < N) {
+        float r0 = 0.f, r1 = 0.f;
+        for (int i = 0; i < 8; ++i) {
+            r0 += part[i][tx * 2];
+            r1 += part[i][tx * 2 + 1];
+        }
+        if (OUT_F32) {
+            float* o = static_cast<float*>(out) + s * N + c;
+            o[0] = r0;
+            o[1] = r1;
+        } else {
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out) + s * N + c;
+            o[0] = __float2bfloat16_rn(r0);
+            o[1] = __float2bfloat16_rn(r1);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ layouts
+// Column shard: dst[i][r][c] = src[r][i*cs + c] in 16-byte units (rows of cs*esize bytes).
+__global__ void shard_columns_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long rows,
+                                     long long units_per_row /*cols*esize/16*/, long long units_per_shard_row,
+                                     int p, int inverse) {
+    const long long total = rows * units_per_row;
+    for (long long u = blockIdx.x * (long long)blockDim.x + threadIdx.x; u < total;
+         u += (long long)gridDim.x * blockDim.x) {
+        // u enumerates the sharded layout: (i, r, cu)
+        const long long per_shard = rows * units_per_shard_row;
+        const long long i = u / per_shard;
+        const long long rem = u - i * per_shard;
+        const long long r = rem / units_per_shard_row;
+        const long long cu = rem - r * units_per_shard_row;
+        const long long unsharded = r * units_per_row + i * units_per_shard_row + cu;
+        if (!inverse) dst[u] = src[unsharded];
+        else dst[unsharded] = src[u];
+    }
+    (void)p;
+}
+
+__device__ __forceinline__ long long qkv_src_col_dev(long long dst_col, long long h, long long d) {
+    const long long blk = dst_col / d, e = dst_col - blk * d;
+    const long long g = blk / 3, t = blk - g * 3;
+    return t * h + g * d + e;
+}
+
+template <typename T>
+__global__ void qkv_kernel(const T* __restrict__ src, T* __restrict__ dst, long long rows, long long cols_units,
+                           long long h_units, long long d_units, int inverse) {
+    const long long total = rows * cols_units;
+    for (long long u = blockIdx.x * (long long)blockDim.x + threadIdx.x; u < total;
+         u += (long long)gridDim.x * blockDim.x) {
+        const long long r = u / cols_units, c = u - r * cols_units;
+        const long long sc = qkv_src_col_dev(c, h_units, d_units);
+        if (!inverse) dst[u] = src[r * cols_units + sc];
+        else dst[r * cols_units + sc] = src[u];
+    }
+}
+
+// ------------------------------------------------------------------ bounded-wait hook
+__global__ void debug_wait_kernel(uint32_t* status, unsigned long long timeout_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbarrier_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0) {
+        // Nothing ever arrives on `bar`: the wait must give up on its own.
+        mbar_wait_bounded(&bar, 0, status, timeout_ns, kWhereDebug, /*watch_status=*/false);
+    }
+}
+
+int grid_for(long long work, int block) {
+    long long g = (work + block - 1) / block;
+    if (g > 152 * 16) g = 152 * 16;
+    if (g < 1) g = 1;
+    return static_cast<int>(g);
+}
+
+tpmlp_status check_launch(const char* what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("%s launch: %s", what, cudaGetErrorString(e));
+        return TPMLP_ERR_CUDA;
+    }
+    return TPMLP_OK;
+}
+
+}  // namespace
+
+tpmlp_status launch_simt_gemm(const Operand& a, const Operand& b, const GemmSpec& g, const DeviceInfo& dev,
+                              cudaStream_t st) {
+    (void)dev;
+    SimtArgs p{};
+    p.M = (int)g.M; p.N = (int)g.N; p.K = (int)g.K;
+    p.n_shards = (int)g.n_shards; p.sum_shards = g.sum_shards; p.a_batched = g.a_batched; p.b_batched = g.b_batched;
+    p.a = static_cast<const float*>(a.ptr); p.a_ld = a.ld; p.a_ss = a.ss; p.a_mn = a.mn_major;
+    p.b = static_cast<const float*>(b.ptr); p.b_ld = b.ld; p.b_ss = b.ss; p.b_mn = b.mn_major;
+    p.epi = g.epi; p.act = g.act;
+    p.out = static_cast<float*>(g.out); p.out_ld = g.out_ld; p.out_ss = g.out_ss;
+    p.out2 = static_cast<float*>(g.out2); p.out2_ld = g.out2_ld; p.out2_ss = g.out2_ss;
+    p.bias = static_cast<const float*>(g.bias); p.bias_ss = g.bias_ss;
+    p.aux = static_cast<const float*>(g.aux); p.aux_ld = g.aux_ld; p.aux_ss = g.aux_ss;
+    dim3 grid((unsigned)((g.N + ST - 1) / ST), (unsigned)((g.M + ST - 1) / ST), (unsigned)(g.sum_shards ? 1 : g.n_shards));
+    simt_gemm_kernel<<<grid, 256, 0, st>>>(p);
+    return check_launch("fp32 GEMM");
+}
+
+tpmlp_status launch_colsum(const void* in, bool in_f32, int64_t shards, int64_t M, int64_t N, void* out, bool out_f32,
+                           cudaStream_t st) {
+    dim3 grid((unsigned)((N + 63) / 64), (unsigned)shards);
+    if (in_f32 && out_f32) colsum_kernel<true, true><<<grid, 256, 0, st>>>(in, M, N, out);
+    else if (in_f32) colsum_kernel<true, false><<<grid, 256, 0, st>>>(in, M, N, out);
+    else if (out_f32) colsum_kernel<false, true><<<grid, 256, 0, st>>>(in, M, N, out);
+    else colsum_kernel<false, false><<<grid, 256, 0, st>>>(in, M, N, out);
+    return check_launch("column sum");
+}
+
+tpmlp_status launch_shard_columns(const void* src, void* dst, int64_t rows, int64_t cols, int p, int esize,
+                                  bool inverse, cudaStream_t st) {
+    const long long upr = cols * esize / 16, upsr = upr / p;
+    const long long total = rows * upr;
+    shard_columns_kernel<<<grid_for(total, 256), 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
+                                                               rows, upr, upsr, p, inverse ? 1 : 0);
+    return check_launch("column shard");
+}
+
+tpmlp_status launch_qkv_interleave(const void* src, void* dst, int64_t rows, int64_t h, int64_t n_heads, int esize,
+                                   bool inverse, cudaStream_t st) {
+    const long long d = h / n_heads;
+    const long long cols = 3 * h;
+    if ((d * esize) % 16 == 0) {
+        const long long k = 16 / esize;  // elements per unit
+        const long long total = rows * (cols / k);
+        qkv_kernel<uint4><<<grid_for(total, 256), 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
+                                                               rows, cols / k, h / k, d / k, inverse ? 1 : 0);
+    } else if (esize == 2) {
+        qkv_kernel<uint16_t><<<grid_for(rows * cols, 256), 256, 0, st>>>(
+            static_cast<const uint16_t*>(src), static_cast<uint16_t*>(dst), rows, cols, h, d, inverse ? 1 : 0);
+    } else {
+        qkv_kernel<uint32_t><<<grid_for(rows * cols, 256), 256, 0, st>>>(
+            static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst), rows, cols, h, d, inverse ? 1 : 0);
+    }
+    return check_launch("QKV interleave");
+}
+
+tpmlp_status launch_debug_wait(uint32_t timeout_us, uint32_t* status, cudaStream_t st) {
+    debug_wait_kernel<<<1, 32, 0, st>>>(status, static_cast<unsigned long long>(timeout_us) * 1000ull);
+    return check_launch("debug wait");
+}
+
+}  // namespace tpmlp

@@ -1,0 +1,500 @@
+// C-ABI front end: argument validation (host only, before any CUDA call),
+// per-device state, and the mapping of each entry point onto GEMM launches.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tpmlp {
+
+// Device status word: written by kernels whose bounded waits give up.
+__device__ uint32_t g_status_word;
+
+namespace {
+thread_local char t_err[512] = "";
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ok[kMaxDevices];
+std::mutex g_dev_mu;
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+int esize(tpmlp_dtype dt) { return dt == TPMLP_F32 ? 4 : 2; }
+
+struct Range {
+    const void* p;
+    int64_t bytes;
+};
+
+bool overlap(const Range& a, const Range& b) {
+    if (!a.p || !b.p || a.bytes <= 0 || b.bytes <= 0) return false;
+    auto a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + static_cast<uintptr_t>(b.bytes) && b0 < a0 + static_cast<uintptr_t>(a.bytes);
+}
+
+// Outputs must not overlap inputs or each other.
+tpmlp_status check_alias(std::initializer_list<Range> outs, std::initializer_list<Range> ins) {
+    int i = 0;
+    for (const Range& o : outs) {
+        for (const Range& in : ins)
+            if (overlap(o, in)) {
+                set_error("output %d overlaps an input", i);
+                return TPMLP_ERR_ALIAS;
+            }
+        int j = 0;
+        for (const Range& o2 : outs) {
+            if (j > i && overlap(o, o2)) {
+                set_error("outputs %d and %d overlap", i, j);
+                return TPMLP_ERR_ALIAS;
+            }
+            ++j;
+        }
+        ++i;
+    }
+    return TPMLP_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+tpmlp_status check_aligned(std::initializer_list<const void*> ptrs) {
+    int i = 0;
+    for (const void* p : ptrs) {
+        if (p && !aligned16(p)) {
+            set_error("pointer argument %d is not 16-byte aligned", i);
+            return TPMLP_ERR_ALIGNMENT;
+        }
+        ++i;
+    }
+    return TPMLP_OK;
+}
+
+tpmlp_status check_pitch(int64_t elems, tpmlp_dtype dt, const char* what) {
+    if ((elems * esize(dt)) % 16 != 0) {
+        set_error("%s = %lld elements is not a multiple of 16 bytes", what, (long long)elems);
+        return TPMLP_ERR_ALIGNMENT;
+    }
+    return TPMLP_OK;
+}
+
+// Common shape checks of the MLP entry points.
+tpmlp_status check_mlp_shape(int64_t s, int64_t b, int64_t h, int64_t ffn, int p, bool need_h_div) {
+    if (s < 0 || b < 0 || h < 1 || ffn < 1 || p < 1) {
+        set_error("bad shape: s=%lld b=%lld h=%lld ffn=%lld p=%d", (long long)s, (long long)b, (long long)h,
+                  (long long)ffn, p);
+        return TPMLP_ERR_SHAPE;
+    }
+    if (h > kMaxDim || ffn > kMaxDim || (b > 0 && s > kMaxDim / b)) {
+        set_error("shape too large: s*b, h and ffn must each be below 2^31");
+        return TPMLP_ERR_SHAPE;
+    }
+    if (ffn % p != 0) {
+        set_error("ffn=%lld is not divisible by p=%d", (long long)ffn, p);
+        return TPMLP_ERR_DIVISIBILITY;
+    }
+    if (need_h_div && h % p != 0) {
+        set_error("h=%lld is not divisible by p=%d", (long long)h, p);
+        return TPMLP_ERR_DIVISIBILITY;
+    }
+    return TPMLP_OK;
+}
+
+tpmlp_status check_dtype(tpmlp_dtype dt) {
+    if (dt != TPMLP_BF16 && dt != TPMLP_F32) {
+        set_error("unknown dtype %d", (int)dt);
+        return TPMLP_ERR_DTYPE;
+    }
+    return TPMLP_OK;
+}
+
+#define TP_TRY(expr)                          \
+    do {                                      \
+        tpmlp_status _st = (expr);            \
+        if (_st != TPMLP_OK) return _st;      \
+    } while (0)
+
+tpmlp_status get_device(const DeviceInfo** out) {
+    const DeviceInfo* d = device_info();
+    if (!d) return TPMLP_ERR_CUDA;
+    if (d->cc_major != 10 || d->cc_minor != 3) {
+        set_error("device %d has compute capability %d.%d; this library is built for sm_103a (10.3) only", d->device,
+                  d->cc_major, d->cc_minor);
+        return TPMLP_ERR_ARCH;
+    }
+    *out = d;
+    return TPMLP_OK;
+}
+
+tpmlp_status run_gemm(const Operand& a, const Operand& b, const GemmSpec& g, tpmlp_dtype dt, const DeviceInfo& dev,
+                      cudaStream_t st) {
+    if (dt == TPMLP_BF16) return launch_tc_gemm(a, b, g, dev, st);
+    return launch_simt_gemm(a, b, g, dev, st);
+}
+
+GemmSpec spec_base() {
+    GemmSpec g;
+    std::memset(&g, 0, sizeof(g));
+    return g;
+}
+
+// Column layer (validated arguments).  One launch over all p shards.
+tpmlp_status do_column(const void* X, const void* A_sh, const void* b1_sh, void* Y_sh, void* H_sh, int64_t M,
+                       int64_t h, int64_t ffn, int p, tpmlp_dtype dt, int act, const DeviceInfo& dev,
+                       cudaStream_t st) {
+    const int64_t fs = ffn / p;
+    Operand a{X, h, 0, 1, false};                     // X [M][h], K-major
+    Operand b{A_sh, fs, h * fs, p, true};             // A_i [h][fs]: [K][N], MN-major
+    GemmSpec g = spec_base();
+    g.M = M; g.N = fs; g.K = h; g.n_shards = p;
+    g.sum_shards = false; g.a_batched = false; g.b_batched = true;
+    g.epi = EPI_BIAS_ACT; g.act = act;
+    g.out = Y_sh; g.out_ld = fs; g.out_ss = M * fs;
+    g.out2 = H_sh; g.out2_ld = fs; g.out2_ss = M * fs;
+    g.bias = b1_sh; g.bias_ss = fs;
+    return run_gemm(a, b, g, dt, dev, st);
+}
+
+// Row layer with the shard sum in the K loop.
+tpmlp_status do_row(const void* Y_sh, const void* B_sh, const void* b2, void* Z, int64_t M, int64_t h, int64_t ffn,
+                    int p, tpmlp_dtype dt, const DeviceInfo& dev, cudaStream_t st) {
+    const int64_t fs = ffn / p;
+    Operand a{Y_sh, fs, M * fs, p, false};            // Y_i [M][fs], K-major
+    Operand b{B_sh, h, fs * h, p, true};              // B_i [fs][h]: [K][N], MN-major
+    GemmSpec g = spec_base();
+    g.M = M; g.N = h; g.K = fs; g.n_shards = p;
+    g.sum_shards = true;
+    g.epi = EPI_BIAS_ACT; g.act = TPMLP_ACT_NONE;
+    g.out = Z; g.out_ld = h; g.out_ss = 0;
+    g.bias = b2; g.bias_ss = 0;
+    return run_gemm(a, b, g, dt, dev, st);
+}
+
+}  // namespace
+
+void set_error(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(t_err, sizeof(t_err), fmt, ap);
+    va_end(ap);
+}
+
+const DeviceInfo* device_info() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        set_error("cudaGetDevice: %s", cudaGetErrorString(e));
+        return nullptr;
+    }
+    if (dev < 0 || dev >= kMaxDevices) {
+        set_error("device index %d out of range", dev);
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_dev_ok[dev]) {
+        DeviceInfo d{};
+        d.device = dev;
+        if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) {
+            set_error("cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+            return nullptr;
+        }
+        if (d.cc_major == 10 && d.cc_minor == 3) {
+            void* addr = nullptr;
+            if ((e = cudaGetSymbolAddress(&addr, g_status_word)) != cudaSuccess) {
+                set_error("cudaGetSymbolAddress(status word): %s", cudaGetErrorString(e));
+                return nullptr;
+            }
+            d.status = static_cast<uint32_t*>(addr);
+        }
+        g_dev[dev] = d;
+        g_dev_ok[dev] = true;
+    }
+    return &g_dev[dev];
+}
+
+}  // namespace tpmlp
+
+using namespace tpmlp;
+
+extern "C" {
+
+tpmlp_status tpmlp_column_fwd(const void* X, const void* A_sh, const void* b1_sh, void* Y_sh, void* H_sh, int64_t s,
+                              int64_t b, int64_t h, int64_t ffn, int p, tpmlp_dtype dt, tpmlp_act act, void* stream) {
+    if (!X || !A_sh || !Y_sh) {
+        set_error("X, A_sh and Y_sh must not be NULL");
+        return TPMLP_ERR_NULL;
+    }
+    TP_TRY(check_mlp_shape(s, b, h, ffn, p, false));
+    TP_TRY(check_dtype(dt));
+    if (act != TPMLP_ACT_NONE && act != TPMLP_ACT_GELU_ERF) {
+        set_error("unknown activation %d", (int)act);
+        return TPMLP_ERR_DTYPE;
+    }
+    const int64_t M = s * b, fs = ffn / p, es = esize(dt);
+    TP_TRY(check_aligned({X, A_sh, b1_sh, Y_sh, H_sh}));
+    TP_TRY(check_pitch(h, dt, "h"));
+    TP_TRY(check_pitch(fs, dt, "ffn/p"));
+    TP_TRY(check_alias({{Y_sh, M * ffn * es}, {H_sh, M * ffn * es}},
+                       {{X, M * h * es}, {A_sh, h * ffn * es}, {b1_sh, ffn * es}}));
+    const DeviceInfo* dev;
+    TP_TRY(get_device(&dev));
+    if (M == 0) return TPMLP_OK;
+    return do_column(X, A_sh, b1_sh, Y_sh, H_sh, M, h, ffn, p, dt, act, *dev, static_cast<cudaStream_t>(stream));
+}
+
+tpmlp_status tpmlp_row_fwd(const void* Y_sh, const void* B_sh, const void* b2, void* Z, int64_t s, int64_t b,
+                           int64_t h, int64_t ffn, int p, tpmlp_dtype dt, void* stream) {
+    if (!Y_sh || !B_sh || !Z) {
+        set_error("Y_sh, B_sh and Z must not be NULL");
+        return TPMLP_ERR_NULL;
+    }
+    TP_TRY(check_mlp_shape(s, b, h, ffn, p, false));
+    TP_TRY(check_dtype(dt));
+    const int64_t M = s * b, fs = ffn / p, es = esize(dt);
+    TP_TRY(check_aligned({Y_sh, B_sh, b2, Z}));
+    TP_TRY(check_pitch(h, dt, "h"));
+    TP_TRY(check_pitch(fs, dt, "ffn/p"));
+    TP_TRY(check_alias({{Z, M * h * es}}, {{Y_sh, M * ffn * es}, {B_sh, ffn * h * es}, {b2, h * es}}));
+    const DeviceInfo* dev;
+    TP_TRY(get_device(&dev));
+    if (M == 0) return TPMLP_OK;
+    return do_row(Y_sh, B_sh, b2, Z, M, h, ffn, p, dt, *dev, static_cast<cudaStream_t>(stream));
+}
+
+tpmlp_status tpmlp_mlp_fwd(const void* X, const void* A_sh, const void* b1_sh, const void* B_sh, const void* b2,
+                           void* Z, void* Y_ws, void* H_sh, int64_t s, int64_t b, int64_t h, int64_t ffn, int p,
+                           tpmlp_dtype dt, void* stream) {
+    if (!X || !A_sh || !B_sh || !Z || !Y_ws) {
+        set_error("X, A_sh, B_sh, Z and Y_ws must not be NULL");
+        return TPMLP_ERR_NULL;
+    }
+    TP_TRY(check_mlp_shape(s, b, h, ffn, p, true));
+    TP_TRY(check_dtype(dt));
+    const int64_t M = s * b, fs = ffn / p, es = esize(dt);
+    TP_TRY(check_aligned({X, A_sh, b1_sh, B_sh, b2, Z, Y_ws, H_sh}));
+    TP_TRY(check_pitch(h, dt, "h"));
+    TP_TRY(check_pitch(fs, dt, "ffn/p"));
+    TP_TRY(check_alias({{Z, M * h * es}, {Y_ws, M * ffn * es}, {H_sh, M * ffn * es}},
+                       {{X, M * h * es}, {A_sh, h * ffn * es}, {b1_sh, ffn * es}, {B_sh, ffn * h * es},
+                        {b2, h * es}}));
+    const DeviceInfo* dev;
+    TP_TRY(get_device(&dev));
+    if (M == 0) return TPMLP_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    TP_TRY(do_column(X, A_sh, b1_sh, Y_ws, H_sh, M, h, ffn, p, dt, TPMLP_ACT_GELU_ERF, *dev, st));
+    return do_row(Y_ws, B_sh, b2, Z, M, h, ffn, p, dt, *dev, st);
+}
+
+tpmlp_status tpmlp_mlp_bwd(const void* X, const void* A_sh, const void* B_sh, const void* H_sh, const void* Y_sh,
+                           const void* dZ, void* dX, void* dA_sh, void* dB_sh, void* db1_sh, void* db2, void* dH_ws,
+                           int64_t s, int64_t b, int64_t h, int64_t ffn, int p, tpmlp_dtype dt, tpmlp_dtype grad_dt,
+                           void* stream) {
+    if (!X || !A_sh || !B_sh || !H_sh || !Y_sh || !dZ || !dX || !dA_sh || !dB_sh || !dH_ws) {
+        set_error("only db1_sh and db2 may be NULL");
+        return TPMLP_ERR_NULL;
+    }
+    TP_TRY(check_mlp_shape(s, b, h, ffn, p, true));
+    TP_TRY(check_dtype(dt));
+    TP_TRY(check_dtype(grad_dt));
+    if (dt == TPMLP_F32 && grad_dt != TPMLP_F32) {
+        set_error("grad_dt must be TPMLP_F32 when dt is TPMLP_F32");
+        return TPMLP_ERR_DTYPE;
+    }
+    const int64_t M = s * b, fs = ffn / p, es = esize(dt), gs = esize(grad_dt);
+    TP_TRY(check_aligned({X, A_sh, B_sh, H_sh, Y_sh, dZ, dX, dA_sh, dB_sh, db1_sh, db2, dH_ws}));
+    TP_TRY(check_pitch(h, dt, "h"));
+    TP_TRY(check_pitch(fs, dt, "ffn/p"));
+    TP_TRY(check_alias({{dX, M * h * es}, {dA_sh, h * ffn * gs}, {dB_sh, ffn * h * gs}, {db1_sh, ffn * gs},
+                        {db2, h * gs}, {dH_ws, M * ffn * es}},
+                       {{X, M * h * es}, {A_sh, h * ffn * es}, {B_sh, ffn * h * es}, {H_sh, M * ffn * es},
+                        {Y_sh, M * ffn * es}, {dZ, M * h * es}}));
+    const DeviceInfo* dev;
+    TP_TRY(get_device(&dev));
+    if (M == 0) return TPMLP_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool gf32 = grad_dt == TPMLP_F32;
+
+    // 1. dH_i = (dZ B_i^T) * GeLU'(H_i)
+    {
+        Operand a{dZ, h, 0, 1, false};               // dZ [M][h]: [M][K]
+        Operand bb{B_sh, h, fs * h, p, false};       // B_i [fs][h]: [N][K], K-major
+        GemmSpec g = spec_base();
+        g.M = M; g.N = fs; g.K = h; g.n_shards = p;
+        g.a_batched = false; g.b_batched = true;
+        g.epi = EPI_DGELU;
+        g.aux = H_sh; g.aux_ld = fs; g.aux_ss = M * fs;
+        g.out = dH_ws; g.out_ld = fs; g.out_ss = M * fs;
+        TP_TRY(run_gemm(a, bb, g, dt, *dev, st));
+    }
+    // 2. bias gradients (column sums)
+    if (db1_sh) TP_TRY(launch_colsum(dH_ws, dt == TPMLP_F32, p, M, fs, db1_sh, gf32, st));
+    if (db2) TP_TRY(launch_colsum(dZ, dt == TPMLP_F32, 1, M, h, db2, gf32, st));
+    // 3. dB_i = Y_i^T dZ   ([fs][h] per shard, K = tokens)
+    {
+        Operand a{Y_sh, fs, M * fs, p, true};        // Y_i [M][fs]: [K][M_gemm], MN-major
+        Operand bb{dZ, h, 0, 1, true};               // dZ [M][h]: [K][N], MN-major
+        GemmSpec g = spec_base();
+        g.M = fs; g.N = h; g.K = M; g.n_shards = p;
+        g.a_batched = true; g.b_batched = false;
+        g.epi = EPI_STORE; g.out_f32 = gf32;
+        g.out = dB_sh; g.out_ld = h; g.out_ss = fs * h;
+        TP_TRY(run_gemm(a, bb, g, dt, *dev, st));
+    }
+    // 4. dA_i = X^T dH_i   ([h][fs] per shard, K = tokens)
+    {
+        Operand a{X, h, 0, 1, true};                 // X [M][h]: [K][M_gemm], MN-major
+        Operand bb{dH_ws, fs, M * fs, p, true};      // dH_i [M][fs]: [K][N], MN-major
+        GemmSpec g = spec_base();
+        g.M = h; g.N = fs; g.K = M; g.n_shards = p;
+        g.a_batched = false; g.b_batched = true;
+        g.epi = EPI_STORE; g.out_f32 = gf32;
+        g.out = dA_sh; g.out_ld = fs; g.out_ss = h * fs;
+        TP_TRY(run_gemm(a, bb, g, dt, *dev, st));
+    }
+    // 5. dX = sum_i dH_i A_i^T   (shard sum in the K loop)
+    {
+        Operand a{dH_ws, fs, M * fs, p, false};      // dH_i [M][fs]: [M][K]
+        Operand bb{A_sh, fs, h * fs, p, false};      // A_i [h][fs]: [N][K], K-major
+        GemmSpec g = spec_base();
+        g.M = M; g.N = h; g.K = fs; g.n_shards = p;
+        g.sum_shards = true;
+        g.epi = EPI_STORE; g.out_f32 = (dt == TPMLP_F32);
+        g.out = dX; g.out_ld = h; g.out_ss = 0;
+        TP_TRY(run_gemm(a, bb, g, dt, *dev, st));
+    }
+    return TPMLP_OK;
+}
+
+static tpmlp_status shard_common(const void* src, void* dst, int64_t rows, int64_t cols, int p, tpmlp_dtype dt,
+                                 bool inverse, void* stream) {
+    if (!src || !dst) {
+        set_error("pointers must not be NULL");
+        return TPMLP_ERR_NULL;
+    }
+    if (rows < 0 || cols < 1 || p < 1 || rows > kMaxDim || cols > kMaxDim) {
+        set_error("bad shape rows=%lld cols=%lld p=%d", (long long)rows, (long long)cols, p);
+        return TPMLP_ERR_SHAPE;
+    }
+    if (cols % p != 0) {
+        set_error("cols=%lld is not divisible by p=%d", (long long)cols, p);
+        return TPMLP_ERR_DIVISIBILITY;
+    }
+    TP_TRY(check_dtype(dt));
+    TP_TRY(check_aligned({src, dst}));
+    TP_TRY(check_pitch(cols / p, dt, "cols/p"));
+    const int64_t bytes = rows * cols * esize(dt);
+    TP_TRY(check_alias({{dst, bytes}}, {{src, bytes}}));
+    const DeviceInfo* dev;
+    TP_TRY(get_device(&dev));
+    if (rows == 0) return TPMLP_OK;
+    return launch_shard_columns(src, dst, rows, cols, p, esize(dt), inverse, static_cast<cudaStream_t>(stream));
+}
+
+tpmlp_status tpmlp_shard_columns(const void* W, void* W_sh, int64_t rows, int64_t cols, int p, tpmlp_dtype dt,
+                                 void* stream) {
+    return shard_common(W, W_sh, rows, cols, p, dt, false, stream);
+}
+
+tpmlp_status tpmlp_unshard_columns(const void* W_sh, void* W, int64_t rows, int64_t cols, int p, tpmlp_dtype dt,
+                                   void* stream) {
+    return shard_common(W_sh, W, rows, cols, p, dt, true, stream);
+}
+
+tpmlp_status tpmlp_qkv_interleave(const void* W_qkv, void* W_out, int64_t rows, int64_t h, int64_t n_heads, int p,
+                                  tpmlp_dtype dt, int inverse, void* stream) {
+    if (!W_qkv || !W_out) {
+        set_error("pointers must not be NULL");
+        return TPMLP_ERR_NULL;
+    }
+    if (rows < 0 || h < 1 || n_heads < 1 || p < 1 || rows > kMaxDim || h > kMaxDim / 3) {
+        set_error("bad shape rows=%lld h=%lld n_heads=%lld p=%d", (long long)rows, (long long)h, (long long)n_heads, p);
+        return TPMLP_ERR_SHAPE;
+    }
+    if (h % n_heads != 0 || n_heads % p != 0) {
+        set_error("need h %% n_heads == 0 and n_heads %% p == 0 (h=%lld n_heads=%lld p=%d)", (long long)h,
+                  (long long)n_heads, p);
+        return TPMLP_ERR_DIVISIBILITY;
+    }
+    TP_TRY(check_dtype(dt));
+    TP_TRY(check_aligned({W_qkv, W_out}));
+    const int64_t bytes = rows * 3 * h * esize(dt);
+    TP_TRY(check_alias({{W_out, bytes}}, {{W_qkv, bytes}}));
+    const DeviceInfo* dev;
+    TP_TRY(get_device(&dev));
+    if (rows == 0) return TPMLP_OK;
+    return launch_qkv_interleave(W_qkv, W_out, rows, h, n_heads, esize(dt), inverse != 0,
+                                 static_cast<cudaStream_t>(stream));
+}
+
+int64_t tpmlp_qkv_src_col(int64_t dst_col, int64_t h, int64_t n_heads) {
+    if (h < 1 || n_heads < 1 || h % n_heads != 0 || dst_col < 0 || dst_col >= 3 * h) return -1;
+    const int64_t d = h / n_heads;
+    const int64_t blk = dst_col / d, e = dst_col % d;
+    return (blk % 3) * h + (blk / 3) * d + e;
+}
+
+tpmlp_status tpmlp_device_status(void* stream) {
+    const DeviceInfo* dev;
+    TP_TRY(get_device(&dev));
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        set_error("cudaStreamSynchronize: %s", cudaGetErrorString(e));
+        return TPMLP_ERR_CUDA;
+    }
+    uint32_t v = 0;
+    if ((e = cudaMemcpy(&v, dev->status, sizeof(v), cudaMemcpyDeviceToHost)) != cudaSuccess) {
+        set_error("reading the status word: %s", cudaGetErrorString(e));
+        return TPMLP_ERR_CUDA;
+    }
+    if (v == 0) return TPMLP_OK;
+    const uint32_t zero = 0;
+    if ((e = cudaMemcpy(dev->status, &zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess) {
+        set_error("clearing the status word: %s", cudaGetErrorString(e));
+        return TPMLP_ERR_CUDA;
+    }
+    if (v & kStatusTimeout) {
+        set_error("a device-side wait gave up (where=%u)", v & 0xFFFFu);
+        return TPMLP_ERR_TIMEOUT;
+    }
+    set_error("device status word 0x%x", v);
+    return TPMLP_ERR_DEVICE;
+}
+
+tpmlp_status tpmlp_debug_wait_timeout(uint32_t timeout_us, void* stream) {
+    if (timeout_us < 1 || timeout_us > 1000000) {
+        set_error("timeout_us must be in 1..1000000");
+        return TPMLP_ERR_SHAPE;
+    }
+    const DeviceInfo* dev;
+    TP_TRY(get_device(&dev));
+    return launch_debug_wait(timeout_us, dev->status, static_cast<cudaStream_t>(stream));
+}
+
+const char* tpmlp_status_string(tpmlp_status st) {
+    switch (st) {
+    case TPMLP_OK: return "TPMLP_OK";
+    case TPMLP_ERR_NULL: return "TPMLP_ERR_NULL";
+    case TPMLP_ERR_SHAPE: return "TPMLP_ERR_SHAPE";
+    case TPMLP_ERR_DIVISIBILITY: return "TPMLP_ERR_DIVISIBILITY";
+    case TPMLP_ERR_DTYPE: return "TPMLP_ERR_DTYPE";
+    case TPMLP_ERR_ALIGNMENT: return "TPMLP_ERR_ALIGNMENT";
+    case TPMLP_ERR_ALIAS: return "TPMLP_ERR_ALIAS";
+    case TPMLP_ERR_ARCH: return "TPMLP_ERR_ARCH";
+    case TPMLP_ERR_CUDA: return "TPMLP_ERR_CUDA";
+    case TPMLP_ERR_TIMEOUT: return "TPMLP_ERR_TIMEOUT";
+    case TPMLP_ERR_DEVICE: return "TPMLP_ERR_DEVICE";
+    }
+    return "TPMLP_ERR_UNKNOWN";
+}
+
+const char* tpmlp_last_error(void) { return t_err; }
+
+int tpmlp_version(void) { return 100; }
+
+}  // extern "C"

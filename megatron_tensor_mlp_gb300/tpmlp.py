@@ -1,0 +1,158 @@
+"""Thin ctypes binding of the tpmlp C-ABI (``include/tpmlp.h``).
+
+Argument marshalling only: every function has the C entry point's name and
+arguments; torch tensors are passed as their device pointers, ``stream``
+defaults to torch's current CUDA stream.  Every step of the computation runs
+in the CUDA kernels of ``libtpmlp.so``; there is no other code path, and
+importing this module fails if the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.environ.get("TPMLP_LIB") or os.path.join(_HERE, "libtpmlp.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "tpmlp.h")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is not built: run `python -c 'import __graft_entry__ as g; g.build()'`")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+BF16, F32 = 0, 1
+ACT_NONE, ACT_GELU_ERF = 0, 1
+
+STATUS = {0: "TPMLP_OK", 1: "TPMLP_ERR_NULL", 2: "TPMLP_ERR_SHAPE", 3: "TPMLP_ERR_DIVISIBILITY",
+          4: "TPMLP_ERR_DTYPE", 5: "TPMLP_ERR_ALIGNMENT", 6: "TPMLP_ERR_ALIAS", 7: "TPMLP_ERR_ARCH",
+          8: "TPMLP_ERR_CUDA", 9: "TPMLP_ERR_TIMEOUT", 10: "TPMLP_ERR_DEVICE"}
+OK, ERR_NULL, ERR_SHAPE, ERR_DIVISIBILITY, ERR_DTYPE, ERR_ALIGNMENT, ERR_ALIAS, ERR_ARCH, ERR_CUDA, \
+    ERR_TIMEOUT, ERR_DEVICE = range(11)
+
+_vp, _i64, _i32, _u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32
+_SIGS = {
+    "tpmlp_column_fwd": [_vp] * 5 + [_i64] * 4 + [_i32, _i32, _i32, _vp],
+    "tpmlp_row_fwd": [_vp] * 4 + [_i64] * 4 + [_i32, _i32, _vp],
+    "tpmlp_mlp_fwd": [_vp] * 8 + [_i64] * 4 + [_i32, _i32, _vp],
+    "tpmlp_mlp_bwd": [_vp] * 12 + [_i64] * 4 + [_i32, _i32, _i32, _vp],
+    "tpmlp_shard_columns": [_vp, _vp, _i64, _i64, _i32, _i32, _vp],
+    "tpmlp_unshard_columns": [_vp, _vp, _i64, _i64, _i32, _i32, _vp],
+    "tpmlp_qkv_interleave": [_vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32, _vp],
+    "tpmlp_device_status": [_vp],
+    "tpmlp_debug_wait_timeout": [_u32, _vp],
+}
+for _name, _args in _SIGS.items():
+    _f = getattr(lib, _name)
+    _f.argtypes = _args
+    _f.restype = ctypes.c_int
+lib.tpmlp_qkv_src_col.argtypes = [_i64, _i64, _i64]
+lib.tpmlp_qkv_src_col.restype = _i64
+lib.tpmlp_status_string.argtypes = [ctypes.c_int]
+lib.tpmlp_status_string.restype = ctypes.c_char_p
+lib.tpmlp_last_error.argtypes = []
+lib.tpmlp_last_error.restype = ctypes.c_char_p
+lib.tpmlp_version.argtypes = []
+lib.tpmlp_version.restype = ctypes.c_int
+
+
+class TpmlpError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/tpmlp.h."""
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(tpmlp_[a-z0-9_]+)\s*\(", txt)))
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def last_error() -> str:
+    return lib.tpmlp_last_error().decode()
+
+
+def _done(st: int, check: bool):
+    if check and st != OK:
+        raise TpmlpError(st, last_error())
+    return st
+
+
+def tpmlp_column_fwd(X, A_sh, b1_sh, Y_sh, H_sh, s, b, h, ffn, p, dt=BF16, act=ACT_GELU_ERF, stream=None,
+                     check=True):
+    st = lib.tpmlp_column_fwd(_ptr(X), _ptr(A_sh), _ptr(b1_sh), _ptr(Y_sh), _ptr(H_sh), s, b, h, ffn, p, dt, act,
+                              _stream(stream))
+    return _done(st, check)
+
+
+def tpmlp_row_fwd(Y_sh, B_sh, b2, Z, s, b, h, ffn, p, dt=BF16, stream=None, check=True):
+    st = lib.tpmlp_row_fwd(_ptr(Y_sh), _ptr(B_sh), _ptr(b2), _ptr(Z), s, b, h, ffn, p, dt, _stream(stream))
+    return _done(st, check)
+
+
+def tpmlp_mlp_fwd(X, A_sh, b1_sh, B_sh, b2, Z, Y_ws, H_sh, s, b, h, ffn, p, dt=BF16, stream=None, check=True):
+    st = lib.tpmlp_mlp_fwd(_ptr(X), _ptr(A_sh), _ptr(b1_sh), _ptr(B_sh), _ptr(b2), _ptr(Z), _ptr(Y_ws), _ptr(H_sh),
+                           s, b, h, ffn, p, dt, _stream(stream))
+    return _done(st, check)
+
+
+def tpmlp_mlp_bwd(X, A_sh, B_sh, H_sh, Y_sh, dZ, dX, dA_sh, dB_sh, db1_sh, db2, dH_ws, s, b, h, ffn, p, dt=BF16,
+                  grad_dt=F32, stream=None, check=True):
+    st = lib.tpmlp_mlp_bwd(_ptr(X), _ptr(A_sh), _ptr(B_sh), _ptr(H_sh), _ptr(Y_sh), _ptr(dZ), _ptr(dX), _ptr(dA_sh),
+                           _ptr(dB_sh), _ptr(db1_sh), _ptr(db2), _ptr(dH_ws), s, b, h, ffn, p, dt, grad_dt,
+                           _stream(stream))
+    return _done(st, check)
+
+
+def tpmlp_shard_columns(W, W_sh, rows, cols, p, dt=BF16, stream=None, check=True):
+    return _done(lib.tpmlp_shard_columns(_ptr(W), _ptr(W_sh), rows, cols, p, dt, _stream(stream)), check)
+
+
+def tpmlp_unshard_columns(W_sh, W, rows, cols, p, dt=BF16, stream=None, check=True):
+    return _done(lib.tpmlp_unshard_columns(_ptr(W_sh), _ptr(W), rows, cols, p, dt, _stream(stream)), check)
+
+
+def tpmlp_qkv_interleave(W_qkv, W_out, rows, h, n_heads, p, dt=BF16, inverse=0, stream=None, check=True):
+    st = lib.tpmlp_qkv_interleave(_ptr(W_qkv), _ptr(W_out), rows, h, n_heads, p, dt, int(inverse), _stream(stream))
+    return _done(st, check)
+
+
+def tpmlp_qkv_src_col(dst_col, h, n_heads) -> int:
+    return int(lib.tpmlp_qkv_src_col(dst_col, h, n_heads))
+
+
+def tpmlp_device_status(stream=None, check=True):
+    return _done(lib.tpmlp_device_status(_stream(stream)), check)
+
+
+def tpmlp_debug_wait_timeout(timeout_us, stream=None, check=True):
+    return _done(lib.tpmlp_debug_wait_timeout(timeout_us, _stream(stream)), check)
+
+
+def tpmlp_status_string(st: int) -> str:
+    return lib.tpmlp_status_string(st).decode()
+
+
+def tpmlp_last_error() -> str:
+    return last_error()
+
+
+def tpmlp_version() -> int:
+    return int(lib.tpmlp_version())

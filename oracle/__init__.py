@@ -70,6 +70,8 @@ class Oracle:
         lib.oracle_bwd_dX_rows.argtypes = [i64, i64, i64, i32] + [vp] * 5 + [i64, vp, vp]
         lib.oracle_bwd_ffn_cols.restype = None
         lib.oracle_bwd_ffn_cols.argtypes = [i64, i64, i64, i32] + [vp] * 5 + [i64, vp, vp, vp, vp]
+        lib.oracle_bwd_db2.restype = None
+        lib.oracle_bwd_db2.argtypes = [i64, i64, vp, vp]
         lib.oracle_shard_columns.restype = None
         lib.oracle_shard_columns.argtypes = [i64, i64, i64, i64, vp, vp]
         lib.oracle_qkv_src_col.restype = i64
@@ -134,6 +136,14 @@ class Oracle:
         self.lib.oracle_bwd_ffn_cols(M, h, f, act, _ptr(X), _ptr(A), _ptr(b1), _ptr(B), _ptr(dZ),
                                      n, _ptr(cols), _ptr(dA_c), _ptr(dB_r), _ptr(db1_c))
         return dA_c, dB_r, db1_c
+
+    def bwd_db2(self, dZ):
+        """db2 = column sums of dZ."""
+        dZ = _f64(dZ)
+        M, h = dZ.shape
+        out = np.empty(h)
+        self.lib.oracle_bwd_db2(M, h, _ptr(dZ), _ptr(out))
+        return out
 
     def shard_columns(self, W, p):
         """[rows, cols] -> [p, rows, cols/p] (element words copied verbatim)."""

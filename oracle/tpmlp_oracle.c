@@ -243,6 +243,14 @@ void oracle_bwd_ffn_cols(int64_t M, int64_t h, int64_t f, int act,
     }
 }
 
+/* db2 = 1^T dZ (the row-parallel bias gradient: b2 is added once to the summed
+ * output, so its gradient is the plain column sum of dZ). */
+void oracle_bwd_db2(int64_t M, int64_t h, const double* dZ, double* db2) {
+    for (int64_t n = 0; n < h; ++n) db2[n] = 0.0;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < h; ++n) db2[n] += dZ[m * h + n];
+}
+
 /* ------------------------------------------------------------------------ */
 /* Layout maps (integer index work; compared bit for bit).                   */
 

@@ -234,6 +234,7 @@ def pin_sampled_backward_matches_full(orc):
     assert np.max(np.abs(dAc - g["dA"][:, cols])) <= 1e-12 * np.max(np.abs(g["dA"]))
     assert np.max(np.abs(dBr - g["dB"][cols, :])) <= 1e-12 * np.max(np.abs(g["dB"]))
     assert np.max(np.abs(db1c - g["db1"][cols])) <= 1e-12 * np.max(np.abs(g["db1"]))
+    assert np.max(np.abs(orc.bwd_db2(dZ) - g["db2"])) <= 1e-12 * np.max(np.abs(g["db2"]))
 
 
 # --------------------------------------------------------------------------

@@ -1,0 +1,76 @@
+"""The five workloads at full size, in the launch configuration the benchmark
+times, against the oracle on sampled outputs computed one by one (GPU)."""
+import numpy as np
+import pytest
+
+import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from megatron_tensor_mlp_gb300 import harness, synth, tpmlp
+    return harness, synth, tpmlp
+
+
+def _rows(M, n_random, seed):
+    rng = np.random.default_rng(seed)
+    r = {0, 1, 127, 128, M // 2, M - 1} | set(rng.integers(0, M, n_random).tolist())
+    return np.array(sorted(x for x in r if 0 <= x < M), dtype=np.int64)
+
+
+def _cols(f, p, n_random, seed):
+    fs = f // p
+    rng = np.random.default_rng(seed + 1)
+    c = {0, fs - 1, fs, f - 1, 255, 256} | set(rng.integers(0, f, n_random).tolist())
+    return np.array(sorted(x for x in c if 0 <= x < f), dtype=np.int64)
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+def test_workload_sampled(env, orc, cfg):
+    import torch
+    harness, synth, T = env
+    wl = synth.WORKLOADS[cfg]
+    buf = harness.MLPBuffers(wl)
+    for t in (buf.Z, buf.Y, buf.H):
+        if t is not None:
+            t.fill_(float("nan"))
+    buf.fwd()
+    if wl.backward:
+        buf.bwd()
+    T.tpmlp_device_status()
+    M, h, f, p = wl.M, wl.h, wl.ffn, wl.p
+    rows = _rows(M, 10, cfg)
+    widen = synth.widen
+    X = widen(buf.host["X"])
+    A = widen(buf.host["A"])
+    B = widen(buf.host["B"])
+    b1 = None if buf.host["b1"] is None else widen(buf.host["b1"])
+    b2 = None if buf.host["b2"] is None else widen(buf.host["b2"])
+    Hr, Yr, Zr = orc.mlp_fwd(X[rows], A, b1, B, b2)
+    ridx = torch.from_numpy(rows).cuda()
+    U.assert_close(harness.to_host(buf.Z[ridx]), Zr, "bf16", f"Z rows (cfg {cfg})")
+    U.assert_close(harness.to_host(buf.Y_full()[ridx]), Yr, "bf16", f"Y rows (cfg {cfg})")
+    if buf.H is not None:
+        U.assert_close(harness.to_host(buf.H_full()[ridx]), Hr, "bf16", f"H rows (cfg {cfg})")
+    # a property at full size: every output finite
+    assert bool(torch.isfinite(buf.Z).all())
+    if not wl.backward:
+        return
+    dZ = widen(buf.host["dZ"])
+    cols = _cols(f, p, 6, cfg)
+    dAc, dBr, db1c = orc.bwd_ffn_cols(X, A, b1, B, dZ, cols)
+    cidx = torch.from_numpy(cols).cuda()
+    U.assert_close(harness.to_host(buf.dA_full()[:, cidx]), dAc, "bf16", "dA cols")
+    U.assert_close(harness.to_host(buf.dB_full()[cidx]), dBr, "bf16", "dB rows")
+    U.assert_close(harness.to_host(buf.db1_sh.reshape(-1)[cidx]), db1c, "bf16", "db1")
+    U.assert_close(harness.to_host(buf.db2), orc.bwd_db2(dZ), "bf16", "db2")
+    xr = rows[:: max(1, len(rows) // 4)][:4]
+    dXr = orc.bwd_dX_rows(X, A, b1, B, dZ, xr)
+    U.assert_close(harness.to_host(buf.dX[torch.from_numpy(xr).cuda()]), dXr, "bf16", "dX rows")
+    for t in (buf.dX, buf.dA_sh, buf.dB_sh):
+        assert bool(torch.isfinite(t).all())

@@ -1,0 +1,197 @@
+"""The MLP block through the C-ABI against the fp64 oracle on small shapes that
+span several tiles and ragged tails in every GEMM dimension (GPU)."""
+import numpy as np
+import pytest
+
+import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from megatron_tensor_mlp_gb300 import harness, synth, tpmlp
+    return harness, synth, tpmlp
+
+
+# (s, b, h, ffn, p): tiles are 128 (tokens) x 256 (outputs) x 64 (reduction)
+SHAPES = [
+    (25, 8, 72, 264, 3),      # M=200 ragged, h=72 ragged K, fs=88 ragged N
+    (16, 8, 128, 512, 1),     # p = 1: the plain MLP
+    (33, 4, 256, 1024, 2),    # M=132 (one row past a tile), fs=512 (two full N tiles)
+    (64, 4, 320, 1280, 4),    # h=320: row GEMM N tail of 64, K of 5 blocks
+    (7, 3, 512, 2048, 8),     # M=21, p=8
+    (100, 3, 136, 544, 2),    # h=136 (2 K blocks + 8), fs=272 (256 + 16), M=300
+    (128, 2, 192, 768, 6),    # p=6, fs=128
+]
+
+
+def _run_and_check(env, orc, wl, check_bwd=True):
+    harness, synth, T = env
+    buf = harness.MLPBuffers(wl, backward=check_bwd)
+    # poison outputs so that unwritten elements show up as NaN
+    for t in (buf.Z, buf.Y, buf.H):
+        if t is not None:
+            t.fill_(float("nan"))
+    buf.fwd()
+    if check_bwd:
+        for t in (buf.dX, buf.dA_sh, buf.dB_sh, buf.db1_sh, buf.db2, buf.dH):
+            t.fill_(float("nan"))
+        buf.bwd()
+    T.tpmlp_device_status()
+    x = U.host_inputs_f64(buf)
+    H, Y, Z = orc.mlp_fwd(x["X"], x["A"], x["b1"], x["B"], x["b2"])
+    dt = wl.dtype
+    U.assert_close(harness.to_host(buf.Z), Z, dt, "Z")
+    U.assert_close(harness.to_host(buf.Y_full()), Y, dt, "Y")
+    if buf.H is not None:
+        U.assert_close(harness.to_host(buf.H_full()), H, dt, "H")
+    if check_bwd:
+        g = orc.mlp_bwd(x["X"], x["A"], x["B"], H, Y, x["dZ"])
+        U.assert_close(harness.to_host(buf.dX), g["dX"], dt, "dX")
+        U.assert_close(harness.to_host(buf.dA_full()), g["dA"], dt, "dA")
+        U.assert_close(harness.to_host(buf.dB_full()), g["dB"], dt, "dB")
+        U.assert_close(harness.to_host(buf.db1_sh).reshape(-1), g["db1"], dt, "db1")
+        U.assert_close(harness.to_host(buf.db2), g["db2"], dt, "db2")
+    return buf
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "s{}b{}h{}f{}p{}".format(*s))
+def test_bf16_fwd_bwd_small(env, orc, shape):
+    _, synth, _ = env
+    wl = synth.custom(*shape, dtype="bf16", sigma_w=0.05, sigma_bias=0.05, seed=sum(shape))
+    _run_and_check(env, orc, wl)
+
+
+def test_f32_tiny_workload(env, orc):
+    """The tiny fp32 workload (s=8, b=2, h=64, ffn=256, p=2), forward and backward, <= 1e-5."""
+    _, synth, _ = env
+    _run_and_check(env, orc, synth.WORKLOADS[1])
+
+
+@pytest.mark.parametrize("shape", [(5, 3, 48, 144, 3), (9, 7, 64, 256, 4)], ids=str)
+def test_f32_small(env, orc, shape):
+    _, synth, _ = env
+    wl = synth.custom(*shape, dtype="f32", sigma_w=0.1, sigma_bias=0.1, seed=3)
+    _run_and_check(env, orc, wl)
+
+
+def test_every_divisor_p(env, orc):
+    """Sharded == unsharded for every legal p of one small problem (forward)."""
+    _, synth, _ = env
+    h, ffn = 96, 384
+    for p in [d for d in range(1, 13) if ffn % d == 0 and h % d == 0 and (ffn // d) % 8 == 0]:
+        wl = synth.custom(6, 11, h, ffn, p, dtype="bf16", sigma_w=0.05, sigma_bias=0.05, seed=5)
+        _run_and_check(env, orc, wl, check_bwd=False)
+
+
+def test_column_and_row_entry_points(env, orc):
+    """tpmlp_column_fwd (GeLU and identity) and tpmlp_row_fwd on their own."""
+    import torch
+    harness, synth, T = env
+    wl = synth.custom(10, 13, 136, 528, 2, dtype="bf16", sigma_w=0.05, sigma_bias=0.05, seed=11)
+    buf = harness.MLPBuffers(wl, backward=False)
+    s, b, h, f, p = buf.dims()
+    M, fs = s * b, f // p
+    x = U.host_inputs_f64(buf)
+    for act in (T.ACT_GELU_ERF, T.ACT_NONE):
+        Y = torch.full((p, M, fs), float("nan"), dtype=torch.bfloat16, device="cuda")
+        Hs = torch.full((p, M, fs), float("nan"), dtype=torch.bfloat16, device="cuda")
+        T.tpmlp_column_fwd(buf.X, buf.A_sh, buf.b1_sh, Y, Hs, s, b, h, f, p, act=act)
+        T.tpmlp_device_status()
+        Href, Yref, _ = orc.mlp_fwd(x["X"], x["A"], x["b1"], x["B"], None,
+                                    act=1 if act == T.ACT_GELU_ERF else 0)
+        U.assert_close(harness.to_host(Y.permute(1, 0, 2).reshape(M, f)), Yref, "bf16", f"Y act={act}")
+        U.assert_close(harness.to_host(Hs.permute(1, 0, 2).reshape(M, f)), Href, "bf16", f"H act={act}")
+    # row layer alone on the GPU's own Y: Z = sum_i Y_i B_i + b2
+    Z = torch.full((M, h), float("nan"), dtype=torch.bfloat16, device="cuda")
+    T.tpmlp_column_fwd(buf.X, buf.A_sh, buf.b1_sh, buf.Y, None, s, b, h, f, p)
+    T.tpmlp_row_fwd(buf.Y, buf.B_sh, buf.b2, Z, s, b, h, f, p)
+    T.tpmlp_device_status()
+    Yg = harness.to_host(buf.Y_full())
+    Zref = Yg @ x["B"] + x["b2"]
+    U.assert_close(harness.to_host(Z), Zref, "bf16", "Z(row on GPU Y)")
+
+
+def test_bias_added_once(env, orc):
+    """With p = 4 a per-shard b2 would give Z + 3 b2: the oracle comparison catches it;
+    here we also check Z(b2) - Z(0) == b2 exactly up to bf16 rounding."""
+    import torch
+    harness, synth, T = env
+    wl = synth.custom(4, 8, 64, 256, 4, dtype="bf16", sigma_w=0.02, sigma_bias=0.5, seed=21)
+    buf = harness.MLPBuffers(wl, backward=False)
+    s, b, h, f, p = buf.dims()
+    buf.fwd()
+    Z0 = torch.empty_like(buf.Z)
+    T.tpmlp_row_fwd(buf.Y, buf.B_sh, None, Z0, s, b, h, f, p)
+    T.tpmlp_device_status()
+    diff = harness.to_host(buf.Z) - harness.to_host(Z0)
+    b2 = U.host_inputs_f64(buf)["b2"]
+    assert np.max(np.abs(diff - b2)) < 0.02 * np.max(np.abs(b2)) + 0.02
+
+
+def test_deterministic(env, orc):
+    harness, synth, T = env
+    wl = synth.custom(50, 6, 256, 1024, 4, dtype="bf16", seed=2)
+    buf = harness.MLPBuffers(wl, backward=True)
+    buf.fwd()
+    buf.bwd()
+    first = [t.clone() for t in (buf.Z, buf.Y, buf.H, buf.dX, buf.dA_sh, buf.dB_sh, buf.db1_sh, buf.db2)]
+    buf.fwd()
+    buf.bwd()
+    T.tpmlp_device_status()
+    again = (buf.Z, buf.Y, buf.H, buf.dX, buf.dA_sh, buf.dB_sh, buf.db1_sh, buf.db2)
+    import torch
+    for a, b_ in zip(first, again):
+        assert torch.equal(a, b_), "results differ between runs"
+
+
+def test_guard_canaries(env, orc):
+    """Outputs written through pointers into the middle of larger buffers leave the
+    surrounding guard bytes untouched."""
+    import torch
+    harness, synth, T = env
+    wl = synth.custom(40, 5, 136, 544, 2, dtype="bf16", seed=8)
+    buf = harness.MLPBuffers(wl, backward=True)
+    s, b, h, f, p = buf.dims()
+    M, fs = s * b, f // p
+    G = 4096  # guard elements on each side (8 KiB)
+
+    def guarded(n, dtype):
+        big = torch.full((n + 2 * G,), 7.0, dtype=dtype, device="cuda")
+        return big, big[G:G + n]
+
+    zb, Z = guarded(M * h, torch.bfloat16)
+    yb, Y = guarded(p * M * fs, torch.bfloat16)
+    hb, Hs = guarded(p * M * fs, torch.bfloat16)
+    T.tpmlp_mlp_fwd(buf.X, buf.A_sh, buf.b1_sh, buf.B_sh, buf.b2, Z, Y, Hs, s, b, h, f, p)
+    xb, dX = guarded(M * h, torch.bfloat16)
+    ab, dA = guarded(p * h * fs, torch.float32)
+    bb, dB = guarded(p * fs * h, torch.float32)
+    db1b, db1 = guarded(f, torch.float32)
+    db2b, db2 = guarded(h, torch.float32)
+    dhb, dH = guarded(p * M * fs, torch.bfloat16)
+    T.tpmlp_mlp_bwd(buf.X, buf.A_sh, buf.B_sh, Hs, Y, buf.dZ, dX, dA, dB, db1, db2, dH, s, b, h, f, p)
+    T.tpmlp_device_status()
+    for big in (zb, yb, hb, xb, ab, bb, db1b, db2b, dhb):
+        assert bool((big[:G] == 7.0).all()) and bool((big[-G:] == 7.0).all())
+    # and the results equal the plain run
+    buf.fwd()
+    buf.bwd()
+    T.tpmlp_device_status()
+    assert bool((buf.Z.view(-1) == Z).all())
+    assert bool((buf.dX.view(-1) == dX).all())
+
+
+def test_empty_batch(env):
+    import torch
+    harness, synth, T = env
+    dummy = torch.zeros(1024, dtype=torch.bfloat16, device="cuda")
+    out = torch.full((1024,), 3.0, dtype=torch.bfloat16, device="cuda")
+    ws = torch.full((1024,), 3.0, dtype=torch.bfloat16, device="cuda")
+    assert T.tpmlp_mlp_fwd(dummy, dummy, None, dummy, None, out, ws, None, 0, 4, 64, 256, 2) == T.OK
+    T.tpmlp_device_status()
+    assert bool((out == 3.0).all()) and bool((ws == 3.0).all())
