@@ -360,6 +360,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     }
 
+    __syncwarp();  // reconverge the single-lane producer / MMA branches
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
