@@ -1,0 +1,386 @@
+#!/usr/bin/env python3
+"""Benchmark of the tensor-parallel MLP block on GB300.
+
+One step = one pass of the whole hot path over one batch: the column-parallel
+GEMM with fused bias + erf-GeLU, the row-parallel GEMM with the on-device
+shard sum, and the full backward (dH with fused GeLU', dB_i, dA_i, the summed
+dX, db1, db2).  The workload is s=2048, b=4, h=5120, ffn=20480, p=4 (bf16,
+fp32 accumulation).  The line also carries the forward at the pages' sizing
+(s=4096, b=1, h=8192, ffn=32768, p=8).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs an independent
+replica of the workload on its own GPU (no exchange between ranks: all p shards
+of a block live on one GPU); `value` is the total over ranks divided by the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "TP-MLP fwd/bwd TFLOP/s & tokens/s on 1 GB300; % of dense BF16 tensor peak"
+NOMINAL_BF16_TFLOPS = 2250.0
+MAIN_WORKLOAD = 5      # fwd + bwd
+FWD_WORKLOAD = 4       # forward at the pages' sizing
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="tpmlp", choices=["tpmlp", "reference"])
+    ap.add_argument("--workload", type=int, default=MAIN_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fwd-pages", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return json.load(fh), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = f"/tmp/tpmlp_clocks_{os.getpid()}.csv"
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_median": statistics.median(power) if power else None}
+
+
+# --------------------------------------------------------------------------- CPU (oracle) arm
+class OracleSample:
+    """The oracle (fp64 CPU) on a row sample of the workload: forward (+ backward)
+    on the first M' tokens with the full weights.  Inputs are generated once."""
+
+    def __init__(self, wl):
+        import oracle
+        from megatron_tensor_mlp_gb300 import synth
+
+        self.wl = wl
+        self.orc = oracle.get()
+        self.synth = synth
+        self.A = synth.widen(wl.gen("A"))
+        self.B = synth.widen(wl.gen("B"))
+        self.b1 = None if wl.sigma_bias == 0 else synth.widen(wl.gen("b1"))
+        self.b2 = None if wl.sigma_bias == 0 else synth.widen(wl.gen("b2"))
+        self.per_token = (wl.fwd_flops() + (wl.bwd_flops() if wl.backward else 0.0)) / wl.M
+
+    def run(self, tokens):
+        """Seconds for one oracle pass over the first `tokens` tokens."""
+        wl = self.wl
+        X = self.synth.widen(wl.gen("X", 0, tokens))
+        dZ = self.synth.widen(wl.gen("dZ", 0, tokens)) if wl.backward else None
+        t0 = time.perf_counter()
+        H, Y, _ = self.orc.mlp_fwd(X, self.A, self.b1, self.B, self.b2)
+        if wl.backward:
+            self.orc.mlp_bwd(X, self.A, self.B, H, Y, dZ)
+        return time.perf_counter() - t0
+
+    def calibrate(self, target_seconds):
+        """Largest power-of-two token count whose pass stays near target_seconds."""
+        tokens = 1
+        dt = self.run(tokens)
+        while tokens * 2 <= self.wl.M and dt * 2 <= target_seconds:
+            tokens *= 2
+            dt = self.run(tokens)
+        return tokens, dt
+
+    def describe(self, tokens, dt):
+        wl = self.wl
+        return (f"oracle fp64 {'fwd+bwd' if wl.backward else 'fwd'} on the first {tokens} of {wl.M} tokens "
+                f"with the full weights ({dt:.2f} s per pass)")
+
+    def tflops(self, tokens, dt):
+        return self.per_token * tokens / dt / 1e12
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from megatron_tensor_mlp_gb300 import synth
+
+    wl = synth.WORKLOADS[args.workload]
+    sample = OracleSample(wl)
+    per_step = min(30.0, 150.0 / max(1, args.steps + args.warmup))  # whole run within a few minutes
+    tokens, _ = sample.calibrate(per_step)
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt = sample.run(tokens)
+        if i >= args.warmup:
+            times.append(dt)
+    dt = statistics.median(times)
+    v = sample.tflops(tokens, dt)
+    out = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": ws,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": wl.name, "s": wl.s, "b": wl.b, "h": wl.h, "ffn": wl.ffn, "p": wl.p,
+                      "parallelism": "replicas"},
+           "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": sample.orc.num_threads(),
+                            "kind": "oracle", "sample": sample.describe(tokens, dt)},
+           "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import torch
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    from megatron_tensor_mlp_gb300 import harness, synth
+    from megatron_tensor_mlp_gb300 import tpmlp as T
+
+    peaks, peak_kind = load_peaks()
+    wl = synth.WORKLOADS[args.workload]
+    buf = harness.MLPBuffers(wl)
+    s, b, h, f, p = buf.dims()
+    M = wl.M
+    stream = torch.cuda.current_stream()
+
+    def step():
+        T.tpmlp_column_fwd(buf.X, buf.A_sh, buf.b1_sh, buf.Y, buf.H, s, b, h, f, p, stream=stream)
+        T.tpmlp_row_fwd(buf.Y, buf.B_sh, buf.b2, buf.Z, s, b, h, f, p, stream=stream)
+        if wl.backward:
+            buf.bwd(stream=stream)
+
+    launches_per_step = 2 + (6 if wl.backward else 0)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    T.tpmlp_device_status()
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # timed region: per-call events on the launching stream
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(K):
+        e = ev[i]
+        e[0].record(stream)
+        T.tpmlp_column_fwd(buf.X, buf.A_sh, buf.b1_sh, buf.Y, buf.H, s, b, h, f, p, stream=stream)
+        e[1].record(stream)
+        T.tpmlp_row_fwd(buf.Y, buf.B_sh, buf.b2, buf.Z, s, b, h, f, p, stream=stream)
+        e[2].record(stream)
+        if wl.backward:
+            buf.bwd(stream=stream)
+        e[3].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    T.tpmlp_device_status()
+    total_ms = t_start.elapsed_time(t_end)
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / K
+    col_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    row_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev) if wl.backward else 0.0
+    flops_step = wl.fwd_flops() + (wl.bwd_flops() if wl.backward else 0.0)
+    value = flops_step * ws / (ms_step * 1e-3) / 1e12
+    tokens_s = M * ws / (ms_step * 1e-3)
+
+    # roofline: the single-launch GEMM with the larger time (column with GeLU, or row with shard sum)
+    gemm_flops = 2.0 * M * h * f
+    dom_name, dom_ms = ("column_fwd (tcgen05 GEMM + bias + erf-GeLU epilogue)", col_ms) if col_ms >= row_ms else \
+        ("row_fwd (tcgen05 GEMM + in-TMEM shard sum)", row_ms)
+    achieved = gemm_flops / (dom_ms * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", 1700.0)
+    roofline = {"bound": "tensor", "kernel": dom_name, "achieved": round(achieved, 1), "peak": peak,
+                "peak_kind": f"bf16_tflops_sustained ({peak_kind})", "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "per_launch_ms": {"column_fwd": round(col_ms, 4), "row_fwd": round(row_ms, 4),
+                                  "mlp_bwd(6 launches)": round(bwd_ms, 4)}}
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    e2e = None
+    if args.e2e_steps > 0:
+        X_host = buf.X.cpu().pin_memory()
+        dZ_host = buf.dZ.cpu().pin_memory() if wl.backward else None
+        Z_host = torch.empty(buf.Z.shape, dtype=buf.Z.dtype).pin_memory()
+        dX_host = torch.empty(buf.dX.shape, dtype=buf.dX.dtype).pin_memory() if wl.backward else None
+        h2d = X_host.numel() * X_host.element_size() + (dZ_host.numel() * dZ_host.element_size() if wl.backward else 0)
+        d2h = Z_host.numel() * Z_host.element_size() + (dX_host.numel() * dX_host.element_size() if wl.backward else 0)
+
+        def e2e_step():
+            buf.X.copy_(X_host, non_blocking=True)
+            if wl.backward:
+                buf.dZ.copy_(dZ_host, non_blocking=True)
+            buf.fwd(stream=stream)
+            if wl.backward:
+                buf.bwd(stream=stream)
+            Z_host.copy_(buf.Z, non_blocking=True)
+            if wl.backward:
+                dX_host.copy_(buf.dX, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        z.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(z) / args.e2e_steps
+        if ws > 1:
+            import torch.distributed as dist
+            t = torch.tensor([e2e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": round(flops_step * ws / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "note": "inputs X, dZ copied from pinned host memory and Z, dX read back every step; "
+                       "weights stay resident"}
+    T.tpmlp_device_status()
+
+    # the forward at the pages' sizing (the >= 60% of dense bf16 target)
+    fwd_pages = None
+    if not args.no_fwd_pages and args.workload != FWD_WORKLOAD:
+        del buf
+        torch.cuda.empty_cache()
+        w4 = synth.WORKLOADS[FWD_WORKLOAD]
+        b4 = harness.MLPBuffers(w4, backward=False)
+        for _ in range(5):
+            b4.fwd(stream=stream)
+        torch.cuda.synchronize()
+        n4 = max(20, K // 2)
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n4):
+            b4.fwd(stream=stream)
+        z.record(stream)
+        torch.cuda.synchronize()
+        T.tpmlp_device_status()
+        ms4 = a.elapsed_time(z) / n4
+        tf4 = w4.fwd_flops() / (ms4 * 1e-3) / 1e12
+        fwd_pages = {"workload": w4.name, "ms": round(ms4, 4), "TFLOP/s": round(tf4, 1),
+                     "tokens_per_s": round(w4.M / (ms4 * 1e-3), 1),
+                     "pct_of_nominal_2250": round(100 * tf4 / NOMINAL_BF16_TFLOPS, 2),
+                     "pct_of_measured_sustained": round(100 * tf4 / peaks.get("bf16_tflops_sustained", 1700.0), 2),
+                     "steps": n4}
+        del b4
+        torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        sample = OracleSample(wl)
+        tokens, dt = sample.calibrate(args.cpu_seconds)
+        cpu = {"value": round(sample.tflops(tokens, dt), 6), "unit": "TFLOP/s", "cores": sample.orc.num_threads(),
+               "kind": "oracle", "sample": sample.describe(tokens, dt)}
+
+    if rank == 0:
+        out = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
+               "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+               "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+               "config": {"workload": wl.name, "s": s, "b": b, "h": h, "ffn": f, "p": p,
+                          "step": "fwd+bwd" if wl.backward else "fwd",
+                          "parallelism": f"replicas x{ws} (all p shards on each GPU)",
+                          "l2": "inputs larger than L2 (working set > 1 GB per step)"},
+               "tokens_per_s": round(tokens_s, 1),
+               "pct_of_nominal_bf16_peak": round(100 * value / ws / NOMINAL_BF16_TFLOPS, 2),
+               "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+               "gpu_launches": launches_per_step * K, "clocks": clocks,
+               "fwd_pages_sizing": fwd_pages}
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
