@@ -130,6 +130,31 @@ tpmlp_status tpmlp_mlp_bwd(const void* X, const void* A_sh, const void* B_sh, co
                            tpmlp_dtype dt, tpmlp_dtype grad_dt, void* stream);
 
 /*
+ * The MLP block forward without a caller workspace.  The pages have no
+ * counterpart: this entry point exists for callers that cannot allocate device
+ * memory where they run the block (for example an inference-engine plugin whose
+ * host engine owns all device memory, or a runtime that forbids allocation after
+ * start-up because an allocation can synchronise the device).
+ *   Same arguments and results as tpmlp_mlp_fwd without Y_ws and H_sh: the
+ *   intermediate Y lives in a fixed array inside the library of
+ *   TPMLP_NOALLOC_SCRATCH_BYTES bytes (32 MiB), which every GPU that loads the
+ *   library holds until the process exits.  Calls needing more than that
+ *   (s*b*ffn*element size bytes) return TPMLP_ERR_SHAPE.
+ *   This call allocates nothing (no cudaMalloc, no allocating library routine).
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *   first call before any stream capture.
+ *   Every call shares the one array per device and it keeps the last call's
+ *   contents; each call overwrites all of the Y it reads, so nothing needs
+ *   clearing.  Calls whose kernels overlap on the GPU (different streams, or
+ *   threads without ordering) race on the array.
+ */
+#define TPMLP_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+tpmlp_status tpmlp_mlp_fwd_noalloc(const void* X, const void* A_sh, const void* b1_sh, const void* B_sh,
+                                   const void* b2, void* Z, int64_t s, int64_t b, int64_t h, int64_t ffn, int p,
+                                   tpmlp_dtype dt, void* stream);
+
+/*
  * Column shard layout ("列并行" article, 切分原理: W = [W(1) || ... || W(p)];
  * the article's NumPy demo uses np.split(W, p, axis=1)):
  *   W_sh[i][r][c] = W[r][i * cols/p + c],   W [rows, cols] dt,  W_sh [p][rows][cols/p] dt.

@@ -16,7 +16,7 @@ from concurrent.futures import ThreadPoolExecutor
 PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libtpmlp.so")
-SOURCES = ["tpmlp_api.cu", "gemm_tc.cu", "kernels_misc.cu"]
+SOURCES = ["tpmlp_api.cu", "gemm_tc.cu", "kernels_misc.cu", "noalloc.cu"]
 HEADERS = ["ptx.cuh", "gemm_tc.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -36,6 +36,7 @@ _SIGS = {
     "tpmlp_row_fwd": [_vp] * 4 + [_i64] * 4 + [_i32, _i32, _vp],
     "tpmlp_mlp_fwd": [_vp] * 8 + [_i64] * 4 + [_i32, _i32, _vp],
     "tpmlp_mlp_bwd": [_vp] * 12 + [_i64] * 4 + [_i32, _i32, _i32, _vp],
+    "tpmlp_mlp_fwd_noalloc": [_vp] * 6 + [_i64] * 4 + [_i32, _i32, _vp],
     "tpmlp_shard_columns": [_vp, _vp, _i64, _i64, _i32, _i32, _vp],
     "tpmlp_unshard_columns": [_vp, _vp, _i64, _i64, _i32, _i32, _vp],
     "tpmlp_qkv_interleave": [_vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32, _vp],
@@ -119,6 +120,16 @@ def tpmlp_mlp_bwd(X, A_sh, B_sh, H_sh, Y_sh, dZ, dX, dA_sh, dB_sh, db1_sh, db2, 
                            _ptr(dB_sh), _ptr(db1_sh), _ptr(db2), _ptr(dH_ws), s, b, h, ffn, p, dt, grad_dt,
                            _stream(stream))
     return _done(st, check)
+
+
+def tpmlp_mlp_fwd_noalloc(X, A_sh, b1_sh, B_sh, b2, Z, s, b, h, ffn, p, dt=BF16, stream=None, check=True):
+    """The block forward with Y kept in the library's fixed array (no caller workspace)."""
+    st = lib.tpmlp_mlp_fwd_noalloc(_ptr(X), _ptr(A_sh), _ptr(b1_sh), _ptr(B_sh), _ptr(b2), _ptr(Z), s, b, h, ffn, p,
+                                   dt, _stream(stream))
+    return _done(st, check)
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
 def tpmlp_shard_columns(W, W_sh, rows, cols, p, dt=BF16, stream=None, check=True):
