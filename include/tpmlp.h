@@ -197,6 +197,16 @@ tpmlp_status tpmlp_device_status(void* stream);
  */
 tpmlp_status tpmlp_debug_wait_timeout(uint32_t timeout_us, void* stream);
 
+/*
+ * Tiling of the bf16 GEMMs, process wide: 0 = automatic (default: 256x256 tiles
+ * on CTA pairs when there are enough of them to fill the GPU, else 128x256 tiles
+ * on single CTAs), 1 = single-CTA tiles only, 2 = CTA-pair tiles only.  Results
+ * agree within rounding in every mode; the control exists for tuning and tests.
+ * Returns TPMLP_ERR_SHAPE for other values.
+ */
+tpmlp_status tpmlp_set_gemm_mode(int mode);
+int tpmlp_get_gemm_mode(void);
+
 /* Human-readable name of a status code. */
 const char* tpmlp_status_string(tpmlp_status st);
 

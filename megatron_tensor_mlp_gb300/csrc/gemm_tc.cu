@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "gemm_tc.cuh"
@@ -53,19 +54,27 @@ bool make_map(CUtensorMap* map, const Operand& op, uint64_t inner, uint64_t oute
     return true;
 }
 
+std::atomic<int> g_gemm_mode{0};  // 0 automatic, 1 single-CTA tiles, 2 CTA-pair tiles
+
+template <typename Kern>
+bool set_smem_attr(Kern kern, int device, int bytes, bool* done) {
+    if (device < 64 && done[device]) return true;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) {
+        set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        return false;
+    }
+    if (device < 64) done[device] = true;
+    return true;
+}
+
 template <bool A_MN, bool B_MN, int EPI>
-tpmlp_status launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const tc::KArgs& k, int grid,
-                            const DeviceInfo& dev, cudaStream_t st) {
+tpmlp_status launch_single(const CUtensorMap& ma, const CUtensorMap& mb, const tc::KArgs& k, const DeviceInfo& dev,
+                           cudaStream_t st) {
     auto kern = tc::gemm_kernel<A_MN, B_MN, EPI>;
     static bool attr_done[64] = {};
-    if (dev.device < 64 && !attr_done[dev.device]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
-        if (e != cudaSuccess) {
-            set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-            return TPMLP_ERR_CUDA;
-        }
-        attr_done[dev.device] = true;
-    }
+    if (!set_smem_attr(kern, dev.device, tc::SMEM_BYTES, attr_done)) return TPMLP_ERR_CUDA;
+    const int grid = k.num_tiles < dev.sm_count ? k.num_tiles : dev.sm_count;
     kern<<<grid, tc::NUM_THREADS, tc::SMEM_BYTES, st>>>(ma, mb, k);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -75,17 +84,88 @@ tpmlp_status launch_variant(const CUtensorMap& ma, const CUtensorMap& mb, const 
     return TPMLP_OK;
 }
 
+// Co-resident CTA pairs of the pair kernel on this device (0 if it cannot run).
+template <bool A_MN, bool B_MN, int EPI>
+int pair_capacity(const DeviceInfo& dev) {
+    static int cap[64];
+    static bool done[64];
+    static bool attr_done[64] = {};
+    if (dev.device >= 64) return 0;
+    if (done[dev.device]) return cap[dev.device];
+    auto kern = tc::gemm_pair_kernel<A_MN, B_MN, EPI>;
+    int n = 0;
+    if (set_smem_attr(kern, dev.device, tc::P_SMEM_BYTES, attr_done)) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (dev.sm_count / 2));
+        cfg.blockDim = dim3(tc::NUM_THREADS);
+        cfg.dynamicSmemBytes = tc::P_SMEM_BYTES;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+        cudaGetLastError();
+    }
+    cap[dev.device] = n;
+    done[dev.device] = true;
+    return n;
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+tpmlp_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const tc::KArgs& k, int clusters,
+                         cudaStream_t st) {
+    auto kern = tc::gemm_pair_kernel<A_MN, B_MN, EPI>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(tc::NUM_THREADS);
+    cfg.dynamicSmemBytes = tc::P_SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, k);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("tcgen05 CTA-pair GEMM launch: %s", cudaGetErrorString(e));
+        return TPMLP_ERR_CUDA;
+    }
+    return TPMLP_OK;
+}
+
+// Picks single-CTA or CTA-pair tiles and launches.  Pair tiles when there are at
+// least as many 256-row tiles as co-resident pairs (or when forced).
+template <bool A_MN, bool B_MN, int EPI>
+tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& g, tc::KArgs k, const DeviceInfo& dev,
+                            cudaStream_t st) {
+    const int mode = g_gemm_mode.load(std::memory_order_relaxed);
+    const int m_pairs = static_cast<int>((g.M + 2 * tc::BM - 1) / (2 * tc::BM));
+    const int pair_tiles = m_pairs * k.n_blocks * k.batch;
+    int cap = (mode == 1) ? 0 : pair_capacity<A_MN, B_MN, EPI>(dev);
+    const bool use_pair = cap > 0 && (mode == 2 || pair_tiles >= cap);
+    CUtensorMap ma, mb;
+    bool ok = a.mn_major ? make_map(&ma, a, g.M, g.K, 64, tc::BK) : make_map(&ma, a, g.K, g.M, tc::BK, tc::BM);
+    if (!ok) return TPMLP_ERR_CUDA;
+    const uint32_t b_rows = use_pair ? tc::BN / 2 : tc::BN;
+    ok = b.mn_major ? make_map(&mb, b, g.N, g.K, 64, tc::BK) : make_map(&mb, b, g.K, g.N, tc::BK, b_rows);
+    if (!ok) return TPMLP_ERR_CUDA;
+    if (!use_pair) return launch_single<A_MN, B_MN, EPI>(ma, mb, k, dev, st);
+    k.m_blocks = m_pairs;
+    k.num_tiles = pair_tiles;
+    const int clusters = pair_tiles < cap ? pair_tiles : cap;
+    return launch_pair<A_MN, B_MN, EPI>(ma, mb, k, clusters, st);
+}
+
 }  // namespace
 
 tpmlp_status launch_tc_gemm(const Operand& a, const Operand& b, const GemmSpec& g, const DeviceInfo& dev,
                             cudaStream_t st) {
-    CUtensorMap ma, mb;
-    // A: K-major [shards][M][K]; MN-major [shards][K][M].  B: K-major [shards][N][K]; MN-major [shards][K][N].
-    bool ok = a.mn_major ? make_map(&ma, a, g.M, g.K, 64, tc::BK) : make_map(&ma, a, g.K, g.M, tc::BK, tc::BM);
-    if (!ok) return TPMLP_ERR_CUDA;
-    ok = b.mn_major ? make_map(&mb, b, g.N, g.K, 64, tc::BK) : make_map(&mb, b, g.K, g.N, tc::BK, tc::BN);
-    if (!ok) return TPMLP_ERR_CUDA;
-
     tc::KArgs k{};
     k.M = static_cast<int>(g.M);
     k.N = static_cast<int>(g.N);
@@ -117,15 +197,17 @@ tpmlp_status launch_tc_gemm(const Operand& a, const Operand& b, const GemmSpec& 
     k.status = dev.status;
     k.timeout_ns = 2000000000ull;  // 2 s per wait
     if (k.num_tiles == 0) return TPMLP_OK;
-    const int grid = k.num_tiles < dev.sm_count ? k.num_tiles : dev.sm_count;
 
     const bool amn = a.mn_major, bmn = b.mn_major;
-    if (g.epi == EPI_BIAS_ACT && !amn && bmn) return launch_variant<false, true, EPI_BIAS_ACT>(ma, mb, k, grid, dev, st);
-    if (g.epi == EPI_DGELU && !amn && !bmn) return launch_variant<false, false, EPI_DGELU>(ma, mb, k, grid, dev, st);
-    if (g.epi == EPI_STORE && amn && bmn) return launch_variant<true, true, EPI_STORE>(ma, mb, k, grid, dev, st);
-    if (g.epi == EPI_STORE && !amn && !bmn) return launch_variant<false, false, EPI_STORE>(ma, mb, k, grid, dev, st);
+    if (g.epi == EPI_BIAS_ACT && !amn && bmn) return launch_variant<false, true, EPI_BIAS_ACT>(a, b, g, k, dev, st);
+    if (g.epi == EPI_DGELU && !amn && !bmn) return launch_variant<false, false, EPI_DGELU>(a, b, g, k, dev, st);
+    if (g.epi == EPI_STORE && amn && bmn) return launch_variant<true, true, EPI_STORE>(a, b, g, k, dev, st);
+    if (g.epi == EPI_STORE && !amn && !bmn) return launch_variant<false, false, EPI_STORE>(a, b, g, k, dev, st);
     set_error("internal: no tcgen05 GEMM variant for epi=%d a_mn=%d b_mn=%d", g.epi, (int)amn, (int)bmn);
     return TPMLP_ERR_CUDA;
 }
+
+void set_gemm_mode(int mode) { g_gemm_mode.store(mode, std::memory_order_relaxed); }
+int get_gemm_mode() { return g_gemm_mode.load(std::memory_order_relaxed); }
 
 }  // namespace tpmlp

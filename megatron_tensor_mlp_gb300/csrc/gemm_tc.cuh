@@ -370,5 +370,239 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
+
+// ============================================================================
+// CTA-pair variant: a cluster of two CTAs on neighbouring SMs computes one
+// 256x256 output tile with tcgen05.mma.cta_group::2 (M=256, N=256, K=16).
+// CTA r (r = %cluster_ctarank) loads rows [256 mb + 128 r, +128) of A and
+// columns [256 nb + 128 r, +128) of B into its own shared memory; the UMMA
+// reads A from each CTA and exchanges the B halves in hardware, and writes
+// rows 128 r .. 128 r + 127 of the tile into CTA r's tensor memory.  So each
+// SM holds half as many B bytes per stage as the single-CTA kernel (32 KiB
+// stages, six in flight) and the pair reads a third fewer bytes from L2.
+//
+//   leader (r = 0)  warp 0: TMA producer, arms its full barrier for both CTAs'
+//                            bytes (the peer's copies complete on it too)
+//                   warp 1: UMMA issuer; commits multicast to both CTAs'
+//                            empty / tmem-full barriers
+//   peer   (r = 1)  warp 0: TMA producer (gated by its own empty barrier)
+//   both            warp 1: TMEM allocation (collective for the pair)
+//                   warps 4-11: epilogue of its 128 rows; the accumulator is
+//                            released by 16 arrivals on the leader's barrier
+// ============================================================================
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = BM * BK * 2;        // 16 KiB: this CTA's 128 rows of A
+constexpr int P_B_BYTES = (BN / 2) * BK * 2;  // 16 KiB: this CTA's 128 columns of B
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + BAR_BYTES;
+
+template <bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const KArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + P_STAGES * P_A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
+    uint64_t* empty = full + P_STAGES;
+    uint64_t* tfull = empty + P_STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int cluster_id = blockIdx.x >> 1;
+    const int n_clusters = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P_STAGES; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull + a, 1);
+            mbar_init(tempty + a, 2 * NUM_EPI_WARPS);
+        }
+        mbar_init(drain, 1);
+        fence_mbarrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // the peer may signal the leader's barriers from here on
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------------ producer (both CTAs)
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0, last_parity = 0;
+            bool ok = true;
+            for (int t = cluster_id; t < p.num_tiles && ok; t += n_clusters) {
+                int mb, nb, shard;
+                decode_tile(p, t, mb, nb, shard);
+                const int row0 = mb * (2 * BM) + static_cast<int>(rank) * BM;
+                const int col0 = nb * BN + static_cast<int>(rank) * (BN / 2);
+                for (int it = 0; it < p.k_iters; ++it) {
+                    int ks, kb;
+                    if (p.sum_shards) {
+                        ks = it / p.kb_per_shard;
+                        kb = it - ks * p.kb_per_shard;
+                    } else {
+                        ks = shard;
+                        kb = it;
+                    }
+                    const int sa = p.sum_shards ? ks : (p.a_batched ? shard : 0);
+                    const int sb = p.sum_shards ? ks : (p.b_batched ? shard : 0);
+                    if (!mbar_wait_bounded(empty + stage, phase ^ 1u, p.status, p.timeout_ns, kWhereProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) {
+                        mbar_arrive_expect_tx(full + stage, 2 * P_STAGE_BYTES);
+                        armed |= 1u << stage;
+                        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                    }
+                    const uint32_t bar = mapa_shared(smem_u32(full + stage), 0);
+                    uint8_t* a_dst = sA + stage * P_A_BYTES;
+                    uint8_t* b_dst = sB + stage * P_B_BYTES;
+                    const int k0 = kb * BK;
+                    if constexpr (!A_MN) {
+                        tma_load_3d_pair(a_dst, &tmA, bar, k0, row0, sa);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < BM / 64; ++c)
+                            tma_load_3d_pair(a_dst + c * MN_CHUNK_BYTES, &tmA, bar, row0 + c * 64, k0, sa);
+                    }
+                    if constexpr (!B_MN) {
+                        tma_load_3d_pair(b_dst, &tmB, bar, k0, col0, sb);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < (BN / 2) / 64; ++c)
+                            tma_load_3d_pair(b_dst + c * MN_CHUNK_BYTES, &tmB, bar, col0 + c * 64, k0, sb);
+                    }
+                    if (++stage == P_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                if (leader) {
+                    // the leader's full barriers count both CTAs' copies: wait for all of them
+                    for (int s = 0; s < P_STAGES; ++s)
+                        if (armed & (1u << s))
+                            mbar_wait_bounded(full + s, (last_parity >> s) & 1u, p.status, p.timeout_ns, kWhereDrain,
+                                              /*watch_status=*/false);
+                } else {
+                    spin_ns(200000);  // let this CTA's last copies land before it can exit
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            if (leader) {
+                // -------------------------------------------------------- UMMA issuer (leader)
+                constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
+                int stage = 0;
+                uint32_t phase = 0;
+                int lt = 0;
+                bool ok = true;
+                for (int t = cluster_id; t < p.num_tiles && ok; t += n_clusters, ++lt) {
+                    const int acc = lt & 1;
+                    const uint32_t acc_phase = (lt >> 1) & 1;
+                    if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, p.status, p.timeout_ns, kWhereMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + acc * BN;
+                    for (int it = 0; it < p.k_iters; ++it) {
+                        if (!mbar_wait_bounded(full + stage, phase, p.status, p.timeout_ns, kWhereMma)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_base = smem_u32(sA + stage * P_A_BYTES);
+                        const uint32_t b_base = smem_u32(sB + stage * P_B_BYTES);
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            uint64_t adesc, bdesc;
+                            if constexpr (!A_MN) adesc = sdesc_sw128(a_base + kk * 32, 16, 1024);
+                            else adesc = sdesc_sw128(a_base + kk * 2048, TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES);
+                            if constexpr (!B_MN) bdesc = sdesc_sw128(b_base + kk * 32, 16, 1024);
+                            else bdesc = sdesc_sw128(b_base + kk * 2048, TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES);
+                            umma_f16_pair(d_tmem, adesc, bdesc, idesc, (it | kk) != 0 ? 1u : 0u);
+                        }
+                        umma_commit_pair_mc(empty + stage, 0x3);
+                        if (++stage == P_STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (ok) umma_commit_pair_mc(tfull + acc, 0x3);
+                }
+                umma_commit_pair_mc(drain, 0x3);
+            }
+            // both CTAs: every UMMA (and its multicast arrivals) is done once `drain` flips
+            mbar_wait_bounded(drain, 0, p.status, p.timeout_ns, kWhereDrain, /*watch_status=*/false);
+        }
+    } else if (warp >= FIRST_EPI_WARP) {
+        // ---------------------------------------------------------------- epilogue (both CTAs)
+        const int q = warp & 3;
+        const int half = (warp - FIRST_EPI_WARP) >> 2;
+        const uint32_t tempty_leader0 = mapa_shared(smem_u32(tempty), 0);
+        int lt = 0;
+        for (int t = cluster_id; t < p.num_tiles; t += n_clusters, ++lt) {
+            const int acc = lt & 1;
+            const uint32_t acc_phase = (lt >> 1) & 1;
+            int okw = 0;
+            if (lane == 0) okw = mbar_wait_bounded(tfull + acc, acc_phase, p.status, p.timeout_ns, kWhereEpilogue);
+            okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+            if (!okw) break;
+            tc_fence_after();
+            int mb, nb, shard;
+            decode_tile(p, t, mb, nb, shard);
+            const int gm = mb * (2 * BM) + static_cast<int>(rank) * BM + q * 32 + lane;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                const int col = half * 128 + c * 32;
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(t_row + col, r);
+                tmem_ld_wait();
+                epilogue_chunk<EPI>(p, r, gm, nb * BN + col, shard);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_leader0 + acc * 8);
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // no CTA leaves while its peer may still touch its shared or tensor memory
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
 }  // namespace tc
 }  // namespace tpmlp

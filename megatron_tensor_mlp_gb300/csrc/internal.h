@@ -69,4 +69,8 @@ tpmlp_status launch_qkv_interleave(const void* src, void* dst, int64_t rows, int
                                    int esize, bool inverse, cudaStream_t st);
 tpmlp_status launch_debug_wait(uint32_t timeout_us, uint32_t* status, cudaStream_t st);
 
+// Process-wide GEMM tiling mode (see tpmlp_set_gemm_mode).
+void set_gemm_mode(int mode);
+int get_gemm_mode();
+
 }  // namespace tpmlp

@@ -497,4 +497,15 @@ const char* tpmlp_last_error(void) { return t_err; }
 
 int tpmlp_version(void) { return 100; }
 
+tpmlp_status tpmlp_set_gemm_mode(int mode) {
+    if (mode < 0 || mode > 2) {
+        set_error("gemm mode must be 0 (automatic), 1 (single-CTA tiles) or 2 (CTA-pair tiles)");
+        return TPMLP_ERR_SHAPE;
+    }
+    set_gemm_mode(mode);
+    return TPMLP_OK;
+}
+
+int tpmlp_get_gemm_mode(void) { return get_gemm_mode(); }
+
 }  // extern "C"

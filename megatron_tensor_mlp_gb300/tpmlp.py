@@ -42,6 +42,7 @@ _SIGS = {
     "tpmlp_qkv_interleave": [_vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32, _vp],
     "tpmlp_device_status": [_vp],
     "tpmlp_debug_wait_timeout": [_u32, _vp],
+    "tpmlp_set_gemm_mode": [_i32],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(lib, _name)
@@ -53,6 +54,8 @@ lib.tpmlp_status_string.argtypes = [ctypes.c_int]
 lib.tpmlp_status_string.restype = ctypes.c_char_p
 lib.tpmlp_last_error.argtypes = []
 lib.tpmlp_last_error.restype = ctypes.c_char_p
+lib.tpmlp_get_gemm_mode.argtypes = []
+lib.tpmlp_get_gemm_mode.restype = ctypes.c_int
 lib.tpmlp_version.argtypes = []
 lib.tpmlp_version.restype = ctypes.c_int
 
@@ -155,6 +158,17 @@ def tpmlp_device_status(stream=None, check=True):
 
 def tpmlp_debug_wait_timeout(timeout_us, stream=None, check=True):
     return _done(lib.tpmlp_debug_wait_timeout(timeout_us, _stream(stream)), check)
+
+
+GEMM_AUTO, GEMM_SINGLE, GEMM_PAIR = 0, 1, 2
+
+
+def tpmlp_set_gemm_mode(mode, check=True):
+    return _done(lib.tpmlp_set_gemm_mode(mode), check)
+
+
+def tpmlp_get_gemm_mode() -> int:
+    return int(lib.tpmlp_get_gemm_mode())
 
 
 def tpmlp_status_string(st: int) -> str:

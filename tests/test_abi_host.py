@@ -80,6 +80,14 @@ def test_bwd_and_layout_validation():
     assert T.tpmlp_debug_wait_timeout(0, check=False) == T.ERR_SHAPE
 
 
+def test_gemm_mode_control():
+    assert T.tpmlp_set_gemm_mode(3, check=False) == T.ERR_SHAPE
+    assert T.tpmlp_set_gemm_mode(-1, check=False) == T.ERR_SHAPE
+    for m in (1, 2, 0):
+        assert T.tpmlp_set_gemm_mode(m) == T.OK
+        assert T.tpmlp_get_gemm_mode() == m
+
+
 def test_qkv_src_col_matches_oracle(orc):
     for (h, n) in [(12, 4), (64, 8), (24, 3), (8, 8), (16, 1)]:
         for c in range(3 * h):

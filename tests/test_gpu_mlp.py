@@ -17,6 +17,15 @@ def env():
     return harness, synth, tpmlp
 
 
+@pytest.fixture(params=[1, 2], ids=["single-cta", "cta-pair"])
+def gemm_mode(request, env):
+    """Force 128x256 single-CTA tiles or 256x256 CTA-pair tiles for the test."""
+    T = env[2]
+    T.tpmlp_set_gemm_mode(request.param)
+    yield request.param
+    T.tpmlp_set_gemm_mode(0)
+
+
 # (s, b, h, ffn, p): tiles are 128 (tokens) x 256 (outputs) x 64 (reduction)
 SHAPES = [
     (25, 8, 72, 264, 3),      # M=200 ragged, h=72 ragged K, fs=88 ragged N
@@ -60,7 +69,7 @@ def _run_and_check(env, orc, wl, check_bwd=True):
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "s{}b{}h{}f{}p{}".format(*s))
-def test_bf16_fwd_bwd_small(env, orc, shape):
+def test_bf16_fwd_bwd_small(env, orc, shape, gemm_mode):
     _, synth, _ = env
     wl = synth.custom(*shape, dtype="bf16", sigma_w=0.05, sigma_bias=0.05, seed=sum(shape))
     _run_and_check(env, orc, wl)
@@ -79,7 +88,7 @@ def test_f32_small(env, orc, shape):
     _run_and_check(env, orc, wl)
 
 
-def test_every_divisor_p(env, orc):
+def test_every_divisor_p(env, orc, gemm_mode):
     """Sharded == unsharded for every legal p of one small problem (forward)."""
     _, synth, _ = env
     h, ffn = 96, 384
@@ -88,7 +97,7 @@ def test_every_divisor_p(env, orc):
         _run_and_check(env, orc, wl, check_bwd=False)
 
 
-def test_column_and_row_entry_points(env, orc):
+def test_column_and_row_entry_points(env, orc, gemm_mode):
     """tpmlp_column_fwd (GeLU and identity) and tpmlp_row_fwd on their own."""
     import torch
     harness, synth, T = env
@@ -133,7 +142,7 @@ def test_bias_added_once(env, orc):
     assert np.max(np.abs(diff - b2)) < 0.02 * np.max(np.abs(b2)) + 0.02
 
 
-def test_deterministic(env, orc):
+def test_deterministic(env, orc, gemm_mode):
     harness, synth, T = env
     wl = synth.custom(50, 6, 256, 1024, 4, dtype="bf16", seed=2)
     buf = harness.MLPBuffers(wl, backward=True)
@@ -149,7 +158,7 @@ def test_deterministic(env, orc):
         assert torch.equal(a, b_), "results differ between runs"
 
 
-def test_guard_canaries(env, orc):
+def test_guard_canaries(env, orc, gemm_mode):
     """Outputs written through pointers into the middle of larger buffers leave the
     surrounding guard bytes untouched."""
     import torch
@@ -195,3 +204,21 @@ def test_empty_batch(env):
     assert T.tpmlp_mlp_fwd(dummy, dummy, None, dummy, None, out, ws, None, 0, 4, 64, 256, 2) == T.OK
     T.tpmlp_device_status()
     assert bool((out == 3.0).all()) and bool((ws == 3.0).all())
+
+
+def test_single_and_pair_tiles_agree(env, orc):
+    """The two tilings accumulate in the same K order per element: results are bit-identical."""
+    import torch
+    harness, synth, T = env
+    wl = synth.custom(150, 4, 384, 1536, 3, dtype="bf16", seed=9)
+    buf = harness.MLPBuffers(wl, backward=True)
+    out = {}
+    for mode in (1, 2):
+        T.tpmlp_set_gemm_mode(mode)
+        buf.fwd()
+        buf.bwd()
+        T.tpmlp_device_status()
+        out[mode] = [t.clone() for t in (buf.Z, buf.Y, buf.dX, buf.dA_sh, buf.dB_sh)]
+    T.tpmlp_set_gemm_mode(0)
+    for a, b_ in zip(out[1], out[2]):
+        assert torch.equal(a, b_)
