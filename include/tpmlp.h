@@ -130,6 +130,35 @@ tpmlp_status tpmlp_mlp_bwd(const void* X, const void* A_sh, const void* B_sh, co
                            tpmlp_dtype dt, tpmlp_dtype grad_dt, void* stream);
 
 /*
+ * Row-parallel layer backward (Level 2, M026: the row layer's input gradient is
+ * naturally the input shard; its weight gradient is local):
+ *   dY_i = dZ B_i^T            act = NONE
+ *   dY_i = (dZ B_i^T) * GeLU'(H_i)   act = GELU_ERF: the gradient at the column
+ *                                     layer's pre-activation, GeLU'(z) = Phi(z) + z phi(z)
+ *   dB_i = Y_i^T dZ,  db2 = 1^T dZ (optional)
+ * Inputs:  Y_sh [p][M][ffn/p] (this layer's input), B_sh [p][ffn/p][h], dZ [M,h] (dt);
+ *          H_sh [p][M][ffn/p] (dt; required iff act = GELU_ERF, else ignored).
+ * Outputs: dY_sh [p][M][ffn/p] dt;  dB_sh [p][ffn/p][h] and db2 [h] (or NULL) grad_dt.
+ * Requires ffn % p == 0; grad_dt must be TPMLP_F32 when dt is TPMLP_F32.
+ */
+tpmlp_status tpmlp_row_bwd(const void* Y_sh, const void* B_sh, const void* dZ, const void* H_sh, void* dY_sh,
+                           void* dB_sh, void* db2, int64_t s, int64_t b, int64_t h, int64_t ffn, int p,
+                           tpmlp_dtype dt, tpmlp_dtype grad_dt, tpmlp_act act, void* stream);
+
+/*
+ * Column-parallel layer backward (Level 2, M025 追问: dW_i = X^T dY_i is local;
+ * the input-gradient contributions dY_i W_i^T of all shards are summed):
+ *   dA_i = X^T dY_i,  db1_i = 1^T dY_i (optional),  dX = sum_i dY_i A_i^T (summed on device)
+ * Inputs:  X [M,h], A_sh [p][h][ffn/p], dY_sh [p][M][ffn/p] (dt).
+ * Outputs: dX [M,h] dt;  dA_sh [p][h][ffn/p] and db1_sh [p][ffn/p] (or NULL) grad_dt.
+ * Requires ffn % p == 0; grad_dt must be TPMLP_F32 when dt is TPMLP_F32.
+ * tpmlp_mlp_bwd is tpmlp_row_bwd (GeLU') followed by tpmlp_column_bwd.
+ */
+tpmlp_status tpmlp_column_bwd(const void* X, const void* A_sh, const void* dY_sh, void* dX, void* dA_sh,
+                              void* db1_sh, int64_t s, int64_t b, int64_t h, int64_t ffn, int p,
+                              tpmlp_dtype dt, tpmlp_dtype grad_dt, void* stream);
+
+/*
  * The MLP block forward without a caller workspace.  The pages have no
  * counterpart: this entry point exists for callers that cannot allocate device
  * memory where they run the block (for example an inference-engine plugin whose
@@ -206,6 +235,15 @@ tpmlp_status tpmlp_debug_wait_timeout(uint32_t timeout_us, void* stream);
  */
 tpmlp_status tpmlp_set_gemm_mode(int mode);
 int tpmlp_get_gemm_mode(void);
+
+/*
+ * Raster order of the output tiles, process wide: tiles are visited in groups
+ * of group_m consecutive M-blocks (all N-blocks of a group before the next
+ * group), so that CTAs running at the same time share operand panels in L2.
+ * Default 16; 1..1024, else TPMLP_ERR_SHAPE.  Affects speed only.
+ */
+tpmlp_status tpmlp_set_gemm_raster(int group_m);
+int tpmlp_get_gemm_raster(void);
 
 /* Human-readable name of a status code. */
 const char* tpmlp_status_string(tpmlp_status st);

@@ -55,6 +55,7 @@ bool make_map(CUtensorMap* map, const Operand& op, uint64_t inner, uint64_t oute
 }
 
 std::atomic<int> g_gemm_mode{0};  // 0 automatic, 1 single-CTA tiles, 2 CTA-pair tiles
+std::atomic<int> g_group_m{16};  // M-blocks per raster group
 
 template <typename Kern>
 bool set_smem_attr(Kern kern, int device, int bytes, bool* done) {
@@ -180,7 +181,7 @@ tpmlp_status launch_tc_gemm(const Operand& a, const Operand& b, const GemmSpec& 
     k.num_tiles = k.m_blocks * k.n_blocks * k.batch;
     k.kb_per_shard = static_cast<int>((g.K + tc::BK - 1) / tc::BK);
     k.k_iters = g.sum_shards ? k.kb_per_shard * k.n_shards : k.kb_per_shard;
-    k.group_m = 16;
+    k.group_m = g_group_m.load(std::memory_order_relaxed);
     k.act = g.act;
     k.out_f32 = g.out_f32 ? 1 : 0;
     k.out = g.out;
@@ -208,6 +209,8 @@ tpmlp_status launch_tc_gemm(const Operand& a, const Operand& b, const GemmSpec& 
 }
 
 void set_gemm_mode(int mode) { g_gemm_mode.store(mode, std::memory_order_relaxed); }
+void set_group_m(int g) { g_group_m.store(g, std::memory_order_relaxed); }
+int get_group_m() { return g_group_m.load(std::memory_order_relaxed); }
 int get_gemm_mode() { return g_gemm_mode.load(std::memory_order_relaxed); }
 
 }  // namespace tpmlp

@@ -72,5 +72,7 @@ tpmlp_status launch_debug_wait(uint32_t timeout_us, uint32_t* status, cudaStream
 // Process-wide GEMM tiling mode (see tpmlp_set_gemm_mode).
 void set_gemm_mode(int mode);
 int get_gemm_mode();
+void set_group_m(int g);
+int get_group_m();
 
 }  // namespace tpmlp

@@ -174,6 +174,70 @@ tpmlp_status do_row(const void* Y_sh, const void* B_sh, const void* b2, void* Z,
     return run_gemm(a, b, g, dt, dev, st);
 }
 
+// Row layer backward: dY_i = dZ B_i^T (times GeLU'(H_i) when act is GeLU), dB_i = Y_i^T dZ, db2.
+tpmlp_status do_row_bwd(const void* Y_sh, const void* B_sh, const void* dZ, const void* H_sh, void* dY_sh,
+                        void* dB_sh, void* db2, int64_t M, int64_t h, int64_t ffn, int p, tpmlp_dtype dt,
+                        bool grad_f32, int act, const DeviceInfo& dev, cudaStream_t st) {
+    const int64_t fs = ffn / p;
+    {
+        Operand a{dZ, h, 0, 1, false};               // dZ [M][h]: [M][K]
+        Operand bb{B_sh, h, fs * h, p, false};       // B_i [fs][h]: [N][K], K-major
+        GemmSpec g = spec_base();
+        g.M = M; g.N = fs; g.K = h; g.n_shards = p;
+        g.a_batched = false; g.b_batched = true;
+        if (act == TPMLP_ACT_GELU_ERF) {
+            g.epi = EPI_DGELU;
+            g.aux = H_sh; g.aux_ld = fs; g.aux_ss = M * fs;
+        } else {
+            g.epi = EPI_STORE;
+            g.out_f32 = (dt == TPMLP_F32);
+        }
+        g.out = dY_sh; g.out_ld = fs; g.out_ss = M * fs;
+        TP_TRY(run_gemm(a, bb, g, dt, dev, st));
+    }
+    if (db2) TP_TRY(launch_colsum(dZ, dt == TPMLP_F32, 1, M, h, db2, grad_f32, st));
+    {
+        Operand a{Y_sh, fs, M * fs, p, true};        // Y_i [M][fs]: [K][M_gemm], MN-major
+        Operand bb{dZ, h, 0, 1, true};               // dZ [M][h]: [K][N], MN-major
+        GemmSpec g = spec_base();
+        g.M = fs; g.N = h; g.K = M; g.n_shards = p;
+        g.a_batched = true; g.b_batched = false;
+        g.epi = EPI_STORE; g.out_f32 = grad_f32;
+        g.out = dB_sh; g.out_ld = h; g.out_ss = fs * h;
+        TP_TRY(run_gemm(a, bb, g, dt, dev, st));
+    }
+    return TPMLP_OK;
+}
+
+// Column layer backward: dA_i = X^T dY_i, db1_i = 1^T dY_i, dX = sum_i dY_i A_i^T.
+tpmlp_status do_column_bwd(const void* X, const void* A_sh, const void* dY_sh, void* dX, void* dA_sh, void* db1_sh,
+                           int64_t M, int64_t h, int64_t ffn, int p, tpmlp_dtype dt, bool grad_f32,
+                           const DeviceInfo& dev, cudaStream_t st) {
+    const int64_t fs = ffn / p;
+    if (db1_sh) TP_TRY(launch_colsum(dY_sh, dt == TPMLP_F32, p, M, fs, db1_sh, grad_f32, st));
+    {
+        Operand a{X, h, 0, 1, true};                 // X [M][h]: [K][M_gemm], MN-major
+        Operand bb{dY_sh, fs, M * fs, p, true};      // dY_i [M][fs]: [K][N], MN-major
+        GemmSpec g = spec_base();
+        g.M = h; g.N = fs; g.K = M; g.n_shards = p;
+        g.a_batched = false; g.b_batched = true;
+        g.epi = EPI_STORE; g.out_f32 = grad_f32;
+        g.out = dA_sh; g.out_ld = fs; g.out_ss = h * fs;
+        TP_TRY(run_gemm(a, bb, g, dt, dev, st));
+    }
+    {
+        Operand a{dY_sh, fs, M * fs, p, false};      // dY_i [M][fs], K-major
+        Operand bb{A_sh, fs, h * fs, p, false};      // A_i [h][fs]: [N][K], K-major
+        GemmSpec g = spec_base();
+        g.M = M; g.N = h; g.K = fs; g.n_shards = p;
+        g.sum_shards = true;
+        g.epi = EPI_STORE; g.out_f32 = (dt == TPMLP_F32);
+        g.out = dX; g.out_ld = h; g.out_ss = 0;
+        TP_TRY(run_gemm(a, bb, g, dt, dev, st));
+    }
+    return TPMLP_OK;
+}
+
 }  // namespace
 
 void set_error(const char* fmt, ...) {
@@ -319,56 +383,69 @@ tpmlp_status tpmlp_mlp_bwd(const void* X, const void* A_sh, const void* B_sh, co
     if (M == 0) return TPMLP_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool gf32 = grad_dt == TPMLP_F32;
+    // row layer backward with GeLU' fused: dH_i = (dZ B_i^T) * GeLU'(H_i); dB_i; db2
+    TP_TRY(do_row_bwd(Y_sh, B_sh, dZ, H_sh, dH_ws, dB_sh, db2, M, h, ffn, p, dt, gf32, TPMLP_ACT_GELU_ERF, *dev, st));
+    // column layer backward from dH: dA_i; db1_i; dX = sum_i dH_i A_i^T
+    return do_column_bwd(X, A_sh, dH_ws, dX, dA_sh, db1_sh, M, h, ffn, p, dt, gf32, *dev, st);
+}
 
-    // 1. dH_i = (dZ B_i^T) * GeLU'(H_i)
-    {
-        Operand a{dZ, h, 0, 1, false};               // dZ [M][h]: [M][K]
-        Operand bb{B_sh, h, fs * h, p, false};       // B_i [fs][h]: [N][K], K-major
-        GemmSpec g = spec_base();
-        g.M = M; g.N = fs; g.K = h; g.n_shards = p;
-        g.a_batched = false; g.b_batched = true;
-        g.epi = EPI_DGELU;
-        g.aux = H_sh; g.aux_ld = fs; g.aux_ss = M * fs;
-        g.out = dH_ws; g.out_ld = fs; g.out_ss = M * fs;
-        TP_TRY(run_gemm(a, bb, g, dt, *dev, st));
+tpmlp_status tpmlp_row_bwd(const void* Y_sh, const void* B_sh, const void* dZ, const void* H_sh, void* dY_sh,
+                           void* dB_sh, void* db2, int64_t s, int64_t b, int64_t h, int64_t ffn, int p, tpmlp_dtype dt,
+                           tpmlp_dtype grad_dt, tpmlp_act act, void* stream) {
+    if (!Y_sh || !B_sh || !dZ || !dY_sh || !dB_sh || (act == TPMLP_ACT_GELU_ERF && !H_sh)) {
+        set_error("Y_sh, B_sh, dZ, dY_sh, dB_sh (and H_sh when act is GeLU) must not be NULL");
+        return TPMLP_ERR_NULL;
     }
-    // 2. bias gradients (column sums)
-    if (db1_sh) TP_TRY(launch_colsum(dH_ws, dt == TPMLP_F32, p, M, fs, db1_sh, gf32, st));
-    if (db2) TP_TRY(launch_colsum(dZ, dt == TPMLP_F32, 1, M, h, db2, gf32, st));
-    // 3. dB_i = Y_i^T dZ   ([fs][h] per shard, K = tokens)
-    {
-        Operand a{Y_sh, fs, M * fs, p, true};        // Y_i [M][fs]: [K][M_gemm], MN-major
-        Operand bb{dZ, h, 0, 1, true};               // dZ [M][h]: [K][N], MN-major
-        GemmSpec g = spec_base();
-        g.M = fs; g.N = h; g.K = M; g.n_shards = p;
-        g.a_batched = true; g.b_batched = false;
-        g.epi = EPI_STORE; g.out_f32 = gf32;
-        g.out = dB_sh; g.out_ld = h; g.out_ss = fs * h;
-        TP_TRY(run_gemm(a, bb, g, dt, *dev, st));
+    TP_TRY(check_mlp_shape(s, b, h, ffn, p, false));
+    TP_TRY(check_dtype(dt));
+    TP_TRY(check_dtype(grad_dt));
+    if (act != TPMLP_ACT_NONE && act != TPMLP_ACT_GELU_ERF) {
+        set_error("unknown activation %d", (int)act);
+        return TPMLP_ERR_DTYPE;
     }
-    // 4. dA_i = X^T dH_i   ([h][fs] per shard, K = tokens)
-    {
-        Operand a{X, h, 0, 1, true};                 // X [M][h]: [K][M_gemm], MN-major
-        Operand bb{dH_ws, fs, M * fs, p, true};      // dH_i [M][fs]: [K][N], MN-major
-        GemmSpec g = spec_base();
-        g.M = h; g.N = fs; g.K = M; g.n_shards = p;
-        g.a_batched = false; g.b_batched = true;
-        g.epi = EPI_STORE; g.out_f32 = gf32;
-        g.out = dA_sh; g.out_ld = fs; g.out_ss = h * fs;
-        TP_TRY(run_gemm(a, bb, g, dt, *dev, st));
+    if (dt == TPMLP_F32 && grad_dt != TPMLP_F32) {
+        set_error("grad_dt must be TPMLP_F32 when dt is TPMLP_F32");
+        return TPMLP_ERR_DTYPE;
     }
-    // 5. dX = sum_i dH_i A_i^T   (shard sum in the K loop)
-    {
-        Operand a{dH_ws, fs, M * fs, p, false};      // dH_i [M][fs]: [M][K]
-        Operand bb{A_sh, fs, h * fs, p, false};      // A_i [h][fs]: [N][K], K-major
-        GemmSpec g = spec_base();
-        g.M = M; g.N = h; g.K = fs; g.n_shards = p;
-        g.sum_shards = true;
-        g.epi = EPI_STORE; g.out_f32 = (dt == TPMLP_F32);
-        g.out = dX; g.out_ld = h; g.out_ss = 0;
-        TP_TRY(run_gemm(a, bb, g, dt, *dev, st));
+    const int64_t M = s * b, fs = ffn / p, es = esize(dt), gs = esize(grad_dt);
+    TP_TRY(check_aligned({Y_sh, B_sh, dZ, H_sh, dY_sh, dB_sh, db2}));
+    TP_TRY(check_pitch(h, dt, "h"));
+    TP_TRY(check_pitch(fs, dt, "ffn/p"));
+    TP_TRY(check_alias({{dY_sh, M * ffn * es}, {dB_sh, ffn * h * gs}, {db2, h * gs}},
+                       {{Y_sh, M * ffn * es}, {B_sh, ffn * h * es}, {dZ, M * h * es},
+                        {act == TPMLP_ACT_GELU_ERF ? H_sh : nullptr, M * ffn * es}}));
+    const DeviceInfo* dev;
+    TP_TRY(get_device(&dev));
+    if (M == 0) return TPMLP_OK;
+    return do_row_bwd(Y_sh, B_sh, dZ, H_sh, dY_sh, dB_sh, db2, M, h, ffn, p, dt, grad_dt == TPMLP_F32, act, *dev,
+                      static_cast<cudaStream_t>(stream));
+}
+
+tpmlp_status tpmlp_column_bwd(const void* X, const void* A_sh, const void* dY_sh, void* dX, void* dA_sh, void* db1_sh,
+                              int64_t s, int64_t b, int64_t h, int64_t ffn, int p, tpmlp_dtype dt, tpmlp_dtype grad_dt,
+                              void* stream) {
+    if (!X || !A_sh || !dY_sh || !dX || !dA_sh) {
+        set_error("only db1_sh may be NULL");
+        return TPMLP_ERR_NULL;
     }
-    return TPMLP_OK;
+    TP_TRY(check_mlp_shape(s, b, h, ffn, p, false));
+    TP_TRY(check_dtype(dt));
+    TP_TRY(check_dtype(grad_dt));
+    if (dt == TPMLP_F32 && grad_dt != TPMLP_F32) {
+        set_error("grad_dt must be TPMLP_F32 when dt is TPMLP_F32");
+        return TPMLP_ERR_DTYPE;
+    }
+    const int64_t M = s * b, fs = ffn / p, es = esize(dt), gs = esize(grad_dt);
+    TP_TRY(check_aligned({X, A_sh, dY_sh, dX, dA_sh, db1_sh}));
+    TP_TRY(check_pitch(h, dt, "h"));
+    TP_TRY(check_pitch(fs, dt, "ffn/p"));
+    TP_TRY(check_alias({{dX, M * h * es}, {dA_sh, h * ffn * gs}, {db1_sh, ffn * gs}},
+                       {{X, M * h * es}, {A_sh, h * ffn * es}, {dY_sh, M * ffn * es}}));
+    const DeviceInfo* dev;
+    TP_TRY(get_device(&dev));
+    if (M == 0) return TPMLP_OK;
+    return do_column_bwd(X, A_sh, dY_sh, dX, dA_sh, db1_sh, M, h, ffn, p, dt, grad_dt == TPMLP_F32, *dev,
+                         static_cast<cudaStream_t>(stream));
 }
 
 static tpmlp_status shard_common(const void* src, void* dst, int64_t rows, int64_t cols, int p, tpmlp_dtype dt,
@@ -507,5 +584,16 @@ tpmlp_status tpmlp_set_gemm_mode(int mode) {
 }
 
 int tpmlp_get_gemm_mode(void) { return get_gemm_mode(); }
+
+tpmlp_status tpmlp_set_gemm_raster(int group_m) {
+    if (group_m < 1 || group_m > 1024) {
+        set_error("group_m must be in 1..1024");
+        return TPMLP_ERR_SHAPE;
+    }
+    set_group_m(group_m);
+    return TPMLP_OK;
+}
+
+int tpmlp_get_gemm_raster(void) { return get_group_m(); }
 
 }  // extern "C"

@@ -37,12 +37,15 @@ _SIGS = {
     "tpmlp_mlp_fwd": [_vp] * 8 + [_i64] * 4 + [_i32, _i32, _vp],
     "tpmlp_mlp_bwd": [_vp] * 12 + [_i64] * 4 + [_i32, _i32, _i32, _vp],
     "tpmlp_mlp_fwd_noalloc": [_vp] * 6 + [_i64] * 4 + [_i32, _i32, _vp],
+    "tpmlp_row_bwd": [_vp] * 7 + [_i64] * 4 + [_i32, _i32, _i32, _i32, _vp],
+    "tpmlp_column_bwd": [_vp] * 6 + [_i64] * 4 + [_i32, _i32, _i32, _vp],
     "tpmlp_shard_columns": [_vp, _vp, _i64, _i64, _i32, _i32, _vp],
     "tpmlp_unshard_columns": [_vp, _vp, _i64, _i64, _i32, _i32, _vp],
     "tpmlp_qkv_interleave": [_vp, _vp, _i64, _i64, _i64, _i32, _i32, _i32, _vp],
     "tpmlp_device_status": [_vp],
     "tpmlp_debug_wait_timeout": [_u32, _vp],
     "tpmlp_set_gemm_mode": [_i32],
+    "tpmlp_set_gemm_raster": [_i32],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(lib, _name)
@@ -54,6 +57,8 @@ lib.tpmlp_status_string.argtypes = [ctypes.c_int]
 lib.tpmlp_status_string.restype = ctypes.c_char_p
 lib.tpmlp_last_error.argtypes = []
 lib.tpmlp_last_error.restype = ctypes.c_char_p
+lib.tpmlp_get_gemm_raster.argtypes = []
+lib.tpmlp_get_gemm_raster.restype = ctypes.c_int
 lib.tpmlp_get_gemm_mode.argtypes = []
 lib.tpmlp_get_gemm_mode.restype = ctypes.c_int
 lib.tpmlp_version.argtypes = []
@@ -125,6 +130,20 @@ def tpmlp_mlp_bwd(X, A_sh, B_sh, H_sh, Y_sh, dZ, dX, dA_sh, dB_sh, db1_sh, db2, 
     return _done(st, check)
 
 
+def tpmlp_row_bwd(Y_sh, B_sh, dZ, H_sh, dY_sh, dB_sh, db2, s, b, h, ffn, p, dt=BF16, grad_dt=F32, act=ACT_NONE,
+                  stream=None, check=True):
+    st = lib.tpmlp_row_bwd(_ptr(Y_sh), _ptr(B_sh), _ptr(dZ), _ptr(H_sh), _ptr(dY_sh), _ptr(dB_sh), _ptr(db2), s, b, h,
+                           ffn, p, dt, grad_dt, act, _stream(stream))
+    return _done(st, check)
+
+
+def tpmlp_column_bwd(X, A_sh, dY_sh, dX, dA_sh, db1_sh, s, b, h, ffn, p, dt=BF16, grad_dt=F32, stream=None,
+                     check=True):
+    st = lib.tpmlp_column_bwd(_ptr(X), _ptr(A_sh), _ptr(dY_sh), _ptr(dX), _ptr(dA_sh), _ptr(db1_sh), s, b, h, ffn,
+                              p, dt, grad_dt, _stream(stream))
+    return _done(st, check)
+
+
 def tpmlp_mlp_fwd_noalloc(X, A_sh, b1_sh, B_sh, b2, Z, s, b, h, ffn, p, dt=BF16, stream=None, check=True):
     """The block forward with Y kept in the library's fixed array (no caller workspace)."""
     st = lib.tpmlp_mlp_fwd_noalloc(_ptr(X), _ptr(A_sh), _ptr(b1_sh), _ptr(B_sh), _ptr(b2), _ptr(Z), s, b, h, ffn, p,
@@ -169,6 +188,14 @@ def tpmlp_set_gemm_mode(mode, check=True):
 
 def tpmlp_get_gemm_mode() -> int:
     return int(lib.tpmlp_get_gemm_mode())
+
+
+def tpmlp_set_gemm_raster(group_m, check=True):
+    return _done(lib.tpmlp_set_gemm_raster(group_m), check)
+
+
+def tpmlp_get_gemm_raster() -> int:
+    return int(lib.tpmlp_get_gemm_raster())
 
 
 def tpmlp_status_string(st: int) -> str:
