@@ -70,6 +70,10 @@ class Oracle:
         lib.oracle_bwd_dX_rows.argtypes = [i64, i64, i64, i32] + [vp] * 5 + [i64, vp, vp]
         lib.oracle_bwd_ffn_cols.restype = None
         lib.oracle_bwd_ffn_cols.argtypes = [i64, i64, i64, i32] + [vp] * 5 + [i64, vp, vp, vp, vp]
+        lib.oracle_linear_fwd.restype = None
+        lib.oracle_linear_fwd.argtypes = [i64, i64, i64, vp, vp, vp, vp]
+        lib.oracle_linear_bwd.restype = None
+        lib.oracle_linear_bwd.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, vp]
         lib.oracle_bwd_db2.restype = None
         lib.oracle_bwd_db2.argtypes = [i64, i64, vp, vp]
         lib.oracle_shard_columns.restype = None
@@ -136,6 +140,24 @@ class Oracle:
         self.lib.oracle_bwd_ffn_cols(M, h, f, act, _ptr(X), _ptr(A), _ptr(b1), _ptr(B), _ptr(dZ),
                                      n, _ptr(cols), _ptr(dA_c), _ptr(dB_r), _ptr(db1_c))
         return dA_c, dB_r, db1_c
+
+    def linear_fwd(self, X, W, b=None):
+        """Y = X W + b."""
+        X, W, b = _f64(X), _f64(W), _f64(b)
+        M, K = X.shape
+        N = W.shape[1]
+        Y = np.empty((M, N))
+        self.lib.oracle_linear_fwd(M, K, N, _ptr(X), _ptr(W), _ptr(b), _ptr(Y))
+        return Y
+
+    def linear_bwd(self, X, W, dY, with_bias=True):
+        """Returns (dX, dW, db) of Y = X W + b."""
+        X, W, dY = _f64(X), _f64(W), _f64(dY)
+        M, K = X.shape
+        N = W.shape[1]
+        dX = np.empty((M, K)); dW = np.empty((K, N)); db = np.empty(N) if with_bias else None
+        self.lib.oracle_linear_bwd(M, K, N, _ptr(X), _ptr(W), _ptr(dY), _ptr(dX), _ptr(dW), _ptr(db))
+        return dX, dW, db
 
     def bwd_db2(self, dZ):
         """db2 = column sums of dZ."""

@@ -251,6 +251,34 @@ void oracle_bwd_db2(int64_t M, int64_t h, const double* dZ, double* db2) {
         for (int64_t n = 0; n < h; ++n) db2[n] += dZ[m * h + n];
 }
 
+/*
+ * A single parallel linear layer, the building block of the attention
+ * projections ([M2] M025 and M026: Y = X W with W [in, out]; dW = X^T dY is
+ * local; dX = dY W^T; [TI]: QKV is column parallel by heads, the output
+ * projection row parallel).
+ *   Y = X W + 1 b^T                  X [M,K], W [K,N], b [N] (may be NULL)
+ *   dX = dY W^T,  dW = X^T dY,  db = 1^T dY   (db may be NULL)
+ */
+void oracle_linear_fwd(int64_t M, int64_t K, int64_t N, const double* X, const double* W, const double* b,
+                       double* Y) {
+    matmul_nn(M, K, N, X, W, Y);
+    if (b) {
+        for (int64_t m = 0; m < M; ++m)
+            for (int64_t n = 0; n < N; ++n) Y[m * N + n] += b[n];
+    }
+}
+
+void oracle_linear_bwd(int64_t M, int64_t K, int64_t N, const double* X, const double* W, const double* dY,
+                       double* dX, double* dW, double* db) {
+    matmul_nt(M, N, K, dY, W, dX);  /* dX = dY W^T  [M,K] */
+    matmul_tn(K, M, N, X, dY, dW);  /* dW = X^T dY  [K,N] */
+    if (db) {
+        for (int64_t n = 0; n < N; ++n) db[n] = 0.0;
+        for (int64_t m = 0; m < M; ++m)
+            for (int64_t n = 0; n < N; ++n) db[n] += dY[m * N + n];
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Layout maps (integer index work; compared bit for bit).                   */
 

@@ -286,6 +286,54 @@ def pin_qkv_interleave_heads_on_one_rank(orc):
         assert abs(lhs - rhs) <= 1e-12 * abs(lhs) + 1e-12
 
 
+# --------------------------------------------------------------------------
+# Linear layer (attention projections; [M2] M025/M026, [TI] QKV by heads)
+
+def pin_linear_vs_numpy_and_fd(orc):
+    r = _rng(11)
+    M, K, N = 7, 9, 12
+    X = r.standard_normal((M, K)); W = r.standard_normal((K, N)); b = r.standard_normal(N)
+    dY = r.standard_normal((M, N))
+    Y = orc.linear_fwd(X, W, b)
+    assert np.max(np.abs(Y - (X @ W + b))) <= 1e-13 * np.max(np.abs(Y))
+    dX, dW, db = orc.linear_bwd(X, W, dY)
+    for name, arr, g in (("X", X, dX), ("W", W, dW), ("b", b, db)):
+        fd = np.zeros_like(arr)
+        it = np.nditer(arr, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            x0 = arr[idx]
+            eps = 1e-6 * max(1.0, abs(x0))
+            arr[idx] = x0 + eps
+            lp = float(np.sum(orc.linear_fwd(X, W, b) * dY))
+            arr[idx] = x0 - eps
+            lm = float(np.sum(orc.linear_fwd(X, W, b) * dY))
+            arr[idx] = x0
+            fd[idx] = (lp - lm) / (2 * eps)
+        assert np.linalg.norm(g - fd) / np.linalg.norm(fd) <= 1e-7, name
+
+
+def pin_qkv_interleave_commutes_with_projection(orc):
+    """Permuting the projection's output columns equals projecting with the permuted
+    weight (bit for bit: every output column is the same dot product), and the p-way
+    column split of the interleaved projection gives each rank exactly its heads' q, k, v."""
+    r = _rng(12)
+    h, n, p, M = 24, 6, 3, 5
+    X = r.standard_normal((M, h)); W = r.standard_normal((h, 3 * h)); b = r.standard_normal(3 * h)
+    Y = orc.linear_fwd(X, W, b)
+    Wi = orc.qkv_interleave(W, h, n)
+    bi = orc.qkv_interleave(b.reshape(1, -1), h, n).reshape(-1)
+    Yi = orc.linear_fwd(X, Wi, bi)
+    assert np.array_equal(Yi, orc.qkv_interleave(Y, h, n))
+    d, cw = h // n, 3 * h // p
+    for rk in range(p):
+        for g_local in range(n // p):
+            g = rk * (n // p) + g_local
+            for t in range(3):
+                got = Yi[:, rk * cw + (3 * g_local + t) * d: rk * cw + (3 * g_local + t + 1) * d]
+                assert np.array_equal(got, Y[:, t * h + g * d: t * h + (g + 1) * d])
+
+
 ALL_PINS = [
     pin_gelu_closed_forms,
     pin_gelu_vs_library,
@@ -300,6 +348,8 @@ ALL_PINS = [
     pin_sampled_backward_matches_full,
     pin_shard_columns_vs_np_split,
     pin_qkv_interleave_heads_on_one_rank,
+    pin_linear_vs_numpy_and_fd,
+    pin_qkv_interleave_commutes_with_projection,
 ]
 
 

@@ -28,6 +28,10 @@ MUTANTS = {
     "sampled_dX_transposed_A": ("for (int64_t n = 0; n < h; ++n) out[n] += dh * A[n * f + j];",
                                 "for (int64_t n = 0; n < h; ++n) out[n] += dh * A[j * h + n];"),
     "sampled_dB_uses_H": ("const double y = act_fwd(act, hv);", "const double y = hv;"),
+    "linear_bias_dropped": ("for (int64_t n = 0; n < N; ++n) Y[m * N + n] += b[n];",
+                            "for (int64_t n = 0; n < N; ++n) Y[m * N + n] += 0.0 * b[n];"),
+    "linear_dX_wrong_operand": ("matmul_nt(M, N, K, dY, W, dX);  /* dX = dY W^T  [M,K] */",
+                                "matmul_nn(M, N, K, dY, W, dX);  /* dX = dY W^T  [M,K] */"),
 }
 
 
