@@ -55,6 +55,24 @@ def dist_env():
     return ws, rank, local
 
 
+def dist_max(value: float) -> float:
+    """Max of a float over all ranks (the value itself when not distributed).
+    Uses the process group's own backend: NCCL on GPUs, gloo on CPU."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_step_per_rank: float, world: int, slowest_ms_per_step: float) -> float:
+    """Whole-job rate: the units every rank processed over the slowest rank's time."""
+    return units_per_step_per_rank * world / (slowest_ms_per_step * 1e-3)
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
@@ -251,19 +269,14 @@ def run_gpu(args):
     barrier()
     clocks = sampler.stop()
     T.tpmlp_device_status()
-    total_ms = t_start.elapsed_time(t_end)
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = dist_max(t_start.elapsed_time(t_end))
     ms_step = total_ms / K
     col_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     row_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev) if wl.backward else 0.0
     flops_step = wl.fwd_flops() + (wl.bwd_flops() if wl.backward else 0.0)
-    value = flops_step * ws / (ms_step * 1e-3) / 1e12
-    tokens_s = M * ws / (ms_step * 1e-3)
+    value = job_throughput(flops_step, ws, ms_step) / 1e12
+    tokens_s = job_throughput(M, ws, ms_step)
 
     # roofline: the single-launch GEMM with the larger time (column with GeLU, or row with shard sum)
     gemm_flops = 2.0 * M * h * f
@@ -308,13 +321,8 @@ def run_gpu(args):
             e2e_step()
         z.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(z) / args.e2e_steps
-        if ws > 1:
-            import torch.distributed as dist
-            t = torch.tensor([e2e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": round(flops_step * ws / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        e2e_ms = dist_max(a.elapsed_time(z) / args.e2e_steps)
+        e2e = {"value": round(job_throughput(flops_step, ws, e2e_ms) / 1e12, 2), "unit": "TFLOP/s",
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "note": "inputs X, dZ copied from pinned host memory and Z, dX read back every step; "
                        "weights stay resident"}
