@@ -69,6 +69,33 @@ bool set_smem_attr(Kern kern, int device, int bytes, bool* done) {
     return true;
 }
 
+// 4-D bf16 tensor map of an MN-major operand whose MN extent is a multiple of 64:
+// [shards][mn/64 chunks][K][64], so that one box (64 x BK x chunks x 1) lands in
+// shared memory as `chunks` consecutive 64-wide MN chunks of BK K-rows.
+bool make_map_chunked(CUtensorMap* map, const Operand& op, uint64_t mn, uint64_t k, uint32_t chunks) {
+    auto fn = encode_fn();
+    if (!fn) {
+        set_error("cuTensorMapEncodeTiled is not available from the driver");
+        return false;
+    }
+    const uint64_t shards = op.shards > 0 ? static_cast<uint64_t>(op.shards) : 1;
+    const uint64_t ld_bytes = static_cast<uint64_t>(op.ld) * 2;
+    uint64_t ss_bytes = static_cast<uint64_t>(op.ss) * 2;
+    if (shards == 1) ss_bytes = ld_bytes * k;
+    cuuint64_t dims[4] = {64, k, mn / 64, shards};
+    cuuint64_t strides[3] = {ld_bytes, 128, ss_bytes};
+    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(tc::BK), chunks, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(op.ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled (chunked) failed (%d)", static_cast<int>(r));
+        return false;
+    }
+    return true;
+}
+
 template <bool A_MN, bool B_MN, int EPI>
 tpmlp_status launch_single(const CUtensorMap& ma, const CUtensorMap& mb, const tc::KArgs& k, const DeviceInfo& dev,
                            cudaStream_t st) {
@@ -151,10 +178,16 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
     int cap = (mode == 1) ? 0 : pair_capacity<A_MN, B_MN, EPI>(dev);
     const bool use_pair = cap > 0 && (mode == 2 || pair_tiles >= cap);
     CUtensorMap ma, mb;
-    bool ok = a.mn_major ? make_map(&ma, a, g.M, g.K, 64, tc::BK) : make_map(&ma, a, g.K, g.M, tc::BK, tc::BM);
-    if (!ok) return TPMLP_ERR_CUDA;
     const uint32_t b_rows = use_pair ? tc::BN / 2 : tc::BN;
-    ok = b.mn_major ? make_map(&mb, b, g.N, g.K, 64, tc::BK) : make_map(&mb, b, g.K, g.N, tc::BK, b_rows);
+    // MN-major operands: one 4-D box per stage when the MN extent is a multiple of 64
+    k.a_chunked = (a.mn_major && g.M % 64 == 0) ? 1 : 0;
+    k.b_chunked = (b.mn_major && g.N % 64 == 0) ? 1 : 0;
+    bool ok;
+    if (k.a_chunked) ok = make_map_chunked(&ma, a, g.M, g.K, tc::BM / 64);
+    else ok = a.mn_major ? make_map(&ma, a, g.M, g.K, 64, tc::BK) : make_map(&ma, a, g.K, g.M, tc::BK, tc::BM);
+    if (!ok) return TPMLP_ERR_CUDA;
+    if (k.b_chunked) ok = make_map_chunked(&mb, b, g.N, g.K, b_rows / 64);
+    else ok = b.mn_major ? make_map(&mb, b, g.N, g.K, 64, tc::BK) : make_map(&mb, b, g.K, g.N, tc::BK, b_rows);
     if (!ok) return TPMLP_ERR_CUDA;
     if (!use_pair) return launch_single<A_MN, B_MN, EPI>(ma, mb, k, dev, st);
     k.m_blocks = m_pairs;

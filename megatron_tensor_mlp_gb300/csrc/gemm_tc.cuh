@@ -60,6 +60,7 @@ struct KArgs {
     int n_shards, sum_shards, a_batched, b_batched;
     int m_blocks, n_blocks, batch, num_tiles, kb_per_shard, k_iters, group_m;
     int act, out_f32;
+    int a_chunked, b_chunked;  // MN-major operand loaded with one 4-D box per stage (MN extent % 64 == 0)
     void* out; long long out_ld, out_ss;
     void* out2; long long out2_ld, out2_ss;
     const void* bias; long long bias_ss;
@@ -257,6 +258,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int k0 = kb * BK;
                     if constexpr (!A_MN) {
                         tma_load_3d(a_dst, &tmA, full + stage, k0, mb * BM, sa);
+                    } else if (p.a_chunked) {
+                        tma_load_4d(a_dst, &tmA, full + stage, 0, k0, (mb * BM) / 64, sa);
                     } else {
 #pragma unroll
                         for (int c = 0; c < BM / 64; ++c)
@@ -264,6 +267,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     if constexpr (!B_MN) {
                         tma_load_3d(b_dst, &tmB, full + stage, k0, nb * BN, sb);
+                    } else if (p.b_chunked) {
+                        tma_load_4d(b_dst, &tmB, full + stage, 0, k0, (nb * BN) / 64, sb);
                     } else {
 #pragma unroll
                         for (int c = 0; c < BN / 64; ++c)
@@ -483,6 +488,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int k0 = kb * BK;
                     if constexpr (!A_MN) {
                         tma_load_3d_pair(a_dst, &tmA, bar, k0, row0, sa);
+                    } else if (p.a_chunked) {
+                        tma_load_4d_pair(a_dst, &tmA, bar, 0, k0, row0 / 64, sa);
                     } else {
 #pragma unroll
                         for (int c = 0; c < BM / 64; ++c)
@@ -490,6 +497,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     if constexpr (!B_MN) {
                         tma_load_3d_pair(b_dst, &tmB, bar, k0, col0, sb);
+                    } else if (p.b_chunked) {
+                        tma_load_4d_pair(b_dst, &tmB, bar, 0, k0, col0 / 64, sb);
                     } else {
 #pragma unroll
                         for (int c = 0; c < (BN / 2) / 64; ++c)
