@@ -232,51 +232,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t armed = 0;        // bit s: stage s has been armed at least once
             uint32_t last_parity = 0;  // bit s: parity of the phase last armed on stage s
             bool ok = true;
+            const int k_end = p.kb_per_shard * BK;
             for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
                 int mb, nb, shard;
                 decode_tile(p, t, mb, nb, shard);
+                const int row0 = mb * BM, col0 = nb * BN;
+                // sum mode: the K loop walks (shard, k); batched: shard fixed per tile
+                int sa = p.sum_shards ? 0 : (p.a_batched ? shard : 0);
+                int sb = p.sum_shards ? 0 : (p.b_batched ? shard : 0);
+                int k0 = 0;
                 for (int it = 0; it < p.k_iters; ++it) {
-                    int ks, kb;
-                    if (p.sum_shards) {
-                        ks = it / p.kb_per_shard;
-                        kb = it - ks * p.kb_per_shard;
-                    } else {
-                        ks = shard;
-                        kb = it;
-                    }
-                    const int sa = p.sum_shards ? ks : (p.a_batched ? shard : 0);
-                    const int sb = p.sum_shards ? ks : (p.b_batched ? shard : 0);
                     if (!mbar_wait_bounded(empty + stage, phase ^ 1u, p.status, p.timeout_ns, kWhereProducer)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full + stage, STAGE_BYTES);
+                    uint64_t* fb = full + stage;
+                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
                     armed |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                     uint8_t* a_dst = sA + stage * A_TILE_BYTES;
                     uint8_t* b_dst = sB + stage * B_TILE_BYTES;
-                    const int k0 = kb * BK;
                     if constexpr (!A_MN) {
-                        tma_load_3d(a_dst, &tmA, full + stage, k0, mb * BM, sa);
+                        tma_load_3d(a_dst, &tmA, fb, k0, row0, sa);
                     } else if (p.a_chunked) {
-                        tma_load_4d(a_dst, &tmA, full + stage, 0, k0, (mb * BM) / 64, sa);
+                        tma_load_4d(a_dst, &tmA, fb, 0, k0, row0 / 64, sa);
                     } else {
 #pragma unroll
                         for (int c = 0; c < BM / 64; ++c)
-                            tma_load_3d(a_dst + c * MN_CHUNK_BYTES, &tmA, full + stage, mb * BM + c * 64, k0, sa);
+                            tma_load_3d(a_dst + c * MN_CHUNK_BYTES, &tmA, fb, row0 + c * 64, k0, sa);
                     }
                     if constexpr (!B_MN) {
-                        tma_load_3d(b_dst, &tmB, full + stage, k0, nb * BN, sb);
+                        tma_load_3d(b_dst, &tmB, fb, k0, col0, sb);
                     } else if (p.b_chunked) {
-                        tma_load_4d(b_dst, &tmB, full + stage, 0, k0, (nb * BN) / 64, sb);
+                        tma_load_4d(b_dst, &tmB, fb, 0, k0, col0 / 64, sb);
                     } else {
 #pragma unroll
                         for (int c = 0; c < BN / 64; ++c)
-                            tma_load_3d(b_dst + c * MN_CHUNK_BYTES, &tmB, full + stage, nb * BN + c * 64, k0, sb);
+                            tma_load_3d(b_dst + c * MN_CHUNK_BYTES, &tmB, fb, col0 + c * 64, k0, sb);
                     }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
+                    }
+                    k0 += BK;
+                    if (k0 == k_end) {  // next shard of the sum (only reached mid-tile in sum mode)
+                        k0 = 0;
+                        ++sa;
+                        ++sb;
                     }
                 }
             }
@@ -292,6 +294,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             // ------------------------------------------------------------ MMA issuer
             constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+            const uint64_t a_desc0 = A_MN ? sdesc_sw128(smem_u32(sA), TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES)
+                                          : sdesc_sw128(smem_u32(sA), 16, 1024);
+            const uint64_t b_desc0 = B_MN ? sdesc_sw128(smem_u32(sB), TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES)
+                                          : sdesc_sw128(smem_u32(sB), 16, 1024);
+            constexpr uint64_t a_kstep = A_MN ? (2048 >> 4) : (32 >> 4);  // one UMMA K step (16 elements)
+            constexpr uint64_t b_kstep = B_MN ? (2048 >> 4) : (32 >> 4);
             int stage = 0;
             uint32_t phase = 0;
             int lt = 0;
@@ -311,17 +319,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_base = smem_u32(sA + stage * A_TILE_BYTES);
-                    const uint32_t b_base = smem_u32(sB + stage * B_TILE_BYTES);
+                    // descriptor start addresses are in 16-byte units in the low bits
+                    const uint64_t adesc = a_desc0 + static_cast<uint64_t>(stage * (A_TILE_BYTES >> 4));
+                    const uint64_t bdesc = b_desc0 + static_cast<uint64_t>(stage * (B_TILE_BYTES >> 4));
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        uint64_t adesc, bdesc;
-                        if constexpr (!A_MN) adesc = sdesc_sw128(a_base + kk * 32, 16, 1024);
-                        else adesc = sdesc_sw128(a_base + kk * 2048, TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES);
-                        if constexpr (!B_MN) bdesc = sdesc_sw128(b_base + kk * 32, 16, 1024);
-                        else bdesc = sdesc_sw128(b_base + kk * 2048, TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES);
-                        umma_f16(d_tmem, adesc, bdesc, idesc, (it | kk) != 0 ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma_f16(d_tmem, adesc + kk * a_kstep, bdesc + kk * b_kstep, idesc, (it | kk) != 0 ? 1u : 0u);
                     umma_commit(empty + stage);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -457,22 +460,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             uint32_t armed = 0, last_parity = 0;
             bool ok = true;
+            const int k_end = p.kb_per_shard * BK;
+            const uint32_t full_leader0 = mapa_shared(smem_u32(full), 0);  // the leader's barriers
             for (int t = cluster_id; t < p.num_tiles && ok; t += n_clusters) {
                 int mb, nb, shard;
                 decode_tile(p, t, mb, nb, shard);
                 const int row0 = mb * (2 * BM) + static_cast<int>(rank) * BM;
                 const int col0 = nb * BN + static_cast<int>(rank) * (BN / 2);
+                int sa = p.sum_shards ? 0 : (p.a_batched ? shard : 0);
+                int sb = p.sum_shards ? 0 : (p.b_batched ? shard : 0);
+                int k0 = 0;
                 for (int it = 0; it < p.k_iters; ++it) {
-                    int ks, kb;
-                    if (p.sum_shards) {
-                        ks = it / p.kb_per_shard;
-                        kb = it - ks * p.kb_per_shard;
-                    } else {
-                        ks = shard;
-                        kb = it;
-                    }
-                    const int sa = p.sum_shards ? ks : (p.a_batched ? shard : 0);
-                    const int sb = p.sum_shards ? ks : (p.b_batched ? shard : 0);
                     if (!mbar_wait_bounded(empty + stage, phase ^ 1u, p.status, p.timeout_ns, kWhereProducer)) {
                         ok = false;
                         break;
@@ -482,10 +480,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         armed |= 1u << stage;
                         last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                     }
-                    const uint32_t bar = mapa_shared(smem_u32(full + stage), 0);
+                    const uint32_t bar = full_leader0 + stage * 8;
                     uint8_t* a_dst = sA + stage * P_A_BYTES;
                     uint8_t* b_dst = sB + stage * P_B_BYTES;
-                    const int k0 = kb * BK;
                     if constexpr (!A_MN) {
                         tma_load_3d_pair(a_dst, &tmA, bar, k0, row0, sa);
                     } else if (p.a_chunked) {
@@ -508,6 +505,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         stage = 0;
                         phase ^= 1u;
                     }
+                    k0 += BK;
+                    if (k0 == k_end) {
+                        k0 = 0;
+                        ++sa;
+                        ++sb;
+                    }
                 }
             }
             if (!ok) {
@@ -527,6 +530,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (leader) {
                 // -------------------------------------------------------- UMMA issuer (leader)
                 constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
+                const uint64_t a_desc0 = A_MN ? sdesc_sw128(smem_u32(sA), TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES)
+                                              : sdesc_sw128(smem_u32(sA), 16, 1024);
+                const uint64_t b_desc0 = B_MN ? sdesc_sw128(smem_u32(sB), TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES)
+                                              : sdesc_sw128(smem_u32(sB), 16, 1024);
+                constexpr uint64_t a_kstep = A_MN ? (2048 >> 4) : (32 >> 4);
+                constexpr uint64_t b_kstep = B_MN ? (2048 >> 4) : (32 >> 4);
                 int stage = 0;
                 uint32_t phase = 0;
                 int lt = 0;
@@ -546,17 +555,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t a_base = smem_u32(sA + stage * P_A_BYTES);
-                        const uint32_t b_base = smem_u32(sB + stage * P_B_BYTES);
+                        const uint64_t adesc = a_desc0 + static_cast<uint64_t>(stage * (P_A_BYTES >> 4));
+                        const uint64_t bdesc = b_desc0 + static_cast<uint64_t>(stage * (P_B_BYTES >> 4));
 #pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk) {
-                            uint64_t adesc, bdesc;
-                            if constexpr (!A_MN) adesc = sdesc_sw128(a_base + kk * 32, 16, 1024);
-                            else adesc = sdesc_sw128(a_base + kk * 2048, TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES);
-                            if constexpr (!B_MN) bdesc = sdesc_sw128(b_base + kk * 32, 16, 1024);
-                            else bdesc = sdesc_sw128(b_base + kk * 2048, TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES);
-                            umma_f16_pair(d_tmem, adesc, bdesc, idesc, (it | kk) != 0 ? 1u : 0u);
-                        }
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            umma_f16_pair(d_tmem, adesc + kk * a_kstep, bdesc + kk * b_kstep, idesc,
+                                          (it | kk) != 0 ? 1u : 0u);
                         umma_commit_pair_mc(empty + stage, 0x3);
                         if (++stage == P_STAGES) {
                             stage = 0;
