@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //                   warps 4-11: epilogue of its 128 rows; the accumulator is
 //                            released by 16 arrivals on the leader's barrier
 // ============================================================================
-constexpr int P_STAGES = 6;
+constexpr int P_STAGES = 7;
 constexpr int P_A_BYTES = BM * BK * 2;        // 16 KiB: this CTA's 128 rows of A
 constexpr int P_B_BYTES = (BN / 2) * BK * 2;  // 16 KiB: this CTA's 128 columns of B
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
