@@ -1,6 +1,7 @@
 // fp32 FMA GEMM (the fp32 path: no TF32, so results stay within fp32 rounding),
 // column sums for the bias gradients, bit-exact layout copies and the
 // bounded-wait test hook.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -135,6 +136,58 @@ __global__ void __launch_bounds__(256) colsum_kernel(const void* in, long long M
     }
 }
 
+// Column sums of a bf16 [shards][M][N] tensor: a cluster of 8 CTAs shares one
+// 256-column strip, each CTA summing every 8th group of 8 rows; the partial sums
+// are added from the cluster's shared memory in a fixed order, so the result is
+// deterministic and needs no global scratch.  (N is a multiple of 8.)
+constexpr int CS_CLUSTER = 8;
+template <bool OUT_F32>
+__global__ void __cluster_dims__(1, CS_CLUSTER, 1) __launch_bounds__(256)
+    colsum_bf16_cluster_kernel(const __nv_bfloat16* __restrict__ in, long long M, long long N, void* out) {
+    namespace cg = cooperative_groups;
+    __shared__ float part[8][256];
+    __shared__ float block_sum[256];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const long long s = blockIdx.z;
+    const long long c = (long long)blockIdx.x * 256 + lane * 8;
+    const int grp = blockIdx.y;  // == rank in the cluster
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (c < N) {
+        const __nv_bfloat16* base = in + s * M * N + c;
+        // rows grp*8 + warp + 64*i
+#pragma unroll 4
+        for (long long m = (long long)grp * 8 + warp; m < M; m += 64) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4*>(base + m * N));
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] += __uint_as_float(w[i] << 16);
+                acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) part[warp][lane * 8 + i] = acc[i];
+    __syncthreads();
+    {
+        float r = 0.f;
+        for (int w = 0; w < 8; ++w) r += part[w][threadIdx.x];
+        block_sum[threadIdx.x] = r;
+    }
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();  // every CTA's block_sum is complete
+    if (grp == 0) {
+        float r = 0.f;
+        for (int g = 0; g < CS_CLUSTER; ++g) r += cluster.map_shared_rank(block_sum, g)[threadIdx.x];
+        const long long col = (long long)blockIdx.x * 256 + threadIdx.x;
+        if (col < N) {
+            if (OUT_F32) static_cast<float*>(out)[s * N + col] = r;
+            else static_cast<__nv_bfloat16*>(out)[s * N + col] = __float2bfloat16_rn(r);
+        }
+    }
+    cluster.sync();  // peers stay resident until CTA 0 has read their shared memory
+}
+
 // ------------------------------------------------------------------ layouts
 // Column shard: dst[i][r][c] = src[r][i*cs + c] in 16-byte units (rows of cs*esize bytes).
 __global__ void shard_columns_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long rows,
@@ -227,6 +280,12 @@ tpmlp_status launch_simt_gemm(const Operand& a, const Operand& b, const GemmSpec
 
 tpmlp_status launch_colsum(const void* in, bool in_f32, int64_t shards, int64_t M, int64_t N, void* out, bool out_f32,
                            cudaStream_t st) {
+    if (!in_f32) {
+        dim3 g((unsigned)((N + 255) / 256), CS_CLUSTER, (unsigned)shards);
+        if (out_f32) colsum_bf16_cluster_kernel<true><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(in), M, N, out);
+        else colsum_bf16_cluster_kernel<false><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(in), M, N, out);
+        return check_launch("column sum");
+    }
     dim3 grid((unsigned)((N + 63) / 64), (unsigned)shards);
     if (in_f32 && out_f32) colsum_kernel<true, true><<<grid, 256, 0, st>>>(in, M, N, out);
     else if (in_f32) colsum_kernel<true, false><<<grid, 256, 0, st>>>(in, M, N, out);
