@@ -82,11 +82,94 @@ __device__ __forceinline__ void decode_tile(const KArgs& p, int t, int& mb, int&
     nb = nbg - shard * p.n_blocks;
 }
 
-__device__ __forceinline__ float gelu_erf(float x) {
-    return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+// ---------------------------------------------------------------------------
+// GeLU(x) = x Phi(x) and GeLU'(x) = Phi(x) + x phi(x), two elements at a time.
+//
+// Phi comes from the complementary error function, evaluated with Hastings'
+// rational approximation as tabulated by Abramowitz & Stegun, "Handbook of
+// Mathematical Functions", formula 7.1.26:
+//     erfc(z) ~= t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2),
+//     t = 1 / (1 + p z),  z >= 0,  |error| <= 1.5e-7,
+// with p = 0.3275911, a1..a5 = 0.254829592, -0.284496736, 1.421413741,
+// -1.453152027, 1.061405429.  With z = |x| / sqrt(2):
+//     Phi(x) = 1 - erfc(z) / 2  (x >= 0),   erfc(z) / 2  (x < 0),
+// and exp(-z^2) = exp(-x^2 / 2) = sqrt(2 pi) phi(x), shared by GeLU'.
+// The factor 1/2 is folded into a1..a5.  The polynomial runs on packed
+// fp32x2 FMAs; the reciprocal and exp2 use the hardware approximations.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
 }
-__device__ __forceinline__ float gelu_erf_grad(float x) {
-    return 0.5f * (1.0f + erff(x * 0.70710678118654752f)) + x * 0.39894228040143268f * expf(-0.5f * x * x);
+__device__ __forceinline__ void f2_unpack(unsigned long long v, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// Phi(x) and exp(-x^2/2) for two elements.
+__device__ __forceinline__ void normal_cdf_pair(float x0, float x1, float& cdf0, float& cdf1, float& e0, float& e1) {
+    const float kInvSqrt2 = 0.70710678118654752f;
+    const unsigned long long z = f2_pack(fabsf(x0) * kInvSqrt2, fabsf(x1) * kInvSqrt2);
+    float s0, s1;
+    f2_unpack(f2_fma(f2_pack(0.3275911f, 0.3275911f), z, f2_pack(1.0f, 1.0f)), s0, s1);
+    const unsigned long long t = f2_pack(rcp_approx(s0), rcp_approx(s1));
+    unsigned long long q = f2_fma(t, f2_pack(0.5307027145f, 0.5307027145f), f2_pack(-0.7265760135f, -0.7265760135f));
+    q = f2_fma(t, q, f2_pack(0.7107068705f, 0.7107068705f));
+    q = f2_fma(t, q, f2_pack(-0.142248368f, -0.142248368f));
+    q = f2_fma(t, q, f2_pack(0.127414796f, 0.127414796f));
+    q = f2_mul(t, q);  // erfc(z) / 2 without the exponential
+    float w0, w1;      // -z^2 log2(e) = -x^2 / 2 log2(e)
+    f2_unpack(f2_mul(f2_mul(z, z), f2_pack(-1.4426950408889634f, -1.4426950408889634f)), w0, w1);
+    e0 = ex2_approx(w0);
+    e1 = ex2_approx(w1);
+    float h0, h1;
+    f2_unpack(f2_mul(q, f2_pack(e0, e1)), h0, h1);  // erfc(z) / 2
+    cdf0 = x0 >= 0.0f ? 1.0f - h0 : h0;
+    cdf1 = x1 >= 0.0f ? 1.0f - h1 : h1;
+}
+
+// v[j] <- GeLU(v[j]) for j in [0, 32)
+__device__ __forceinline__ void gelu_inplace32(float* v) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        float c0, c1, e0, e1;
+        normal_cdf_pair(v[j], v[j + 1], c0, c1, e0, e1);
+        f2_unpack(f2_mul(f2_pack(v[j], v[j + 1]), f2_pack(c0, c1)), v[j], v[j + 1]);
+    }
+}
+
+// v[j] <- v[j] * GeLU'(h[j]) for j in [0, 8)
+__device__ __forceinline__ void dgelu_mul8(float* v, const float* h) {
+    const unsigned long long inv_sqrt_2pi = f2_pack(0.39894228040143268f, 0.39894228040143268f);
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+        float c0, c1, e0, e1;
+        normal_cdf_pair(h[j], h[j + 1], c0, c1, e0, e1);
+        // GeLU' = Phi + x exp(-x^2/2) / sqrt(2 pi)
+        const unsigned long long g = f2_fma(f2_mul(f2_pack(h[j], h[j + 1]), f2_pack(e0, e1)), inv_sqrt_2pi,
+                                            f2_pack(c0, c1));
+        f2_unpack(f2_mul(f2_pack(v[j], v[j + 1]), g), v[j], v[j + 1]);
+    }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -150,10 +233,7 @@ __device__ __forceinline__ void epilogue_chunk(const KArgs& p, const uint32_t (&
             __nv_bfloat16* d2 = static_cast<__nv_bfloat16*>(p.out2) + shard * p.out2_ss + (long long)gm * p.out2_ld + gn0;
             store_bf16x32(d2, v, nvalid);
         }
-        if (p.act == TPMLP_ACT_GELU_ERF) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
-        }
+        if (p.act == TPMLP_ACT_GELU_ERF) gelu_inplace32(v);
         __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.out) + shard * p.out_ss + (long long)gm * p.out_ld + gn0;
         store_bf16x32(d, v, nvalid);
     } else if constexpr (EPI == EPI_DGELU) {
@@ -164,8 +244,7 @@ __device__ __forceinline__ void epilogue_chunk(const KArgs& p, const uint32_t (&
             if (g * 8 < nvalid) {
                 float hv[8];
                 unpack_bf16x8(*reinterpret_cast<const uint4*>(hp + g * 8), hv);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[g * 8 + i] *= gelu_erf_grad(hv[i]);
+                dgelu_mul8(v + g * 8, hv);
             }
         }
         __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.out) + shard * p.out_ss + (long long)gm * p.out_ld + gn0;
