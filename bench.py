@@ -73,6 +73,33 @@ def job_throughput(units_per_step_per_rank: float, world: int, slowest_ms_per_st
     return units_per_step_per_rank * world / (slowest_ms_per_step * 1e-3)
 
 
+def captured_traffic(kernel_key):
+    """DRAM bytes per launch of a forward GEMM at the bench workload, from the committed ncu
+    summary, or None when the kernel sources have changed since that capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic_s2048_b4_h5120_ffn20480_p4.txt")
+    srcs = ["gemm_tc.cuh", "gemm_tc.cu", "ptx.cuh"]
+    try:
+        h = hashlib.sha256()
+        for f in srcs:
+            with open(os.path.join(ROOT, "megatron_tensor_mlp_gb300", "csrc", f), "rb") as fh:
+                h.update(fh.read())
+        recorded, vals = None, {}
+        for line in open(path):
+            parts = line.split()
+            if not parts or parts[0].startswith("#"):
+                continue
+            if parts[0] == "kernel_source_sha256":
+                recorded = parts[1]
+            elif len(parts) >= 3:
+                vals[parts[0]] = int(parts[1]) + int(parts[2])
+        if recorded != h.hexdigest():
+            return None
+        return vals.get(kernel_key)
+    except (OSError, ValueError):
+        return None
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
@@ -280,13 +307,16 @@ def run_gpu(args):
 
     # roofline: the single-launch GEMM with the larger time (column with GeLU, or row with shard sum)
     gemm_flops = 2.0 * M * h * f
-    dom_name, dom_ms = ("column_fwd (tcgen05 GEMM + bias + erf-GeLU epilogue)", col_ms) if col_ms >= row_ms else \
-        ("row_fwd (tcgen05 GEMM + in-TMEM shard sum)", row_ms)
+    dom_key, dom_name, dom_ms = ("column_fwd", "column_fwd (tcgen05 GEMM + bias + erf-GeLU epilogue)", col_ms) \
+        if col_ms >= row_ms else ("row_fwd", "row_fwd (tcgen05 GEMM + in-TMEM shard sum)", row_ms)
     achieved = gemm_flops / (dom_ms * 1e-3) / 1e12
     peak = peaks.get("bf16_tflops_sustained", 1700.0)
     roofline = {"bound": "tensor", "kernel": dom_name, "achieved": round(achieved, 1), "peak": peak,
                 "peak_kind": f"bf16_tflops_sustained ({peak_kind})", "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
+                "frac": round(achieved / peak, 4),
+                "traffic": captured_traffic(dom_key) if args.workload == MAIN_WORKLOAD else None,
+                "traffic_algorithmic": {"column_fwd": 964e6, "row_fwd": 629e6}.get(dom_key)
+                if args.workload == MAIN_WORKLOAD else None,
                 "per_launch_ms": {"column_fwd": round(col_ms, 4), "row_fwd": round(row_ms, 4),
                                   "mlp_bwd(6 launches)": round(bwd_ms, 4)}}
 
