@@ -74,6 +74,16 @@ class Oracle:
         lib.oracle_linear_fwd.argtypes = [i64, i64, i64, vp, vp, vp, vp]
         lib.oracle_linear_bwd.restype = None
         lib.oracle_linear_bwd.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, vp]
+        lib.oracle_silu.restype = d
+        lib.oracle_silu.argtypes = [d]
+        lib.oracle_silu_grad.restype = d
+        lib.oracle_silu_grad.argtypes = [d]
+        lib.oracle_swiglu_fwd.restype = None
+        lib.oracle_swiglu_fwd.argtypes = [i64, i64, i64] + [vp] * 11
+        lib.oracle_swiglu_bwd.restype = None
+        lib.oracle_swiglu_bwd.argtypes = [i64, i64, i64] + [vp] * 16
+        lib.oracle_swiglu_pack.restype = None
+        lib.oracle_swiglu_pack.argtypes = [i64, i64, i64, i64, i32, vp, vp, vp]
         lib.oracle_bwd_db2.restype = None
         lib.oracle_bwd_db2.argtypes = [i64, i64, vp, vp]
         lib.oracle_shard_columns.restype = None
@@ -158,6 +168,51 @@ class Oracle:
         dX = np.empty((M, K)); dW = np.empty((K, N)); db = np.empty(N) if with_bias else None
         self.lib.oracle_linear_bwd(M, K, N, _ptr(X), _ptr(W), _ptr(dY), _ptr(dX), _ptr(dW), _ptr(db))
         return dX, dW, db
+
+    def silu(self, x: float) -> float:
+        return float(self.lib.oracle_silu(float(x)))
+
+    def silu_grad(self, x: float) -> float:
+        return float(self.lib.oracle_silu_grad(float(x)))
+
+    def swiglu_fwd(self, X, G, U, bg, bu, B, b2):
+        """Returns (Hg, Hu, Y, Z) of the SwiGLU block."""
+        X, G, U, bg, bu, B, b2 = map(_f64, (X, G, U, bg, bu, B, b2))
+        M, h = X.shape
+        f = G.shape[1]
+        Hg = np.empty((M, f)); Hu = np.empty((M, f)); Y = np.empty((M, f)); Z = np.empty((M, h))
+        self.lib.oracle_swiglu_fwd(M, h, f, _ptr(X), _ptr(G), _ptr(U), _ptr(bg), _ptr(bu), _ptr(B), _ptr(b2),
+                                   _ptr(Hg), _ptr(Hu), _ptr(Y), _ptr(Z))
+        return Hg, Hu, Y, Z
+
+    def swiglu_bwd(self, X, G, U, B, Hg, Hu, Y, dZ):
+        """Returns dict dX, dG, dU, dB, dbg, dbu, db2."""
+        X, G, U, B, Hg, Hu, Y, dZ = map(_f64, (X, G, U, B, Hg, Hu, Y, dZ))
+        M, h = X.shape
+        f = G.shape[1]
+        out = {k: np.empty(sh) for k, sh in (("dX", (M, h)), ("dG", (h, f)), ("dU", (h, f)), ("dB", (f, h)),
+                                             ("dbg", (f,)), ("dbu", (f,)), ("db2", (h,)))}
+        work = np.empty(3 * M * f + M * h)
+        self.lib.oracle_swiglu_bwd(M, h, f, _ptr(X), _ptr(G), _ptr(U), _ptr(B), _ptr(Hg), _ptr(Hu), _ptr(Y),
+                                   _ptr(dZ), _ptr(out["dX"]), _ptr(out["dG"]), _ptr(out["dU"]), _ptr(out["dB"]),
+                                   _ptr(out["dbg"]), _ptr(out["dbu"]), _ptr(out["db2"]), _ptr(work))
+        return out
+
+    def swiglu_pack(self, G, U, p):
+        """[rows, f] gate and up -> packed [p, rows, 2 f/p] (128-feature blocks)."""
+        G = np.ascontiguousarray(G); U = np.ascontiguousarray(U)
+        rows, f = G.shape
+        out = np.empty((p, rows, 2 * (f // p)), dtype=G.dtype)
+        self.lib.oracle_swiglu_pack(G.itemsize, rows, f, p, 0, _ptr(G), _ptr(U), _ptr(out))
+        return out
+
+    def swiglu_unpack(self, W, p):
+        W = np.ascontiguousarray(W)
+        _, rows, c2 = W.shape
+        f = c2 // 2 * p
+        G = np.empty((rows, f), dtype=W.dtype); U = np.empty((rows, f), dtype=W.dtype)
+        self.lib.oracle_swiglu_pack(W.itemsize, rows, f, p, 1, _ptr(G), _ptr(U), _ptr(W))
+        return G, U
 
     def bwd_db2(self, dZ):
         """db2 = column sums of dZ."""

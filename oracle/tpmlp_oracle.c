@@ -279,6 +279,106 @@ void oracle_linear_bwd(int64_t M, int64_t K, int64_t N, const double* X, const d
     }
 }
 
+/*
+ * SwiGLU variant of the block ([M2] M027: a gated activation such as SwiGLU
+ * works on local pairs of the FFN shard, so the column + row split still needs
+ * only the final sum; M031 notes its two branches as a divisibility constraint).
+ * The gate G and up U projections are both column parallel:
+ *   Hg = X G + 1 bg^T,  Hu = X U + 1 bu^T,  Y = silu(Hg) * Hu,  Z = Y B + 1 b2^T,
+ *   silu(x) = x sigma(x),  sigma(x) = 1 / (1 + exp(-x)).
+ * Backward from dZ:
+ *   dB = Y^T dZ, db2 = 1^T dZ, dY = dZ B^T,
+ *   dHg = dY * Hu * silu'(Hg),  silu'(x) = sigma(x) (1 + x (1 - sigma(x))),
+ *   dHu = dY * silu(Hg),
+ *   dG = X^T dHg, dU = X^T dHu, dbg = 1^T dHg, dbu = 1^T dHu, dX = dHg G^T + dHu U^T.
+ * G, U [h,f]; bg, bu [f] (may be NULL); Hg, Hu, Y [M,f].
+ */
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+double oracle_silu(double x) { return x * sigmoid(x); }
+double oracle_silu_grad(double x) { const double s = sigmoid(x); return s * (1.0 + x * (1.0 - s)); }
+
+void oracle_swiglu_fwd(int64_t M, int64_t h, int64_t f,
+                       const double* X, const double* G, const double* U, const double* bg, const double* bu,
+                       const double* B, const double* b2,
+                       double* Hg, double* Hu, double* Y, double* Z) {
+    matmul_nn(M, h, f, X, G, Hg);
+    matmul_nn(M, h, f, X, U, Hu);
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t j = 0; j < f; ++j) {
+            const double g = Hg[m * f + j] + (bg ? bg[j] : 0.0);
+            const double u = Hu[m * f + j] + (bu ? bu[j] : 0.0);
+            Hg[m * f + j] = g;
+            Hu[m * f + j] = u;
+            Y[m * f + j] = oracle_silu(g) * u;
+        }
+    matmul_nn(M, f, h, Y, B, Z);
+    if (b2) {
+        for (int64_t m = 0; m < M; ++m)
+            for (int64_t n = 0; n < h; ++n) Z[m * h + n] = Z[m * h + n] + b2[n];
+    }
+}
+
+/* work: 3 * M * f + M * h doubles of caller scratch (dY, dHg, dHu, dHu U^T). db* may be NULL. */
+void oracle_swiglu_bwd(int64_t M, int64_t h, int64_t f,
+                       const double* X, const double* G, const double* U, const double* B,
+                       const double* Hg, const double* Hu, const double* Y, const double* dZ,
+                       double* dX, double* dG, double* dU, double* dB, double* dbg, double* dbu, double* db2,
+                       double* work) {
+    double* dY = work;
+    double* dHg = work + M * f;
+    double* dHu = work + 2 * M * f;
+    matmul_tn(f, M, h, Y, dZ, dB);       /* dB = Y^T dZ */
+    matmul_nt(M, h, f, dZ, B, dY);       /* dY = dZ B^T */
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t j = 0; j < f; ++j) {
+            const double g = Hg[m * f + j], u = Hu[m * f + j], dy = dY[m * f + j];
+            dHg[m * f + j] = dy * u * oracle_silu_grad(g);
+            dHu[m * f + j] = dy * oracle_silu(g);
+        }
+    matmul_tn(h, M, f, X, dHg, dG);      /* dG = X^T dHg */
+    matmul_tn(h, M, f, X, dHu, dU);      /* dU = X^T dHu */
+    matmul_nt(M, f, h, dHg, G, dX);      /* dX = dHg G^T ... */
+    double* tmp = work + 3 * M * f;      /* dHu U^T */
+    matmul_nt(M, f, h, dHu, U, tmp);
+    for (int64_t i = 0; i < M * h; ++i) dX[i] += tmp[i];  /* ... + dHu U^T */
+    if (dbg) {
+        for (int64_t j = 0; j < f; ++j) { dbg[j] = 0.0; dbu[j] = 0.0; }
+        for (int64_t m = 0; m < M; ++m)
+            for (int64_t j = 0; j < f; ++j) { dbg[j] += dHg[m * f + j]; dbu[j] += dHu[m * f + j]; }
+    }
+    if (db2) {
+        for (int64_t n = 0; n < h; ++n) db2[n] = 0.0;
+        for (int64_t m = 0; m < M; ++m)
+            for (int64_t n = 0; n < h; ++n) db2[n] += dZ[m * h + n];
+    }
+}
+
+/*
+ * The packed SwiGLU weight layout of the CUDA path, as an index map: each shard's
+ * gate and up columns interleaved in blocks of 128 features,
+ *   W_sh[i][r][256 b + j] = G[r][i fs + 128 b + j]          (j < 128)
+ *                         = U[r][i fs + 128 b + j - 128]    (j >= 128),  fs = f / p.
+ * inverse = 1 unpacks W_sh into G and U.
+ */
+void oracle_swiglu_pack(int64_t elem_size, int64_t rows, int64_t f, int64_t p, int inverse,
+                        void* G, void* U, void* W_sh) {
+    const int64_t fs = f / p;
+    unsigned char* g = (unsigned char*)G;
+    unsigned char* u = (unsigned char*)U;
+    unsigned char* w = (unsigned char*)W_sh;
+    for (int64_t i = 0; i < p; ++i)
+        for (int64_t r = 0; r < rows; ++r)
+            for (int64_t c = 0; c < 2 * fs; ++c) {
+                const int64_t blk = c / 256, j = c % 256;
+                unsigned char* src = (j < 128 ? g : u) + (r * f + i * fs + 128 * blk + (j % 128)) * elem_size;
+                unsigned char* dst = w + ((i * rows + r) * 2 * fs + c) * elem_size;
+                if (!inverse) memcpy(dst, src, (size_t)elem_size);
+                else memcpy(src, dst, (size_t)elem_size);
+            }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Layout maps (integer index work; compared bit for bit).                   */
 

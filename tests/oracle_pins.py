@@ -334,6 +334,97 @@ def pin_qkv_interleave_commutes_with_projection(orc):
                 assert np.array_equal(got, Y[:, t * h + g * d: t * h + (g + 1) * d])
 
 
+# --------------------------------------------------------------------------
+# SwiGLU variant ([M2] M027: gated activations work on local pairs of the shard)
+
+def pin_silu_vs_library(orc):
+    for x in np.linspace(-30.0, 30.0, 241):
+        ref = x * special.expit(x)
+        assert abs(orc.silu(x) - ref) <= 1e-15 * max(1.0, abs(ref)) + 1e-300
+        eps = 1e-5
+        fd = (orc.silu(x + eps) - orc.silu(x - eps)) / (2 * eps)
+        assert abs(orc.silu_grad(x) - fd) < 1e-8
+    assert orc.silu(0.0) == 0.0 and abs(orc.silu_grad(0.0) - 0.5) < 1e-16
+
+
+def pin_swiglu_special_cases(orc):
+    """U = 0, bu = 1: Y = silu(X G + bg), so Z = silu(H) B with scipy's expit; and G = 0 with a large
+    gate bias (silu(40) = 40 up to 4e-17): the block is the affine map 40 (X U + bu) B + b2."""
+    r = _rng(13)
+    M, h, f = 6, 8, 20
+    X = r.standard_normal((M, h)); G = r.standard_normal((h, f)) * 0.4; U = r.standard_normal((h, f)) * 0.4
+    B = r.standard_normal((f, h)) * 0.4; bg = r.standard_normal(f) * 0.1; b2 = r.standard_normal(h) * 0.1
+    Hg, _, _, Z = orc.swiglu_fwd(X, G, np.zeros((h, f)), bg, np.ones(f), B, b2)
+    ref = (Hg * special.expit(Hg)) @ B + b2
+    assert np.max(np.abs(Hg - (X @ G + bg))) <= 1e-13 * np.max(np.abs(Hg))
+    assert np.max(np.abs(Z - ref)) <= 1e-13 * np.max(np.abs(ref))
+    bu = r.standard_normal(f) * 0.1
+    _, _, _, Z2 = orc.swiglu_fwd(X, np.zeros((h, f)), U, np.full(f, 40.0), bu, B, b2)
+    ref2 = 40.0 * (X @ U + bu) @ B + b2
+    assert np.max(np.abs(Z2 - ref2)) <= 1e-12 * np.max(np.abs(ref2))
+
+
+def pin_swiglu_sharded_equals_unsharded(orc):
+    """sum_i [silu(X G_i + bg_i) * (X U_i + bu_i)] B_i + b2 == the unsharded block, every divisor p."""
+    r = _rng(14)
+    M, h, f = 5, 6, 24
+    X = r.standard_normal((M, h)); G = r.standard_normal((h, f)) * 0.4; U = r.standard_normal((h, f)) * 0.4
+    B = r.standard_normal((f, h)) * 0.4; bg = r.standard_normal(f) * 0.1; bu = r.standard_normal(f) * 0.1
+    b2 = r.standard_normal(h) * 0.1
+    _, _, _, Z = orc.swiglu_fwd(X, G, U, bg, bu, B, b2)
+    for p in _divisors(f):
+        fs = f // p
+        acc = np.zeros((M, h))
+        for i in range(p):
+            sl = slice(i * fs, (i + 1) * fs)
+            _, _, _, Zi = orc.swiglu_fwd(X, np.ascontiguousarray(G[:, sl]), np.ascontiguousarray(U[:, sl]),
+                                         bg[sl], bu[sl], np.ascontiguousarray(B[sl, :]), None)
+            acc += Zi
+        assert np.max(np.abs(acc + b2 - Z)) <= 1e-12 * np.max(np.abs(Z))
+
+
+def pin_swiglu_gradients_finite_difference(orc):
+    r = _rng(15)
+    M, h, f = 3, 5, 8
+    X = r.standard_normal((M, h)); G = r.standard_normal((h, f)) * 0.5; U = r.standard_normal((h, f)) * 0.5
+    B = r.standard_normal((f, h)) * 0.5; bg = r.standard_normal(f) * 0.2; bu = r.standard_normal(f) * 0.2
+    b2 = r.standard_normal(h) * 0.2; dZ = r.standard_normal((M, h))
+    Hg, Hu, Y, _ = orc.swiglu_fwd(X, G, U, bg, bu, B, b2)
+    g = orc.swiglu_bwd(X, G, U, B, Hg, Hu, Y, dZ)
+    params = {"dX": X, "dG": G, "dU": U, "dB": B, "dbg": bg, "dbu": bu, "db2": b2}
+    for name, arr in params.items():
+        fd = np.zeros_like(arr)
+        it = np.nditer(arr, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            x0 = arr[idx]
+            eps = 1e-6 * max(1.0, abs(x0))
+            arr[idx] = x0 + eps
+            lp = float(np.sum(orc.swiglu_fwd(X, G, U, bg, bu, B, b2)[3] * dZ))
+            arr[idx] = x0 - eps
+            lm = float(np.sum(orc.swiglu_fwd(X, G, U, bg, bu, B, b2)[3] * dZ))
+            arr[idx] = x0
+            fd[idx] = (lp - lm) / (2 * eps)
+        assert np.linalg.norm(g[name] - fd) / np.linalg.norm(fd) <= 1e-6, name
+
+
+def pin_swiglu_pack_layout(orc):
+    """Brute force: packed column 256 b + j of shard i holds gate (j < 128) or up feature
+    i fs + 128 b + j mod 128; unpack inverts pack bit for bit."""
+    rows, p, fs = 3, 2, 256
+    f = p * fs
+    G = np.arange(rows * f, dtype=np.int64).reshape(rows, f) * 2
+    U = G + 1
+    W = orc.swiglu_pack(G, U, p)
+    for i in range(p):
+        for c in range(2 * fs):
+            b_, j = divmod(c, 256)
+            src = G if j < 128 else U
+            assert np.array_equal(W[i, :, c], src[:, i * fs + 128 * b_ + (j % 128)])
+    G2, U2 = orc.swiglu_unpack(W, p)
+    assert np.array_equal(G2, G) and np.array_equal(U2, U)
+
+
 ALL_PINS = [
     pin_gelu_closed_forms,
     pin_gelu_vs_library,
@@ -350,6 +441,11 @@ ALL_PINS = [
     pin_qkv_interleave_heads_on_one_rank,
     pin_linear_vs_numpy_and_fd,
     pin_qkv_interleave_commutes_with_projection,
+    pin_silu_vs_library,
+    pin_swiglu_special_cases,
+    pin_swiglu_sharded_equals_unsharded,
+    pin_swiglu_gradients_finite_difference,
+    pin_swiglu_pack_layout,
 ]
 
 

@@ -28,6 +28,12 @@ MUTANTS = {
     "sampled_dX_transposed_A": ("for (int64_t n = 0; n < h; ++n) out[n] += dh * A[n * f + j];",
                                 "for (int64_t n = 0; n < h; ++n) out[n] += dh * A[j * h + n];"),
     "sampled_dB_uses_H": ("const double y = act_fwd(act, hv);", "const double y = hv;"),
+    "swiglu_b2_dropped": ("Z[m * h + n] = Z[m * h + n] + b2[n];", "Z[m * h + n] = Z[m * h + n] + 0.0 * b2[n];"),
+    "silu_grad_missing_term": ("return s * (1.0 + x * (1.0 - s));", "return s;"),
+    "swiglu_dHu_uses_grad": ("dHu[m * f + j] = dy * oracle_silu(g);", "dHu[m * f + j] = dy * oracle_silu_grad(g);"),
+    "swiglu_pack_swapped": ("(j < 128 ? g : u)", "(j < 128 ? u : g)"),
+    "swiglu_dX_missing_up": ("for (int64_t i = 0; i < M * h; ++i) dX[i] += tmp[i];",
+                             "for (int64_t i = 0; i < M * h; ++i) dX[i] += 0.0 * tmp[i];"),
     "linear_bias_dropped": ("for (int64_t n = 0; n < N; ++n) Y[m * N + n] += b[n];",
                             "for (int64_t n = 0; n < N; ++n) Y[m * N + n] += 0.0 * b[n];"),
     "linear_dX_wrong_operand": ("matmul_nt(M, N, K, dY, W, dX);  /* dX = dY W^T  [M,K] */",
