@@ -159,6 +159,46 @@ tpmlp_status tpmlp_column_bwd(const void* X, const void* A_sh, const void* dY_sh
                               tpmlp_dtype dt, tpmlp_dtype grad_dt, void* stream);
 
 /*
+ * SwiGLU variant of the block (Level 2, M027: a gated activation works on local
+ * pairs of the FFN shard, so the column + row split still needs only the final sum):
+ *   Hg_i = X G_i + bg_i,  Hu_i = X U_i + bu_i,  Y_i = silu(Hg_i) * Hu_i,  Z = sum_i Y_i B_i + b2,
+ *   silu(x) = x / (1 + exp(-x)).
+ * The gate and up weights of each shard are packed by tpmlp_swiglu_pack into
+ *   W_sh [p][h][2 ffn/p]: columns 256 b .. 256 b + 127 = gate features 128 b ..,
+ *                         columns 256 b + 128 .. 256 b + 255 = up features 128 b ..
+ * bw_sh [p][2 ffn/p] is the packed bias (or NULL); Y_ws [p][M][ffn/p] holds Y on return;
+ * H_ws [p][M][2 ffn/p] fp32 (or NULL) receives the packed pre-activations for the backward, in
+ * fp32 because the backward multiplies by the up pre-activation itself (dHg = dY Hu silu'(Hg)):
+ * rounding Hg and Hu to bf16 would roughly double the bf16 error of dX against the GeLU block.
+ * Requires bf16, ffn % p == 0, h % p == 0 and ffn/p a multiple of 128.
+ */
+tpmlp_status tpmlp_swiglu_mlp_fwd(const void* X, const void* W_sh, const void* bw_sh, const void* B_sh,
+                                  const void* b2, void* Z, void* Y_ws, void* H_ws, int64_t s, int64_t b, int64_t h,
+                                  int64_t ffn, int p, tpmlp_dtype dt, void* stream);
+
+/*
+ * SwiGLU backward from dZ:  dY_i = dZ B_i^T,  dHg = dY Hu silu'(Hg),  dHu = dY silu(Hg),
+ *   dW_i = X^T [dHg | dHu] (packed), dbw_i = 1^T [dHg | dHu], dB_i = Y_i^T dZ, db2 = 1^T dZ,
+ *   dX = sum_i [dHg | dHu]_i W_i^T  (= dHg G^T + dHu U^T, summed on device).
+ *   silu'(x) = sigma(x) (1 + x (1 - sigma(x))).
+ * Inputs: X, W_sh, B_sh, Y_ws and dZ (bf16); H_ws (packed fp32 pre-activations from the forward).
+ * Outputs: dX bf16; dW_sh [p][h][2 ffn/p], dB_sh, dbw_sh [p][2 ffn/p] (or NULL), db2 (or NULL) grad_dt.
+ * Workspace: dH_ws [p][M][2 ffn/p] bf16 (holds the packed dHg, dHu on return).
+ */
+tpmlp_status tpmlp_swiglu_mlp_bwd(const void* X, const void* W_sh, const void* B_sh, const void* H_ws,
+                                  const void* Y_ws, const void* dZ, void* dX, void* dW_sh, void* dB_sh, void* dbw_sh,
+                                  void* db2, void* dH_ws, int64_t s, int64_t b, int64_t h, int64_t ffn, int p,
+                                  tpmlp_dtype dt, tpmlp_dtype grad_dt, void* stream);
+
+/*
+ * SwiGLU weight packing (bit-exact): G, U [rows][ffn] -> W_sh [p][rows][2 ffn/p] as described at
+ * tpmlp_swiglu_mlp_fwd (rows = 1 packs the biases); inverse != 0 unpacks W_sh into G and U.
+ * Requires ffn % p == 0 and ffn/p a multiple of 128.
+ */
+tpmlp_status tpmlp_swiglu_pack(void* G, void* U, void* W_sh, int64_t rows, int64_t ffn, int p, tpmlp_dtype dt,
+                               int inverse, void* stream);
+
+/*
  * The MLP block forward without a caller workspace.  The pages have no
  * counterpart: this entry point exists for callers that cannot allocate device
  * memory where they run the block (for example an inference-engine plugin whose

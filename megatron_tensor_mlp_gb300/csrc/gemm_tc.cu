@@ -235,6 +235,8 @@ tpmlp_status launch_tc_gemm(const Operand& a, const Operand& b, const GemmSpec& 
     const bool amn = a.mn_major, bmn = b.mn_major;
     if (g.epi == EPI_BIAS_ACT && !amn && bmn) return launch_variant<false, true, EPI_BIAS_ACT>(a, b, g, k, dev, st);
     if (g.epi == EPI_DGELU && !amn && !bmn) return launch_variant<false, false, EPI_DGELU>(a, b, g, k, dev, st);
+    if (g.epi == EPI_SWIGLU && !amn && bmn) return launch_variant<false, true, EPI_SWIGLU>(a, b, g, k, dev, st);
+    if (g.epi == EPI_DSWIGLU && !amn && !bmn) return launch_variant<false, false, EPI_DSWIGLU>(a, b, g, k, dev, st);
     if (g.epi == EPI_STORE && amn && bmn) return launch_variant<true, true, EPI_STORE>(a, b, g, k, dev, st);
     if (g.epi == EPI_STORE && !amn && !bmn) return launch_variant<false, false, EPI_STORE>(a, b, g, k, dev, st);
     set_error("internal: no tcgen05 GEMM variant for epi=%d a_mn=%d b_mn=%d", g.epi, (int)amn, (int)bmn);

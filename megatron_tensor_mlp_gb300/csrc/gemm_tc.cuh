@@ -172,6 +172,12 @@ __device__ __forceinline__ void dgelu_mul8(float* v, const float* h) {
     }
 }
 
+// sigma(x) = 1 / (1 + 2^(-x log2 e)) with the hardware approximations; silu(x) = x sigma(x),
+// silu'(x) = sigma(x) (1 + x (1 - sigma(x))).
+__device__ __forceinline__ float sigmoid_approx(float x) {
+    return rcp_approx(1.0f + ex2_approx(-1.4426950408889634f * x));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
@@ -256,6 +262,95 @@ __device__ __forceinline__ void epilogue_chunk(const KArgs& p, const uint32_t (&
         } else {
             __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.out) + shard * p.out_ss + (long long)gm * p.out_ld + gn0;
             store_bf16x32(d, v, nvalid);
+        }
+    }
+}
+
+// SwiGLU forward: TMEM columns [0,128) hold the gate and [128,256) the up projection of the
+// same 128 features (packed layout); this thread's row, features fo..fo+31 of tile nb.
+__device__ __forceinline__ void swiglu_chunk(const KArgs& p, const uint32_t (&rg)[32], const uint32_t (&ru)[32],
+                                             int gm, int nb, int fo, int shard) {
+    if (gm >= p.M) return;
+    float g[32], u[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        g[j] = __uint_as_float(rg[j]);
+        u[j] = __uint_as_float(ru[j]);
+    }
+    const long long pg = (long long)nb * 256 + fo;  // packed gate column (up = pg + 128)
+    if (p.bias != nullptr) {
+        const __nv_bfloat16* bp = static_cast<const __nv_bfloat16*>(p.bias) + shard * p.bias_ss + pg;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float bg[8], bu[8];
+            unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(bp + q * 8)), bg);
+            unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(bp + 128 + q * 8)), bu);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                g[q * 8 + i] += bg[i];
+                u[q * 8 + i] += bu[i];
+            }
+        }
+    }
+    if (p.out2 != nullptr) {  // fp32 pre-activations: the backward multiplies by u itself
+        float* d2 = static_cast<float*>(p.out2) + shard * p.out2_ss + (long long)gm * p.out2_ld + pg;
+        store_f32x32(d2, g, 32);
+        store_f32x32(d2 + 128, u, 32);
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) g[j] = g[j] * sigmoid_approx(g[j]) * u[j];
+    __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.out) + shard * p.out_ss + (long long)gm * p.out_ld +
+                       (long long)nb * 128 + fo;
+    store_bf16x32(d, g, 32);
+}
+
+// SwiGLU dgrad: acc = dY for features f0..f0+31; packed fp32 (g, u) pre-activations from aux,
+// packed bf16 (dg, du) to out:  dg = dY u silu'(g),  du = dY silu(g).
+__device__ __forceinline__ void dswiglu_chunk(const KArgs& p, const uint32_t (&r)[32], int gm, int f0, int shard) {
+    if (gm >= p.M || f0 >= p.N) return;
+    const long long pg = (long long)(f0 >> 7) * 256 + (f0 & 127);
+    const float* hp = static_cast<const float*>(p.aux) + shard * p.aux_ss + (long long)gm * p.aux_ld + pg;
+    __nv_bfloat16* op = static_cast<__nv_bfloat16*>(p.out) + shard * p.out_ss + (long long)gm * p.out_ld + pg;
+    float dg[32], du[32];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 g4 = *reinterpret_cast<const float4*>(hp + q * 4);
+        const float4 u4 = *reinterpret_cast<const float4*>(hp + 128 + q * 4);
+        const float g[4] = {g4.x, g4.y, g4.z, g4.w}, u[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float dy = __uint_as_float(r[q * 4 + i]);
+            const float sg = sigmoid_approx(g[i]);
+            dg[q * 4 + i] = dy * u[i] * (sg * (1.0f + g[i] * (1.0f - sg)));
+            du[q * 4 + i] = dy * g[i] * sg;
+        }
+    }
+    store_bf16x32(op, dg, 32);
+    store_bf16x32(op + 128, du, 32);
+}
+
+// One tile's epilogue for this warp: TMEM lane quarter q, column half `half`.
+template <int EPI>
+__device__ __forceinline__ void epilogue_tile(const KArgs& p, uint32_t t_row, int gm, int nb, int half, int shard) {
+    if constexpr (EPI == EPI_SWIGLU) {
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+            const int fo = half * 64 + c * 32;
+            uint32_t rg[32], ru[32];
+            tmem_ld_32x32b_x32(t_row + fo, rg);
+            tmem_ld_32x32b_x32(t_row + 128 + fo, ru);
+            tmem_ld_wait();
+            swiglu_chunk(p, rg, ru, gm, nb, fo, shard);
+        }
+    } else {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+            const int col = half * 128 + c * 32;
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(t_row + col, r);
+            tmem_ld_wait();
+            if constexpr (EPI == EPI_DSWIGLU) dswiglu_chunk(p, r, gm, nb * BN + col, shard);
+            else epilogue_chunk<EPI>(p, r, gm, nb * BN + col, shard);
         }
     }
 }
@@ -433,14 +528,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             decode_tile(p, t, mb, nb, shard);
             const int gm = mb * BM + q * 32 + lane;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                const int col = half * 128 + c * 32;
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + col, r);
-                tmem_ld_wait();
-                epilogue_chunk<EPI>(p, r, gm, nb * BN + col, shard);
-            }
+            epilogue_tile<EPI>(p, t_row, gm, nb, half, shard);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty + acc);
@@ -671,14 +759,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             decode_tile(p, t, mb, nb, shard);
             const int gm = mb * (2 * BM) + static_cast<int>(rank) * BM + q * 32 + lane;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                const int col = half * 128 + c * 32;
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + col, r);
-                tmem_ld_wait();
-                epilogue_chunk<EPI>(p, r, gm, nb * BN + col, shard);
-            }
+            epilogue_tile<EPI>(p, t_row, gm, nb, half, shard);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader0 + acc * 8);

@@ -13,6 +13,8 @@ enum EpiKind : int {
     EPI_BIAS_ACT = 0,  // out = act(acc + bias[n]); optional out2 = acc + bias (pre-activation)
     EPI_DGELU = 1,     // out = acc * GeLU'(aux[m][n])
     EPI_STORE = 2,     // out = acc (fp32 or bf16)
+    EPI_SWIGLU = 3,    // packed [gate 128 | up 128] tiles: out = silu(g + bg) * (u + bu); out2 = packed fp32 pre-activations
+    EPI_DSWIGLU = 4,   // acc = dY per feature; reads packed fp32 (g, u) from aux, writes packed bf16 (dg, du)
 };
 
 // One operand of D[M,N] = sum_k A[M,K] B[K,N], batched over shards.
@@ -68,6 +70,9 @@ tpmlp_status launch_shard_columns(const void* src, void* dst, int64_t rows, int6
 tpmlp_status launch_qkv_interleave(const void* src, void* dst, int64_t rows, int64_t h, int64_t n_heads,
                                    int esize, bool inverse, cudaStream_t st);
 tpmlp_status launch_debug_wait(uint32_t timeout_us, uint32_t* status, cudaStream_t st);
+// SwiGLU packed layout: W_sh[i][r][256 b + j] = (j < 128 ? G : U)[r][i fs + 128 b + j % 128]
+tpmlp_status launch_swiglu_pack(void* G, void* U, void* W_sh, int64_t rows, int64_t ffn, int p, int esize,
+                                bool inverse, cudaStream_t st);
 
 // Process-wide GEMM tiling mode (see tpmlp_set_gemm_mode).
 void set_gemm_mode(int mode);

@@ -228,6 +228,26 @@ __global__ void qkv_kernel(const T* __restrict__ src, T* __restrict__ dst, long 
     }
 }
 
+// SwiGLU packed layout in 16-byte units (u elements each; 128 is a multiple of u):
+// packed column c = 256 b + j of shard i  <->  (j < 128 ? G : U) column i fs + 128 b + j % 128.
+__global__ void swiglu_pack_kernel(uint4* __restrict__ G, uint4* __restrict__ U, uint4* __restrict__ W, long long rows,
+                                   long long f, long long fs, int p, int u, int inverse) {
+    const long long units_per_row = 2 * fs / u;
+    const long long total = (long long)p * rows * units_per_row;
+    for (long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x; x < total;
+         x += (long long)gridDim.x * blockDim.x) {
+        const long long i = x / (rows * units_per_row);
+        const long long rem = x - i * rows * units_per_row;
+        const long long r = rem / units_per_row;
+        const long long c = (rem - r * units_per_row) * u;
+        const long long blk = c >> 8, j = c & 255;
+        const long long src_col = i * fs + 128 * blk + (j & 127);
+        uint4* src = (j < 128 ? G : U) + (r * f + src_col) / u;
+        if (!inverse) W[x] = *src;
+        else *src = W[x];
+    }
+}
+
 // ------------------------------------------------------------------ bounded-wait hook
 __global__ void debug_wait_kernel(uint32_t* status, unsigned long long timeout_ns) {
     __shared__ uint64_t bar;
@@ -320,6 +340,17 @@ tpmlp_status launch_qkv_interleave(const void* src, void* dst, int64_t rows, int
             static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst), rows, cols, h, d, inverse ? 1 : 0);
     }
     return check_launch("QKV interleave");
+}
+
+tpmlp_status launch_swiglu_pack(void* G, void* U, void* W_sh, int64_t rows, int64_t ffn, int p, int esize,
+                                bool inverse, cudaStream_t st) {
+    const int u = 16 / esize;
+    const long long fs = ffn / p;
+    const long long total = (long long)p * rows * (2 * fs / u);
+    swiglu_pack_kernel<<<grid_for(total, 256), 256, 0, st>>>(static_cast<uint4*>(G), static_cast<uint4*>(U),
+                                                              static_cast<uint4*>(W_sh), rows, ffn, fs, p, u,
+                                                              inverse ? 1 : 0);
+    return check_launch("SwiGLU pack");
 }
 
 tpmlp_status launch_debug_wait(uint32_t timeout_us, uint32_t* status, cudaStream_t st) {

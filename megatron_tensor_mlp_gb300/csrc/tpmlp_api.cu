@@ -238,6 +238,19 @@ tpmlp_status do_column_bwd(const void* X, const void* A_sh, const void* dY_sh, v
     return TPMLP_OK;
 }
 
+// SwiGLU shape rules: ffn/p a multiple of 128 (gate/up blocks of 128 features), bf16 only.
+tpmlp_status check_swiglu(int64_t ffn, int p, tpmlp_dtype dt) {
+    if (dt != TPMLP_BF16) {
+        set_error("the SwiGLU block runs on bf16 tensors only");
+        return TPMLP_ERR_DTYPE;
+    }
+    if ((ffn / p) % 128 != 0) {
+        set_error("SwiGLU needs ffn/p to be a multiple of 128 (ffn=%lld, p=%d)", (long long)ffn, p);
+        return TPMLP_ERR_DIVISIBILITY;
+    }
+    return TPMLP_OK;
+}
+
 }  // namespace
 
 void set_error(const char* fmt, ...) {
@@ -446,6 +459,117 @@ tpmlp_status tpmlp_column_bwd(const void* X, const void* A_sh, const void* dY_sh
     if (M == 0) return TPMLP_OK;
     return do_column_bwd(X, A_sh, dY_sh, dX, dA_sh, db1_sh, M, h, ffn, p, dt, grad_dt == TPMLP_F32, *dev,
                          static_cast<cudaStream_t>(stream));
+}
+
+tpmlp_status tpmlp_swiglu_mlp_fwd(const void* X, const void* W_sh, const void* bw_sh, const void* B_sh,
+                                  const void* b2, void* Z, void* Y_ws, void* H_ws, int64_t s, int64_t b, int64_t h,
+                                  int64_t ffn, int p, tpmlp_dtype dt, void* stream) {
+    if (!X || !W_sh || !B_sh || !Z || !Y_ws) {
+        set_error("X, W_sh, B_sh, Z and Y_ws must not be NULL");
+        return TPMLP_ERR_NULL;
+    }
+    TP_TRY(check_mlp_shape(s, b, h, ffn, p, true));
+    TP_TRY(check_dtype(dt));
+    TP_TRY(check_swiglu(ffn, p, dt));
+    const int64_t M = s * b, fs = ffn / p, es = esize(dt);
+    TP_TRY(check_aligned({X, W_sh, bw_sh, B_sh, b2, Z, Y_ws, H_ws}));
+    TP_TRY(check_pitch(h, dt, "h"));
+    TP_TRY(check_alias({{Z, M * h * es}, {Y_ws, M * ffn * es}, {H_ws, 2 * M * ffn * 4}},
+                       {{X, M * h * es}, {W_sh, 2 * h * ffn * es}, {bw_sh, 2 * ffn * es}, {B_sh, ffn * h * es},
+                        {b2, h * es}}));
+    const DeviceInfo* dev;
+    TP_TRY(get_device(&dev));
+    if (M == 0) return TPMLP_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    {
+        Operand a{X, h, 0, 1, false};                  // X [M][h], K-major
+        Operand bb{W_sh, 2 * fs, h * 2 * fs, p, true};  // packed [gate|up] W_i [h][2 fs], MN-major
+        GemmSpec g = spec_base();
+        g.M = M; g.N = 2 * fs; g.K = h; g.n_shards = p;
+        g.a_batched = false; g.b_batched = true;
+        g.epi = EPI_SWIGLU;
+        g.out = Y_ws; g.out_ld = fs; g.out_ss = M * fs;
+        g.out2 = H_ws; g.out2_ld = 2 * fs; g.out2_ss = M * 2 * fs;
+        g.bias = bw_sh; g.bias_ss = 2 * fs;
+        TP_TRY(run_gemm(a, bb, g, dt, *dev, st));
+    }
+    return do_row(Y_ws, B_sh, b2, Z, M, h, ffn, p, dt, *dev, st);
+}
+
+tpmlp_status tpmlp_swiglu_mlp_bwd(const void* X, const void* W_sh, const void* B_sh, const void* H_ws,
+                                  const void* Y_ws, const void* dZ, void* dX, void* dW_sh, void* dB_sh, void* dbw_sh,
+                                  void* db2, void* dH_ws, int64_t s, int64_t b, int64_t h, int64_t ffn, int p,
+                                  tpmlp_dtype dt, tpmlp_dtype grad_dt, void* stream) {
+    if (!X || !W_sh || !B_sh || !H_ws || !Y_ws || !dZ || !dX || !dW_sh || !dB_sh || !dH_ws) {
+        set_error("only dbw_sh and db2 may be NULL");
+        return TPMLP_ERR_NULL;
+    }
+    TP_TRY(check_mlp_shape(s, b, h, ffn, p, true));
+    TP_TRY(check_dtype(dt));
+    TP_TRY(check_dtype(grad_dt));
+    TP_TRY(check_swiglu(ffn, p, dt));
+    const int64_t M = s * b, fs = ffn / p, es = esize(dt), gs = esize(grad_dt);
+    TP_TRY(check_aligned({X, W_sh, B_sh, H_ws, Y_ws, dZ, dX, dW_sh, dB_sh, dbw_sh, db2, dH_ws}));
+    TP_TRY(check_pitch(h, dt, "h"));
+    TP_TRY(check_alias({{dX, M * h * es}, {dW_sh, 2 * h * ffn * gs}, {dB_sh, ffn * h * gs}, {dbw_sh, 2 * ffn * gs},
+                        {db2, h * gs}, {dH_ws, 2 * M * ffn * es}},
+                       {{X, M * h * es}, {W_sh, 2 * h * ffn * es}, {B_sh, ffn * h * es}, {H_ws, 2 * M * ffn * 4},
+                        {Y_ws, M * ffn * es}, {dZ, M * h * es}}));
+    const DeviceInfo* dev;
+    TP_TRY(get_device(&dev));
+    if (M == 0) return TPMLP_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool gf32 = grad_dt == TPMLP_F32;
+    {
+        // dY = dZ B_i^T per feature; the epilogue writes the packed (dHg, dHu)
+        Operand a{dZ, h, 0, 1, false};
+        Operand bb{B_sh, h, fs * h, p, false};
+        GemmSpec g = spec_base();
+        g.M = M; g.N = fs; g.K = h; g.n_shards = p;
+        g.a_batched = false; g.b_batched = true;
+        g.epi = EPI_DSWIGLU;
+        g.aux = H_ws; g.aux_ld = 2 * fs; g.aux_ss = M * 2 * fs;
+        g.out = dH_ws; g.out_ld = 2 * fs; g.out_ss = M * 2 * fs;
+        TP_TRY(run_gemm(a, bb, g, dt, *dev, st));
+    }
+    if (db2) TP_TRY(launch_colsum(dZ, false, 1, M, h, db2, gf32, st));
+    {
+        Operand a{Y_ws, fs, M * fs, p, true};          // dB_i = Y_i^T dZ
+        Operand bb{dZ, h, 0, 1, true};
+        GemmSpec g = spec_base();
+        g.M = fs; g.N = h; g.K = M; g.n_shards = p;
+        g.a_batched = true; g.b_batched = false;
+        g.epi = EPI_STORE; g.out_f32 = gf32;
+        g.out = dB_sh; g.out_ld = h; g.out_ss = fs * h;
+        TP_TRY(run_gemm(a, bb, g, dt, *dev, st));
+    }
+    // the packed gate/up layer is a column layer of width 2 ffn: dW = X^T dH, dbw, dX = sum_i dH_i W_i^T
+    return do_column_bwd(X, W_sh, dH_ws, dX, dW_sh, dbw_sh, M, h, 2 * ffn, p, dt, gf32, *dev, st);
+}
+
+tpmlp_status tpmlp_swiglu_pack(void* G, void* U, void* W_sh, int64_t rows, int64_t ffn, int p, tpmlp_dtype dt,
+                               int inverse, void* stream) {
+    if (!G || !U || !W_sh) {
+        set_error("pointers must not be NULL");
+        return TPMLP_ERR_NULL;
+    }
+    if (rows < 0 || ffn < 1 || p < 1 || rows > kMaxDim || ffn > kMaxDim) {
+        set_error("bad shape rows=%lld ffn=%lld p=%d", (long long)rows, (long long)ffn, p);
+        return TPMLP_ERR_SHAPE;
+    }
+    if (ffn % p != 0 || (ffn / p) % 128 != 0) {
+        set_error("SwiGLU packing needs ffn %% p == 0 and ffn/p a multiple of 128");
+        return TPMLP_ERR_DIVISIBILITY;
+    }
+    TP_TRY(check_dtype(dt));
+    TP_TRY(check_aligned({G, U, W_sh}));
+    const int64_t bytes = rows * ffn * esize(dt);
+    if (!inverse) TP_TRY(check_alias({{W_sh, 2 * bytes}}, {{G, bytes}, {U, bytes}}));
+    else TP_TRY(check_alias({{G, bytes}, {U, bytes}}, {{W_sh, 2 * bytes}}));
+    const DeviceInfo* dev;
+    TP_TRY(get_device(&dev));
+    if (rows == 0) return TPMLP_OK;
+    return launch_swiglu_pack(G, U, W_sh, rows, ffn, p, esize(dt), inverse != 0, static_cast<cudaStream_t>(stream));
 }
 
 static tpmlp_status shard_common(const void* src, void* dst, int64_t rows, int64_t cols, int p, tpmlp_dtype dt,

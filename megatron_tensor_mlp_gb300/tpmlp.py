@@ -37,6 +37,9 @@ _SIGS = {
     "tpmlp_mlp_fwd": [_vp] * 8 + [_i64] * 4 + [_i32, _i32, _vp],
     "tpmlp_mlp_bwd": [_vp] * 12 + [_i64] * 4 + [_i32, _i32, _i32, _vp],
     "tpmlp_mlp_fwd_noalloc": [_vp] * 6 + [_i64] * 4 + [_i32, _i32, _vp],
+    "tpmlp_swiglu_mlp_fwd": [_vp] * 8 + [_i64] * 4 + [_i32, _i32, _vp],
+    "tpmlp_swiglu_mlp_bwd": [_vp] * 12 + [_i64] * 4 + [_i32, _i32, _i32, _vp],
+    "tpmlp_swiglu_pack": [_vp] * 3 + [_i64, _i64, _i32, _i32, _i32, _vp],
     "tpmlp_row_bwd": [_vp] * 7 + [_i64] * 4 + [_i32, _i32, _i32, _i32, _vp],
     "tpmlp_column_bwd": [_vp] * 6 + [_i64] * 4 + [_i32, _i32, _i32, _vp],
     "tpmlp_shard_columns": [_vp, _vp, _i64, _i64, _i32, _i32, _vp],
@@ -127,6 +130,26 @@ def tpmlp_mlp_bwd(X, A_sh, B_sh, H_sh, Y_sh, dZ, dX, dA_sh, dB_sh, db1_sh, db2, 
     st = lib.tpmlp_mlp_bwd(_ptr(X), _ptr(A_sh), _ptr(B_sh), _ptr(H_sh), _ptr(Y_sh), _ptr(dZ), _ptr(dX), _ptr(dA_sh),
                            _ptr(dB_sh), _ptr(db1_sh), _ptr(db2), _ptr(dH_ws), s, b, h, ffn, p, dt, grad_dt,
                            _stream(stream))
+    return _done(st, check)
+
+
+def tpmlp_swiglu_mlp_fwd(X, W_sh, bw_sh, B_sh, b2, Z, Y_ws, H_ws, s, b, h, ffn, p, dt=BF16, stream=None,
+                         check=True):
+    st = lib.tpmlp_swiglu_mlp_fwd(_ptr(X), _ptr(W_sh), _ptr(bw_sh), _ptr(B_sh), _ptr(b2), _ptr(Z), _ptr(Y_ws),
+                                  _ptr(H_ws), s, b, h, ffn, p, dt, _stream(stream))
+    return _done(st, check)
+
+
+def tpmlp_swiglu_mlp_bwd(X, W_sh, B_sh, H_ws, Y_ws, dZ, dX, dW_sh, dB_sh, dbw_sh, db2, dH_ws, s, b, h, ffn, p,
+                         dt=BF16, grad_dt=F32, stream=None, check=True):
+    st = lib.tpmlp_swiglu_mlp_bwd(_ptr(X), _ptr(W_sh), _ptr(B_sh), _ptr(H_ws), _ptr(Y_ws), _ptr(dZ), _ptr(dX),
+                                  _ptr(dW_sh), _ptr(dB_sh), _ptr(dbw_sh), _ptr(db2), _ptr(dH_ws), s, b, h, ffn, p, dt,
+                                  grad_dt, _stream(stream))
+    return _done(st, check)
+
+
+def tpmlp_swiglu_pack(G, U, W_sh, rows, ffn, p, dt=BF16, inverse=0, stream=None, check=True):
+    st = lib.tpmlp_swiglu_pack(_ptr(G), _ptr(U), _ptr(W_sh), rows, ffn, p, dt, int(inverse), _stream(stream))
     return _done(st, check)
 
 
