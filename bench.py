@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--workload", type=int, default=MAIN_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fwd-pages", action="store_true")
+    ap.add_argument("--no-next-rows", action="store_true", help="skip the SwiGLU / attention-projection timings")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     return ap.parse_args()
@@ -235,6 +236,89 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------------- GPU arm
+def time_next_rows(stream, steps, peaks):
+    """Forward+backward timings of the widened rows at the fwd+bwd workload's sizes
+    (s=2048, b=4, h=5120, p=4): the SwiGLU block (ffn=20480 per branch) and the attention
+    tensor-parallel projections (QKV column projection over the per-head interleave, 40 heads,
+    and the output row projection).  Inputs are seeded synthetic bf16."""
+    import torch
+    from megatron_tensor_mlp_gb300 import synth
+    from megatron_tensor_mlp_gb300 import tpmlp as T
+
+    s, b, h, f, p, heads = 2048, 4, 5120, 20480, 4, 40
+    M, fs = s * b, f // p
+    bf = torch.bfloat16
+    gen = lambda stream_id, shp, sig: torch.from_numpy(  # noqa: E731
+        synth.normal(11, stream_id, shp, sig, "bf16").view("int16")).view(bf).cuda()
+    out = {}
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        z.record(stream)
+        torch.cuda.synchronize()
+        T.tpmlp_device_status()
+        return a.elapsed_time(z) / n
+
+    n = max(10, steps // 4)
+    # SwiGLU block: gate+up column GEMM (2*2*M*h*f), row GEMM (2*M*f*h); backward twice that
+    X, dZ = gen(1, (M, h), 1.0), gen(6, (M, h), 1.0)
+    W = torch.empty((p, h, 2 * fs), dtype=bf, device="cuda")
+    T.tpmlp_swiglu_pack(gen(2, (h, f), 0.02), gen(9, (h, f), 0.02), W, h, f, p)
+    B = gen(3, (f, h), 0.02).view(p, fs, h)
+    Z, Y = torch.empty((M, h), dtype=bf, device="cuda"), torch.empty((p, M, fs), dtype=bf, device="cuda")
+    H = torch.empty((p, M, 2 * fs), dtype=torch.float32, device="cuda")
+    dX, dH = torch.empty((M, h), dtype=bf, device="cuda"), torch.empty((p, M, 2 * fs), dtype=bf, device="cuda")
+    dW = torch.empty((p, h, 2 * fs), dtype=torch.float32, device="cuda")
+    dB = torch.empty((p, fs, h), dtype=torch.float32, device="cuda")
+    dbw, db2 = torch.empty((p, 2 * fs), dtype=torch.float32, device="cuda"), torch.empty(h, dtype=torch.float32,
+                                                                                         device="cuda")
+
+    def swiglu_step():
+        T.tpmlp_swiglu_mlp_fwd(X, W, None, B, None, Z, Y, H, s, b, h, f, p, stream=stream)
+        T.tpmlp_swiglu_mlp_bwd(X, W, B, H, Y, dZ, dX, dW, dB, dbw, db2, dH, s, b, h, f, p, stream=stream)
+
+    ms = timed(swiglu_step, n)
+    flops = 3 * (2 * 2 * M * h * f + 2 * M * f * h)  # fwd 6 M h f, bwd 12 M h f
+    tf = flops / (ms * 1e-3) / 1e12
+    out["swiglu_fwd_bwd"] = {"shape": f"s{s} b{b} h{h} ffn{f} p{p}", "ms": round(ms, 4), "TFLOP/s": round(tf, 1),
+                             "pct_of_nominal_2250": round(100 * tf / NOMINAL_BF16_TFLOPS, 2)}
+    del W, H, dW, dH, Y, dB, dbw
+    torch.cuda.empty_cache()
+
+    # attention projections: QKV [h, 3h] column parallel by heads, output [h, h] row parallel
+    Wq = torch.empty((h, 3 * h), dtype=bf, device="cuda")
+    T.tpmlp_qkv_interleave(gen(12, (h, 3 * h), 0.02), Wq, h, h, heads, p)
+    Wq_sh = torch.empty((p, h, 3 * h // p), dtype=bf, device="cuda")
+    T.tpmlp_shard_columns(Wq, Wq_sh, h, 3 * h, p)
+    Wo = gen(13, (h, h), 0.02).view(p, h // p, h)
+    QKV = torch.empty((p, M, 3 * h // p), dtype=bf, device="cuda")
+    ctx = gen(14, (p, M, h // p), 1.0)
+    dQKV = gen(15, (p, M, 3 * h // p), 1.0)
+    dWq = torch.empty((p, h, 3 * h // p), dtype=torch.float32, device="cuda")
+    dWo = torch.empty((p, h // p, h), dtype=torch.float32, device="cuda")
+    dctx = torch.empty((p, M, h // p), dtype=bf, device="cuda")
+
+    def attn_step():
+        T.tpmlp_column_fwd(X, Wq_sh, None, QKV, None, s, b, h, 3 * h, p, act=T.ACT_NONE, stream=stream)
+        T.tpmlp_row_fwd(ctx, Wo, None, Z, s, b, h, h, p, stream=stream)
+        T.tpmlp_row_bwd(ctx, Wo, dZ, None, dctx, dWo, None, s, b, h, h, p, act=T.ACT_NONE, stream=stream)
+        T.tpmlp_column_bwd(X, Wq_sh, dQKV, dX, dWq, None, s, b, h, 3 * h, p, stream=stream)
+
+    ms = timed(attn_step, n)
+    flops = 3 * (2 * M * h * 3 * h + 2 * M * h * h)
+    tf = flops / (ms * 1e-3) / 1e12
+    out["attention_projections_fwd_bwd"] = {"shape": f"s{s} b{b} h{h} heads{heads} p{p}", "ms": round(ms, 4),
+                                            "TFLOP/s": round(tf, 1),
+                                            "pct_of_nominal_2250": round(100 * tf / NOMINAL_BF16_TFLOPS, 2)}
+    return out
+
+
 def run_gpu(args):
     import torch
 
@@ -428,6 +512,11 @@ def run_gpu(args):
         del b4
         torch.cuda.empty_cache()
 
+    next_rows = None
+    if not args.no_next_rows and args.workload == MAIN_WORKLOAD:
+        torch.cuda.empty_cache()
+        next_rows = time_next_rows(stream, K, peaks)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         sample = OracleSample(wl)
@@ -447,7 +536,7 @@ def run_gpu(args):
                "pct_of_nominal_bf16_peak": round(100 * value / ws / NOMINAL_BF16_TFLOPS, 2),
                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                "gpu_launches": launches_per_step * K, "clocks": clocks,
-               "fwd_pages_sizing": fwd_pages}
+               "fwd_pages_sizing": fwd_pages, "next_rows": next_rows}
         print(json.dumps(out), flush=True)
     if ws > 1:
         import torch.distributed as dist
