@@ -285,6 +285,14 @@ int tpmlp_get_gemm_mode(void);
 tpmlp_status tpmlp_set_gemm_raster(int group_m);
 int tpmlp_get_gemm_raster(void);
 
+/*
+ * Tail of the CTA-pair tilings, process wide: 1 runs the tiles of a last wave that fills at
+ * most half of the co-resident pairs as two 256x128 halves each, so that the tail costs half a
+ * wave; 0 (default) keeps whole tiles.  Affects speed only; other values TPMLP_ERR_SHAPE.
+ */
+tpmlp_status tpmlp_set_gemm_tail_split(int on);
+int tpmlp_get_gemm_tail_split(void);
+
 /* Human-readable name of a status code. */
 const char* tpmlp_status_string(tpmlp_status st);
 

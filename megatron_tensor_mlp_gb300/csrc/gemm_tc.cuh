@@ -61,6 +61,7 @@ struct KArgs {
     int m_blocks, n_blocks, batch, num_tiles, kb_per_shard, k_iters, group_m;
     int act, out_f32;
     int a_chunked, b_chunked;  // MN-major operand loaded with one 4-D box per stage (MN extent % 64 == 0)
+    int num_items, split_from;  // pair kernel: items >= split_from are half-width (256x128) tiles
     void* out; long long out_ld, out_ss;
     void* out2; long long out2_ld, out2_ss;
     const void* bias; long long bias_ss;
@@ -329,10 +330,14 @@ __device__ __forceinline__ void dswiglu_chunk(const KArgs& p, const uint32_t (&r
     store_bf16x32(op + 128, du, 32);
 }
 
-// One tile's epilogue for this warp: TMEM lane quarter q, column half `half`.
+// One tile's epilogue for this warp: TMEM lane quarter of the caller, `nchunks` chunks of 32
+// accumulator columns starting at col_base; output column = n_base + accumulator column.
 template <int EPI>
-__device__ __forceinline__ void epilogue_tile(const KArgs& p, uint32_t t_row, int gm, int nb, int half, int shard) {
+__device__ __forceinline__ void epilogue_tile(const KArgs& p, uint32_t t_row, int gm, int n_base, int col_base,
+                                              int nchunks, int shard) {
     if constexpr (EPI == EPI_SWIGLU) {
+        // whole tiles only: [gate 128 | up 128] of features n_base/2 .. n_base/2 + 127
+        const int half = col_base >> 7;
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
             const int fo = half * 64 + c * 32;
@@ -340,17 +345,17 @@ __device__ __forceinline__ void epilogue_tile(const KArgs& p, uint32_t t_row, in
             tmem_ld_32x32b_x32(t_row + fo, rg);
             tmem_ld_32x32b_x32(t_row + 128 + fo, ru);
             tmem_ld_wait();
-            swiglu_chunk(p, rg, ru, gm, nb, fo, shard);
+            swiglu_chunk(p, rg, ru, gm, n_base / BN, fo, shard);
         }
     } else {
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-            const int col = half * 128 + c * 32;
+        for (int c = 0; c < nchunks; ++c) {
+            const int col = col_base + c * 32;
             uint32_t r[32];
             tmem_ld_32x32b_x32(t_row + col, r);
             tmem_ld_wait();
-            if constexpr (EPI == EPI_DSWIGLU) dswiglu_chunk(p, r, gm, nb * BN + col, shard);
-            else epilogue_chunk<EPI>(p, r, gm, nb * BN + col, shard);
+            if constexpr (EPI == EPI_DSWIGLU) dswiglu_chunk(p, r, gm, n_base + col, shard);
+            else epilogue_chunk<EPI>(p, r, gm, n_base + col, shard);
         }
     }
 }
@@ -528,7 +533,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             decode_tile(p, t, mb, nb, shard);
             const int gm = mb * BM + q * 32 + lane;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-            epilogue_tile<EPI>(p, t_row, gm, nb, half, shard);
+            epilogue_tile<EPI>(p, t_row, gm, nb * BN, half * 128, 4, shard);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty + acc);
@@ -571,10 +576,26 @@ constexpr int P_B_BYTES = (BN / 2) * BK * 2;  // 16 KiB: this CTA's 128 columns 
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + BAR_BYTES;
 
+// Work item t of the pair kernel: a whole 256x256 tile (t < split_from) or one half
+// (256x128) of tile split_from + (t - split_from) / 2.  n0 = first output column, full = width 256.
+// Returns false for a half item that lies entirely beyond N (all roles skip it).
+__device__ __forceinline__ bool decode_item(const KArgs& p, int t, int& mb, int& nb, int& shard, int& n0, bool& full) {
+    int tile = t, sub = 0;
+    full = t < p.split_from;
+    if (!full) {
+        const int u = t - p.split_from;
+        tile = p.split_from + (u >> 1);
+        sub = u & 1;
+    }
+    decode_tile(p, tile, mb, nb, shard);
+    n0 = nb * BN + sub * (BN / 2);
+    return n0 < p.N;
+}
+
 template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const KArgs p) {
+                     const __grid_constant__ CUtensorMap tmB_half, const KArgs p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
@@ -609,6 +630,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (p.split_from < p.num_items) tma_prefetch_desc(&tmB_half);
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, TMEM_COLS);
@@ -629,11 +651,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             const int k_end = p.kb_per_shard * BK;
             const uint32_t full_leader0 = mapa_shared(smem_u32(full), 0);  // the leader's barriers
-            for (int t = cluster_id; t < p.num_tiles && ok; t += n_clusters) {
-                int mb, nb, shard;
-                decode_tile(p, t, mb, nb, shard);
+            for (int t = cluster_id; t < p.num_items && ok; t += n_clusters) {
+                int mb, nb, shard, n0;
+                bool full_tile;
+                if (!decode_item(p, t, mb, nb, shard, n0, full_tile)) continue;
                 const int row0 = mb * (2 * BM) + static_cast<int>(rank) * BM;
-                const int col0 = nb * BN + static_cast<int>(rank) * (BN / 2);
+                // this CTA's share of the item's columns: 128 of a whole tile, 64 of a half tile
+                const int col0 = n0 + static_cast<int>(rank) * (full_tile ? BN / 2 : BN / 4);
+                const uint32_t stage_tx = full_tile ? 2 * P_STAGE_BYTES : 2 * (P_A_BYTES + P_B_BYTES / 2);
+                const CUtensorMap* mapB = full_tile ? &tmB : &tmB_half;
                 int sa = p.sum_shards ? 0 : (p.a_batched ? shard : 0);
                 int sb = p.sum_shards ? 0 : (p.b_batched ? shard : 0);
                 int k0 = 0;
@@ -643,7 +669,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     if (leader) {
-                        mbar_arrive_expect_tx(full + stage, 2 * P_STAGE_BYTES);
+                        mbar_arrive_expect_tx(full + stage, stage_tx);
                         armed |= 1u << stage;
                         last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                     }
@@ -660,13 +686,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             tma_load_3d_pair(a_dst + c * MN_CHUNK_BYTES, &tmA, bar, row0 + c * 64, k0, sa);
                     }
                     if constexpr (!B_MN) {
-                        tma_load_3d_pair(b_dst, &tmB, bar, k0, col0, sb);
+                        tma_load_3d_pair(b_dst, mapB, bar, k0, col0, sb);
                     } else if (p.b_chunked) {
-                        tma_load_4d_pair(b_dst, &tmB, bar, 0, k0, col0 / 64, sb);
+                        tma_load_4d_pair(b_dst, mapB, bar, 0, k0, col0 / 64, sb);
                     } else {
-#pragma unroll
-                        for (int c = 0; c < (BN / 2) / 64; ++c)
-                            tma_load_3d_pair(b_dst + c * MN_CHUNK_BYTES, &tmB, bar, col0 + c * 64, k0, sb);
+                        // 64-wide boxes of the un-chunked map; a half tile needs one of them
+                        tma_load_3d_pair(b_dst, &tmB, bar, col0, k0, sb);
+                        if (full_tile) tma_load_3d_pair(b_dst + MN_CHUNK_BYTES, &tmB, bar, col0 + 64, k0, sb);
                     }
                     if (++stage == P_STAGES) {
                         stage = 0;
@@ -696,7 +722,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             if (leader) {
                 // -------------------------------------------------------- UMMA issuer (leader)
-                constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
+                constexpr uint32_t idesc_full = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
+                constexpr uint32_t idesc_half = idesc_bf16_f32(2 * BM, BN / 2, A_MN, B_MN);
                 const uint64_t a_desc0 = A_MN ? sdesc_sw128(smem_u32(sA), TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES)
                                               : sdesc_sw128(smem_u32(sA), 16, 1024);
                 const uint64_t b_desc0 = B_MN ? sdesc_sw128(smem_u32(sB), TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES)
@@ -707,9 +734,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 uint32_t phase = 0;
                 int lt = 0;
                 bool ok = true;
-                for (int t = cluster_id; t < p.num_tiles && ok; t += n_clusters, ++lt) {
+                for (int t = cluster_id; t < p.num_items && ok; t += n_clusters) {
+                    int mb, nb, shard, n0;
+                    bool full_tile;
+                    if (!decode_item(p, t, mb, nb, shard, n0, full_tile)) continue;
+                    const uint32_t idesc = full_tile ? idesc_full : idesc_half;
                     const int acc = lt & 1;
                     const uint32_t acc_phase = (lt >> 1) & 1;
+                    ++lt;
                     if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, p.status, p.timeout_ns, kWhereMma)) {
                         ok = false;
                         break;
@@ -747,19 +779,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int half = (warp - FIRST_EPI_WARP) >> 2;
         const uint32_t tempty_leader0 = mapa_shared(smem_u32(tempty), 0);
         int lt = 0;
-        for (int t = cluster_id; t < p.num_tiles; t += n_clusters, ++lt) {
+        for (int t = cluster_id; t < p.num_items; t += n_clusters) {
+            int mb, nb, shard, n0;
+            bool full_tile;
+            if (!decode_item(p, t, mb, nb, shard, n0, full_tile)) continue;
             const int acc = lt & 1;
             const uint32_t acc_phase = (lt >> 1) & 1;
+            ++lt;
             int okw = 0;
             if (lane == 0) okw = mbar_wait_bounded(tfull + acc, acc_phase, p.status, p.timeout_ns, kWhereEpilogue);
             okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
             if (!okw) break;
             tc_fence_after();
-            int mb, nb, shard;
-            decode_tile(p, t, mb, nb, shard);
             const int gm = mb * (2 * BM) + static_cast<int>(rank) * BM + q * 32 + lane;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-            epilogue_tile<EPI>(p, t_row, gm, nb, half, shard);
+            // a whole tile: 128 columns per warp; a half tile: 64
+            if (full_tile) epilogue_tile<EPI>(p, t_row, gm, n0, half * 128, 4, shard);
+            else epilogue_tile<EPI>(p, t_row, gm, n0, half * 64, 2, shard);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader0 + acc * 8);

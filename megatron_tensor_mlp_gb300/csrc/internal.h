@@ -79,5 +79,7 @@ void set_gemm_mode(int mode);
 int get_gemm_mode();
 void set_group_m(int g);
 int get_group_m();
+void set_tail_split(int on);
+int get_tail_split();
 
 }  // namespace tpmlp

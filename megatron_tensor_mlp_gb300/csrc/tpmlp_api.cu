@@ -720,4 +720,15 @@ tpmlp_status tpmlp_set_gemm_raster(int group_m) {
 
 int tpmlp_get_gemm_raster(void) { return get_group_m(); }
 
+tpmlp_status tpmlp_set_gemm_tail_split(int on) {
+    if (on != 0 && on != 1) {
+        set_error("tail split must be 0 or 1");
+        return TPMLP_ERR_SHAPE;
+    }
+    set_tail_split(on);
+    return TPMLP_OK;
+}
+
+int tpmlp_get_gemm_tail_split(void) { return get_tail_split(); }
+
 }  // extern "C"

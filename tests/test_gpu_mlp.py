@@ -17,13 +17,16 @@ def env():
     return harness, synth, tpmlp
 
 
-@pytest.fixture(params=[1, 2], ids=["single-cta", "cta-pair"])
+@pytest.fixture(params=[(1, 0), (2, 0), (2, 1)], ids=["single-cta", "cta-pair", "cta-pair-split-tail"])
 def gemm_mode(request, env):
-    """Force 128x256 single-CTA tiles or 256x256 CTA-pair tiles for the test."""
+    """Force 128x256 single-CTA tiles, or 256x256 CTA-pair tiles with whole or split tail tiles."""
     T = env[2]
-    T.tpmlp_set_gemm_mode(request.param)
-    yield request.param
+    mode, split = request.param
+    T.tpmlp_set_gemm_mode(mode)
+    T.tpmlp_set_gemm_tail_split(split)
+    yield mode
     T.tpmlp_set_gemm_mode(0)
+    T.tpmlp_set_gemm_tail_split(0)
 
 
 # (s, b, h, ffn, p): tiles are 128 (tokens) x 256 (outputs) x 64 (reduction)
@@ -222,3 +225,15 @@ def test_single_and_pair_tiles_agree(env, orc):
     T.tpmlp_set_gemm_mode(0)
     for a, b_ in zip(out[1], out[2]):
         assert torch.equal(a, b_)
+
+
+def test_tail_tiles_split_in_half(env, orc):
+    """A shape whose row and dX GEMMs have 80 pair tiles (76 pairs fit at once): the last 4
+    tiles run as 256x128 halves, and the weight-gradient GEMMs split every tile."""
+    _, synth, T = env
+    wl = synth.custom(320, 8, 2048, 1024, 2, dtype="bf16", sigma_w=0.03, sigma_bias=0.05, seed=77)
+    T.tpmlp_set_gemm_tail_split(1)
+    try:
+        _run_and_check(env, orc, wl)
+    finally:
+        T.tpmlp_set_gemm_tail_split(0)
