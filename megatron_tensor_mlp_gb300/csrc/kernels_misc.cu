@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtArgs p) {
     __shared__ float sa[SK][ST + 1];
     __shared__ float sb[SK][ST + 1];
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    const int n0 = blockIdx.x * ST, m0 = blockIdx.y * ST;
+    const int m0 = blockIdx.x * ST, n0 = blockIdx.y * ST;  // M-blocks on x (no 65535 limit)
     const int shard = p.sum_shards ? 0 : blockIdx.z;
     float acc[4][4] = {};
     const int n_k_shards = p.sum_shards ? p.n_shards : 1;
@@ -293,7 +293,12 @@ tpmlp_status launch_simt_gemm(const Operand& a, const Operand& b, const GemmSpec
     p.out2 = static_cast<float*>(g.out2); p.out2_ld = g.out2_ld; p.out2_ss = g.out2_ss;
     p.bias = static_cast<const float*>(g.bias); p.bias_ss = g.bias_ss;
     p.aux = static_cast<const float*>(g.aux); p.aux_ld = g.aux_ld; p.aux_ss = g.aux_ss;
-    dim3 grid((unsigned)((g.N + ST - 1) / ST), (unsigned)((g.M + ST - 1) / ST), (unsigned)(g.sum_shards ? 1 : g.n_shards));
+    const long long nb = (g.N + ST - 1) / ST, sh = g.sum_shards ? 1 : g.n_shards;
+    if (nb > 65535 || sh > 65535) {
+        set_error("fp32 GEMM: N/64 and the shard count must be at most 65535");
+        return TPMLP_ERR_SHAPE;
+    }
+    dim3 grid((unsigned)((g.M + ST - 1) / ST), (unsigned)nb, (unsigned)sh);
     simt_gemm_kernel<<<grid, 256, 0, st>>>(p);
     return check_launch("fp32 GEMM");
 }

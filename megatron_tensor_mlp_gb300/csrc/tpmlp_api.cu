@@ -93,6 +93,12 @@ tpmlp_status check_mlp_shape(int64_t s, int64_t b, int64_t h, int64_t ffn, int p
         set_error("shape too large: s*b, h and ffn must each be below 2^31");
         return TPMLP_ERR_SHAPE;
     }
+    // every tensor of the block (with the 2x SwiGLU and 4-byte gradient widths) below 2^40 bytes
+    const int64_t M = s * b, kMaxElems = (int64_t(1) << 40) / 16;
+    if ((M > 0 && ffn > kMaxElems / M) || (M > 0 && h > kMaxElems / M) || ffn > kMaxElems / h) {
+        set_error("shape too large: a tensor of the block would exceed 2^40 bytes");
+        return TPMLP_ERR_SHAPE;
+    }
     if (ffn % p != 0) {
         set_error("ffn=%lld is not divisible by p=%d", (long long)ffn, p);
         return TPMLP_ERR_DIVISIBILITY;
@@ -557,6 +563,10 @@ tpmlp_status tpmlp_swiglu_pack(void* G, void* U, void* W_sh, int64_t rows, int64
         set_error("bad shape rows=%lld ffn=%lld p=%d", (long long)rows, (long long)ffn, p);
         return TPMLP_ERR_SHAPE;
     }
+    if (rows > 0 && 2 * ffn > ((int64_t(1) << 40) / 4) / rows) {
+        set_error("shape too large: the packed matrix would exceed 2^40 bytes");
+        return TPMLP_ERR_SHAPE;
+    }
     if (ffn % p != 0 || (ffn / p) % 128 != 0) {
         set_error("SwiGLU packing needs ffn %% p == 0 and ffn/p a multiple of 128");
         return TPMLP_ERR_DIVISIBILITY;
@@ -580,6 +590,10 @@ static tpmlp_status shard_common(const void* src, void* dst, int64_t rows, int64
     }
     if (rows < 0 || cols < 1 || p < 1 || rows > kMaxDim || cols > kMaxDim) {
         set_error("bad shape rows=%lld cols=%lld p=%d", (long long)rows, (long long)cols, p);
+        return TPMLP_ERR_SHAPE;
+    }
+    if (rows > 0 && cols > ((int64_t(1) << 40) / 4) / rows) {
+        set_error("shape too large: the matrix would exceed 2^40 bytes");
         return TPMLP_ERR_SHAPE;
     }
     if (cols % p != 0) {
@@ -615,6 +629,10 @@ tpmlp_status tpmlp_qkv_interleave(const void* W_qkv, void* W_out, int64_t rows, 
     }
     if (rows < 0 || h < 1 || n_heads < 1 || p < 1 || rows > kMaxDim || h > kMaxDim / 3) {
         set_error("bad shape rows=%lld h=%lld n_heads=%lld p=%d", (long long)rows, (long long)h, (long long)n_heads, p);
+        return TPMLP_ERR_SHAPE;
+    }
+    if (rows > 0 && 3 * h > ((int64_t(1) << 40) / 4) / rows) {
+        set_error("shape too large: the matrix would exceed 2^40 bytes");
         return TPMLP_ERR_SHAPE;
     }
     if (h % n_heads != 0 || n_heads % p != 0) {

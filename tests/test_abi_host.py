@@ -47,6 +47,7 @@ def test_validation_order_and_codes():
     assert _fwd(s=-1) == T.ERR_SHAPE
     assert _fwd(p=0) == T.ERR_SHAPE
     assert _fwd(s=1 << 20, b=1 << 12) == T.ERR_SHAPE  # s*b >= 2^31
+    assert _fwd(s=1 << 20, b=1 << 10, h=1 << 20, ffn=1 << 20, p=1) == T.ERR_SHAPE  # tensors beyond 2^40 bytes
     assert _fwd(ffn=250, p=4) == T.ERR_DIVISIBILITY   # ffn % p
     assert _fwd(h=66, p=4, ffn=256) == T.ERR_DIVISIBILITY  # the block also needs h % p
     assert _fwd(dt=7) == T.ERR_DTYPE
@@ -78,6 +79,10 @@ def test_bwd_and_layout_validation():
     assert T.tpmlp_qkv_interleave(FAKE, FAKE + 0x100000, 4, 64, 6, 2, check=False) == T.ERR_DIVISIBILITY
     assert T.tpmlp_qkv_interleave(FAKE, FAKE + 0x100000, 4, 64, 8, 3, check=False) == T.ERR_DIVISIBILITY
     assert T.tpmlp_debug_wait_timeout(0, check=False) == T.ERR_SHAPE
+    assert T.tpmlp_shard_columns(FAKE, FAKE + 0x100000, 1 << 30, 1 << 20, 4, check=False) == T.ERR_SHAPE
+    assert T.tpmlp_qkv_interleave(FAKE, FAKE + 0x100000, 1 << 30, 1 << 20, 8, 2, check=False) == T.ERR_SHAPE
+    assert T.tpmlp_swiglu_pack(FAKE, FAKE + 0x100000, FAKE + 0x200000, 1 << 30, 1 << 20, 4, check=False) \
+        == T.ERR_SHAPE
 
 
 def test_gemm_mode_control():
