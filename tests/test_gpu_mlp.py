@@ -237,3 +237,27 @@ def test_tail_tiles_split_in_half(env, orc):
         _run_and_check(env, orc, wl)
     finally:
         T.tpmlp_set_gemm_tail_split(0)
+
+
+def _random_shapes(n, seed):
+    """Random (s, b, h, ffn, p) with h % p == 0, h % 8 == 0 and ffn/p % 8 == 0."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        p = int(rng.choice([1, 2, 3, 4, 5, 6, 8]))
+        step = 8 * p // int(np.gcd(8, p))          # lcm(8, p)
+        h = step * int(rng.integers(1, 600 // step + 1))
+        fs = 8 * int(rng.integers(1, 65))
+        s, b = int(rng.integers(1, 40)), int(rng.integers(1, 9))
+        if fs * p > 3000:
+            continue
+        out.append((s, b, h, fs * p, p))
+    return out
+
+
+@pytest.mark.parametrize("shape", _random_shapes(12, 2026), ids=lambda s: "s{}b{}h{}f{}p{}".format(*s))
+def test_random_shapes(env, orc, shape, gemm_mode):
+    """Random small shapes (token counts, widths and shard counts off every tile boundary)."""
+    _, synth, _ = env
+    wl = synth.custom(*shape, dtype="bf16", sigma_w=0.05, sigma_bias=0.05, seed=sum(shape) + 1)
+    _run_and_check(env, orc, wl)
