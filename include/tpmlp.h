@@ -293,6 +293,13 @@ int tpmlp_get_gemm_raster(void);
 tpmlp_status tpmlp_set_gemm_tail_split(int on);
 int tpmlp_get_gemm_tail_split(void);
 
+/*
+ * L2 eviction priority of the GEMMs' operand loads, process wide: 0 normal (default),
+ * 1 evict first, 2 evict last, for the A and B operands of every GEMM.  Affects speed only;
+ * other values TPMLP_ERR_SHAPE.
+ */
+tpmlp_status tpmlp_set_gemm_l2_hints(int a_priority, int b_priority);
+
 /* Human-readable name of a status code. */
 const char* tpmlp_status_string(tpmlp_status st);
 

@@ -56,6 +56,7 @@ bool make_map(CUtensorMap* map, const Operand& op, uint64_t inner, uint64_t oute
 
 std::atomic<int> g_gemm_mode{0};  // 0 automatic, 1 single-CTA tiles, 2 CTA-pair tiles
 std::atomic<int> g_group_m{16};  // M-blocks per raster group
+std::atomic<int> g_l2_a{0}, g_l2_b{0};  // L2 eviction priority of A / B loads
 std::atomic<int> g_tail_split{0};  // split the last partial wave of pair tiles in half
 
 template <typename Kern>
@@ -229,6 +230,8 @@ tpmlp_status launch_tc_gemm(const Operand& a, const Operand& b, const GemmSpec& 
     k.kb_per_shard = static_cast<int>((g.K + tc::BK - 1) / tc::BK);
     k.k_iters = g.sum_shards ? k.kb_per_shard * k.n_shards : k.kb_per_shard;
     k.group_m = g_group_m.load(std::memory_order_relaxed);
+    k.l2_a = g_l2_a.load(std::memory_order_relaxed);
+    k.l2_b = g_l2_b.load(std::memory_order_relaxed);
     k.act = g.act;
     k.out_f32 = g.out_f32 ? 1 : 0;
     k.out = g.out;
@@ -259,6 +262,14 @@ tpmlp_status launch_tc_gemm(const Operand& a, const Operand& b, const GemmSpec& 
 
 void set_gemm_mode(int mode) { g_gemm_mode.store(mode, std::memory_order_relaxed); }
 void set_group_m(int g) { g_group_m.store(g, std::memory_order_relaxed); }
+void set_l2_hints(int a, int b) {
+    g_l2_a.store(a, std::memory_order_relaxed);
+    g_l2_b.store(b, std::memory_order_relaxed);
+}
+void get_l2_hints(int* a, int* b) {
+    *a = g_l2_a.load(std::memory_order_relaxed);
+    *b = g_l2_b.load(std::memory_order_relaxed);
+}
 void set_tail_split(int on) { g_tail_split.store(on ? 1 : 0, std::memory_order_relaxed); }
 int get_tail_split() { return g_tail_split.load(std::memory_order_relaxed); }
 int get_group_m() { return g_group_m.load(std::memory_order_relaxed); }

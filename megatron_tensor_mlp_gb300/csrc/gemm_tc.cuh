@@ -62,6 +62,7 @@ struct KArgs {
     int act, out_f32;
     int a_chunked, b_chunked;  // MN-major operand loaded with one 4-D box per stage (MN extent % 64 == 0)
     int num_items, split_from;  // pair kernel: items >= split_from are half-width (256x128) tiles
+    int l2_a, l2_b;             // L2 eviction priority of the A / B loads (0 normal, 1 first, 2 last)
     void* out; long long out_ld, out_ss;
     void* out2; long long out2_ld, out2_ss;
     const void* bias; long long bias_ss;
@@ -412,6 +413,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t last_parity = 0;  // bit s: parity of the phase last armed on stage s
             bool ok = true;
             const int k_end = p.kb_per_shard * BK;
+            const uint64_t pol_a = l2_policy(p.l2_a), pol_b = l2_policy(p.l2_b);
             for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
                 int mb, nb, shard;
                 decode_tile(p, t, mb, nb, shard);
@@ -432,22 +434,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     uint8_t* a_dst = sA + stage * A_TILE_BYTES;
                     uint8_t* b_dst = sB + stage * B_TILE_BYTES;
                     if constexpr (!A_MN) {
-                        tma_load_3d(a_dst, &tmA, fb, k0, row0, sa);
+                        tma_load_3d(a_dst, &tmA, fb, k0, row0, sa, pol_a);
                     } else if (p.a_chunked) {
-                        tma_load_4d(a_dst, &tmA, fb, 0, k0, row0 / 64, sa);
+                        tma_load_4d(a_dst, &tmA, fb, 0, k0, row0 / 64, sa, pol_a);
                     } else {
 #pragma unroll
                         for (int c = 0; c < BM / 64; ++c)
-                            tma_load_3d(a_dst + c * MN_CHUNK_BYTES, &tmA, fb, row0 + c * 64, k0, sa);
+                            tma_load_3d(a_dst + c * MN_CHUNK_BYTES, &tmA, fb, row0 + c * 64, k0, sa, pol_a);
                     }
                     if constexpr (!B_MN) {
-                        tma_load_3d(b_dst, &tmB, fb, k0, col0, sb);
+                        tma_load_3d(b_dst, &tmB, fb, k0, col0, sb, pol_b);
                     } else if (p.b_chunked) {
-                        tma_load_4d(b_dst, &tmB, fb, 0, k0, col0 / 64, sb);
+                        tma_load_4d(b_dst, &tmB, fb, 0, k0, col0 / 64, sb, pol_b);
                     } else {
 #pragma unroll
                         for (int c = 0; c < BN / 64; ++c)
-                            tma_load_3d(b_dst + c * MN_CHUNK_BYTES, &tmB, fb, col0 + c * 64, k0, sb);
+                            tma_load_3d(b_dst + c * MN_CHUNK_BYTES, &tmB, fb, col0 + c * 64, k0, sb, pol_b);
                     }
                     if (++stage == STAGES) {
                         stage = 0;
@@ -650,6 +652,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t armed = 0, last_parity = 0;
             bool ok = true;
             const int k_end = p.kb_per_shard * BK;
+            const uint64_t pol_a = l2_policy(p.l2_a), pol_b = l2_policy(p.l2_b);
             const uint32_t full_leader0 = mapa_shared(smem_u32(full), 0);  // the leader's barriers
             for (int t = cluster_id; t < p.num_items && ok; t += n_clusters) {
                 int mb, nb, shard, n0;
@@ -677,22 +680,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     uint8_t* a_dst = sA + stage * P_A_BYTES;
                     uint8_t* b_dst = sB + stage * P_B_BYTES;
                     if constexpr (!A_MN) {
-                        tma_load_3d_pair(a_dst, &tmA, bar, k0, row0, sa);
+                        tma_load_3d_pair(a_dst, &tmA, bar, k0, row0, sa, pol_a);
                     } else if (p.a_chunked) {
-                        tma_load_4d_pair(a_dst, &tmA, bar, 0, k0, row0 / 64, sa);
+                        tma_load_4d_pair(a_dst, &tmA, bar, 0, k0, row0 / 64, sa, pol_a);
                     } else {
 #pragma unroll
                         for (int c = 0; c < BM / 64; ++c)
-                            tma_load_3d_pair(a_dst + c * MN_CHUNK_BYTES, &tmA, bar, row0 + c * 64, k0, sa);
+                            tma_load_3d_pair(a_dst + c * MN_CHUNK_BYTES, &tmA, bar, row0 + c * 64, k0, sa, pol_a);
                     }
                     if constexpr (!B_MN) {
-                        tma_load_3d_pair(b_dst, mapB, bar, k0, col0, sb);
+                        tma_load_3d_pair(b_dst, mapB, bar, k0, col0, sb, pol_b);
                     } else if (p.b_chunked) {
-                        tma_load_4d_pair(b_dst, mapB, bar, 0, k0, col0 / 64, sb);
+                        tma_load_4d_pair(b_dst, mapB, bar, 0, k0, col0 / 64, sb, pol_b);
                     } else {
                         // 64-wide boxes of the un-chunked map; a half tile needs one of them
-                        tma_load_3d_pair(b_dst, &tmB, bar, col0, k0, sb);
-                        if (full_tile) tma_load_3d_pair(b_dst + MN_CHUNK_BYTES, &tmB, bar, col0 + 64, k0, sb);
+                        tma_load_3d_pair(b_dst, &tmB, bar, col0, k0, sb, pol_b);
+                        if (full_tile) tma_load_3d_pair(b_dst + MN_CHUNK_BYTES, &tmB, bar, col0 + 64, k0, sb, pol_b);
                     }
                     if (++stage == P_STAGES) {
                         stage = 0;

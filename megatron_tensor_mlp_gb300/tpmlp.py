@@ -50,6 +50,7 @@ _SIGS = {
     "tpmlp_set_gemm_mode": [_i32],
     "tpmlp_set_gemm_raster": [_i32],
     "tpmlp_set_gemm_tail_split": [_i32],
+    "tpmlp_set_gemm_l2_hints": [_i32, _i32],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(lib, _name)
@@ -226,6 +227,10 @@ def tpmlp_get_gemm_raster() -> int:
 
 def tpmlp_set_gemm_tail_split(on, check=True):
     return _done(lib.tpmlp_set_gemm_tail_split(int(on)), check)
+
+
+def tpmlp_set_gemm_l2_hints(a_priority, b_priority, check=True):
+    return _done(lib.tpmlp_set_gemm_l2_hints(a_priority, b_priority), check)
 
 
 def tpmlp_get_gemm_tail_split() -> int:
