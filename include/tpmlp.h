@@ -285,21 +285,6 @@ int tpmlp_get_gemm_mode(void);
 tpmlp_status tpmlp_set_gemm_raster(int group_m);
 int tpmlp_get_gemm_raster(void);
 
-/*
- * Tail of the CTA-pair tilings, process wide: 1 runs the tiles of a last wave that fills at
- * most half of the co-resident pairs as two 256x128 halves each, so that the tail costs half a
- * wave; 0 (default) keeps whole tiles.  Affects speed only; other values TPMLP_ERR_SHAPE.
- */
-tpmlp_status tpmlp_set_gemm_tail_split(int on);
-int tpmlp_get_gemm_tail_split(void);
-
-/*
- * L2 eviction priority of the GEMMs' operand loads, process wide: 0 normal (default),
- * 1 evict first, 2 evict last, for the A and B operands of every GEMM.  Affects speed only;
- * other values TPMLP_ERR_SHAPE.
- */
-tpmlp_status tpmlp_set_gemm_l2_hints(int a_priority, int b_priority);
-
 /* Human-readable name of a status code. */
 const char* tpmlp_status_string(tpmlp_status st);
 

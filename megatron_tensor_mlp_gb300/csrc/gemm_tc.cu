@@ -56,8 +56,6 @@ bool make_map(CUtensorMap* map, const Operand& op, uint64_t inner, uint64_t oute
 
 std::atomic<int> g_gemm_mode{0};  // 0 automatic, 1 single-CTA tiles, 2 CTA-pair tiles
 std::atomic<int> g_group_m{16};  // M-blocks per raster group
-std::atomic<int> g_l2_a{0}, g_l2_b{0};  // L2 eviction priority of A / B loads
-std::atomic<int> g_tail_split{0};  // split the last partial wave of pair tiles in half
 
 template <typename Kern>
 bool set_smem_attr(Kern kern, int device, int bytes, bool* done) {
@@ -145,8 +143,8 @@ int pair_capacity(const DeviceInfo& dev) {
 }
 
 template <bool A_MN, bool B_MN, int EPI>
-tpmlp_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mb_half,
-                         const tc::KArgs& k, int clusters, cudaStream_t st) {
+tpmlp_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const tc::KArgs& k, int clusters,
+                         cudaStream_t st) {
     auto kern = tc::gemm_pair_kernel<A_MN, B_MN, EPI>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
@@ -160,7 +158,7 @@ tpmlp_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mb_half, k);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, k);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("tcgen05 CTA-pair GEMM launch: %s", cudaGetErrorString(e));
@@ -194,21 +192,8 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
     if (!use_pair) return launch_single<A_MN, B_MN, EPI>(ma, mb, k, dev, st);
     k.m_blocks = m_pairs;
     k.num_tiles = pair_tiles;
-    // Tail: when the last wave fills at most half of the pairs, its tiles run as two
-    // 256x128 halves each, so the tail costs half a wave.  (Not for the packed SwiGLU
-    // forward, whose 256-wide tiles hold gate and up together.)
-    const int rem = pair_tiles % cap;
-    const bool split = g_tail_split.load(std::memory_order_relaxed) != 0 && EPI != EPI_SWIGLU && rem > 0 && 2 * rem <= cap;
-    k.split_from = split ? pair_tiles - rem : pair_tiles;
-    k.num_items = split ? pair_tiles + rem : pair_tiles;
-    CUtensorMap mb_half = mb;
-    if (split && !(b.mn_major && !k.b_chunked)) {
-        ok = b.mn_major ? make_map_chunked(&mb_half, b, g.N, g.K, (tc::BN / 4) / 64)
-                        : make_map(&mb_half, b, g.K, g.N, tc::BK, tc::BN / 4);
-        if (!ok) return TPMLP_ERR_CUDA;
-    }
-    const int clusters = k.num_items < cap ? k.num_items : cap;
-    return launch_pair<A_MN, B_MN, EPI>(ma, mb, mb_half, k, clusters, st);
+    const int clusters = pair_tiles < cap ? pair_tiles : cap;
+    return launch_pair<A_MN, B_MN, EPI>(ma, mb, k, clusters, st);
 }
 
 }  // namespace
@@ -230,8 +215,6 @@ tpmlp_status launch_tc_gemm(const Operand& a, const Operand& b, const GemmSpec& 
     k.kb_per_shard = static_cast<int>((g.K + tc::BK - 1) / tc::BK);
     k.k_iters = g.sum_shards ? k.kb_per_shard * k.n_shards : k.kb_per_shard;
     k.group_m = g_group_m.load(std::memory_order_relaxed);
-    k.l2_a = g_l2_a.load(std::memory_order_relaxed);
-    k.l2_b = g_l2_b.load(std::memory_order_relaxed);
     k.act = g.act;
     k.out_f32 = g.out_f32 ? 1 : 0;
     k.out = g.out;
@@ -262,16 +245,6 @@ tpmlp_status launch_tc_gemm(const Operand& a, const Operand& b, const GemmSpec& 
 
 void set_gemm_mode(int mode) { g_gemm_mode.store(mode, std::memory_order_relaxed); }
 void set_group_m(int g) { g_group_m.store(g, std::memory_order_relaxed); }
-void set_l2_hints(int a, int b) {
-    g_l2_a.store(a, std::memory_order_relaxed);
-    g_l2_b.store(b, std::memory_order_relaxed);
-}
-void get_l2_hints(int* a, int* b) {
-    *a = g_l2_a.load(std::memory_order_relaxed);
-    *b = g_l2_b.load(std::memory_order_relaxed);
-}
-void set_tail_split(int on) { g_tail_split.store(on ? 1 : 0, std::memory_order_relaxed); }
-int get_tail_split() { return g_tail_split.load(std::memory_order_relaxed); }
 int get_group_m() { return g_group_m.load(std::memory_order_relaxed); }
 int get_gemm_mode() { return g_gemm_mode.load(std::memory_order_relaxed); }
 

@@ -61,8 +61,6 @@ struct KArgs {
     int m_blocks, n_blocks, batch, num_tiles, kb_per_shard, k_iters, group_m;
     int act, out_f32;
     int a_chunked, b_chunked;  // MN-major operand loaded with one 4-D box per stage (MN extent % 64 == 0)
-    int num_items, split_from;  // pair kernel: items >= split_from are half-width (256x128) tiles
-    int l2_a, l2_b;             // L2 eviction priority of the A / B loads (0 normal, 1 first, 2 last)
     void* out; long long out_ld, out_ss;
     void* out2; long long out2_ld, out2_ss;
     const void* bias; long long bias_ss;
@@ -331,14 +329,10 @@ __device__ __forceinline__ void dswiglu_chunk(const KArgs& p, const uint32_t (&r
     store_bf16x32(op + 128, du, 32);
 }
 
-// One tile's epilogue for this warp: TMEM lane quarter of the caller, `nchunks` chunks of 32
-// accumulator columns starting at col_base; output column = n_base + accumulator column.
+// One tile's epilogue for this warp: TMEM lane quarter q, column half `half`.
 template <int EPI>
-__device__ __forceinline__ void epilogue_tile(const KArgs& p, uint32_t t_row, int gm, int n_base, int col_base,
-                                              int nchunks, int shard) {
+__device__ __forceinline__ void epilogue_tile(const KArgs& p, uint32_t t_row, int gm, int nb, int half, int shard) {
     if constexpr (EPI == EPI_SWIGLU) {
-        // whole tiles only: [gate 128 | up 128] of features n_base/2 .. n_base/2 + 127
-        const int half = col_base >> 7;
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
             const int fo = half * 64 + c * 32;
@@ -346,17 +340,17 @@ __device__ __forceinline__ void epilogue_tile(const KArgs& p, uint32_t t_row, in
             tmem_ld_32x32b_x32(t_row + fo, rg);
             tmem_ld_32x32b_x32(t_row + 128 + fo, ru);
             tmem_ld_wait();
-            swiglu_chunk(p, rg, ru, gm, n_base / BN, fo, shard);
+            swiglu_chunk(p, rg, ru, gm, nb, fo, shard);
         }
     } else {
 #pragma unroll 1
-        for (int c = 0; c < nchunks; ++c) {
-            const int col = col_base + c * 32;
+        for (int c = 0; c < 4; ++c) {
+            const int col = half * 128 + c * 32;
             uint32_t r[32];
             tmem_ld_32x32b_x32(t_row + col, r);
             tmem_ld_wait();
-            if constexpr (EPI == EPI_DSWIGLU) dswiglu_chunk(p, r, gm, n_base + col, shard);
-            else epilogue_chunk<EPI>(p, r, gm, n_base + col, shard);
+            if constexpr (EPI == EPI_DSWIGLU) dswiglu_chunk(p, r, gm, nb * BN + col, shard);
+            else epilogue_chunk<EPI>(p, r, gm, nb * BN + col, shard);
         }
     }
 }
@@ -413,7 +407,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t last_parity = 0;  // bit s: parity of the phase last armed on stage s
             bool ok = true;
             const int k_end = p.kb_per_shard * BK;
-            const uint64_t pol_a = l2_policy(p.l2_a), pol_b = l2_policy(p.l2_b);
             for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
                 int mb, nb, shard;
                 decode_tile(p, t, mb, nb, shard);
@@ -434,22 +427,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     uint8_t* a_dst = sA + stage * A_TILE_BYTES;
                     uint8_t* b_dst = sB + stage * B_TILE_BYTES;
                     if constexpr (!A_MN) {
-                        tma_load_3d(a_dst, &tmA, fb, k0, row0, sa, pol_a);
+                        tma_load_3d(a_dst, &tmA, fb, k0, row0, sa);
                     } else if (p.a_chunked) {
-                        tma_load_4d(a_dst, &tmA, fb, 0, k0, row0 / 64, sa, pol_a);
+                        tma_load_4d(a_dst, &tmA, fb, 0, k0, row0 / 64, sa);
                     } else {
 #pragma unroll
                         for (int c = 0; c < BM / 64; ++c)
-                            tma_load_3d(a_dst + c * MN_CHUNK_BYTES, &tmA, fb, row0 + c * 64, k0, sa, pol_a);
+                            tma_load_3d(a_dst + c * MN_CHUNK_BYTES, &tmA, fb, row0 + c * 64, k0, sa);
                     }
                     if constexpr (!B_MN) {
-                        tma_load_3d(b_dst, &tmB, fb, k0, col0, sb, pol_b);
+                        tma_load_3d(b_dst, &tmB, fb, k0, col0, sb);
                     } else if (p.b_chunked) {
-                        tma_load_4d(b_dst, &tmB, fb, 0, k0, col0 / 64, sb, pol_b);
+                        tma_load_4d(b_dst, &tmB, fb, 0, k0, col0 / 64, sb);
                     } else {
 #pragma unroll
                         for (int c = 0; c < BN / 64; ++c)
-                            tma_load_3d(b_dst + c * MN_CHUNK_BYTES, &tmB, fb, col0 + c * 64, k0, sb, pol_b);
+                            tma_load_3d(b_dst + c * MN_CHUNK_BYTES, &tmB, fb, col0 + c * 64, k0, sb);
                     }
                     if (++stage == STAGES) {
                         stage = 0;
@@ -535,7 +528,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             decode_tile(p, t, mb, nb, shard);
             const int gm = mb * BM + q * 32 + lane;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-            epilogue_tile<EPI>(p, t_row, gm, nb * BN, half * 128, 4, shard);
+            epilogue_tile<EPI>(p, t_row, gm, nb, half, shard);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty + acc);
@@ -578,26 +571,10 @@ constexpr int P_B_BYTES = (BN / 2) * BK * 2;  // 16 KiB: this CTA's 128 columns 
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + BAR_BYTES;
 
-// Work item t of the pair kernel: a whole 256x256 tile (t < split_from) or one half
-// (256x128) of tile split_from + (t - split_from) / 2.  n0 = first output column, full = width 256.
-// Returns false for a half item that lies entirely beyond N (all roles skip it).
-__device__ __forceinline__ bool decode_item(const KArgs& p, int t, int& mb, int& nb, int& shard, int& n0, bool& full) {
-    int tile = t, sub = 0;
-    full = t < p.split_from;
-    if (!full) {
-        const int u = t - p.split_from;
-        tile = p.split_from + (u >> 1);
-        sub = u & 1;
-    }
-    decode_tile(p, tile, mb, nb, shard);
-    n0 = nb * BN + sub * (BN / 2);
-    return n0 < p.N;
-}
-
 template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmB_half, const KArgs p) {
+                     const KArgs p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
@@ -632,7 +609,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        if (p.split_from < p.num_items) tma_prefetch_desc(&tmB_half);
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, TMEM_COLS);
@@ -652,17 +628,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t armed = 0, last_parity = 0;
             bool ok = true;
             const int k_end = p.kb_per_shard * BK;
-            const uint64_t pol_a = l2_policy(p.l2_a), pol_b = l2_policy(p.l2_b);
             const uint32_t full_leader0 = mapa_shared(smem_u32(full), 0);  // the leader's barriers
-            for (int t = cluster_id; t < p.num_items && ok; t += n_clusters) {
-                int mb, nb, shard, n0;
-                bool full_tile;
-                if (!decode_item(p, t, mb, nb, shard, n0, full_tile)) continue;
+            for (int t = cluster_id; t < p.num_tiles && ok; t += n_clusters) {
+                int mb, nb, shard;
+                decode_tile(p, t, mb, nb, shard);
                 const int row0 = mb * (2 * BM) + static_cast<int>(rank) * BM;
-                // this CTA's share of the item's columns: 128 of a whole tile, 64 of a half tile
-                const int col0 = n0 + static_cast<int>(rank) * (full_tile ? BN / 2 : BN / 4);
-                const uint32_t stage_tx = full_tile ? 2 * P_STAGE_BYTES : 2 * (P_A_BYTES + P_B_BYTES / 2);
-                const CUtensorMap* mapB = full_tile ? &tmB : &tmB_half;
+                const int col0 = nb * BN + static_cast<int>(rank) * (BN / 2);
                 int sa = p.sum_shards ? 0 : (p.a_batched ? shard : 0);
                 int sb = p.sum_shards ? 0 : (p.b_batched ? shard : 0);
                 int k0 = 0;
@@ -672,7 +643,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     if (leader) {
-                        mbar_arrive_expect_tx(full + stage, stage_tx);
+                        mbar_arrive_expect_tx(full + stage, 2 * P_STAGE_BYTES);
                         armed |= 1u << stage;
                         last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                     }
@@ -680,22 +651,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     uint8_t* a_dst = sA + stage * P_A_BYTES;
                     uint8_t* b_dst = sB + stage * P_B_BYTES;
                     if constexpr (!A_MN) {
-                        tma_load_3d_pair(a_dst, &tmA, bar, k0, row0, sa, pol_a);
+                        tma_load_3d_pair(a_dst, &tmA, bar, k0, row0, sa);
                     } else if (p.a_chunked) {
-                        tma_load_4d_pair(a_dst, &tmA, bar, 0, k0, row0 / 64, sa, pol_a);
+                        tma_load_4d_pair(a_dst, &tmA, bar, 0, k0, row0 / 64, sa);
                     } else {
 #pragma unroll
                         for (int c = 0; c < BM / 64; ++c)
-                            tma_load_3d_pair(a_dst + c * MN_CHUNK_BYTES, &tmA, bar, row0 + c * 64, k0, sa, pol_a);
+                            tma_load_3d_pair(a_dst + c * MN_CHUNK_BYTES, &tmA, bar, row0 + c * 64, k0, sa);
                     }
                     if constexpr (!B_MN) {
-                        tma_load_3d_pair(b_dst, mapB, bar, k0, col0, sb, pol_b);
+                        tma_load_3d_pair(b_dst, &tmB, bar, k0, col0, sb);
                     } else if (p.b_chunked) {
-                        tma_load_4d_pair(b_dst, mapB, bar, 0, k0, col0 / 64, sb, pol_b);
+                        tma_load_4d_pair(b_dst, &tmB, bar, 0, k0, col0 / 64, sb);
                     } else {
-                        // 64-wide boxes of the un-chunked map; a half tile needs one of them
-                        tma_load_3d_pair(b_dst, &tmB, bar, col0, k0, sb, pol_b);
-                        if (full_tile) tma_load_3d_pair(b_dst + MN_CHUNK_BYTES, &tmB, bar, col0 + 64, k0, sb, pol_b);
+#pragma unroll
+                        for (int c = 0; c < (BN / 2) / 64; ++c)
+                            tma_load_3d_pair(b_dst + c * MN_CHUNK_BYTES, &tmB, bar, col0 + c * 64, k0, sb);
                     }
                     if (++stage == P_STAGES) {
                         stage = 0;
@@ -725,8 +696,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             if (leader) {
                 // -------------------------------------------------------- UMMA issuer (leader)
-                constexpr uint32_t idesc_full = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
-                constexpr uint32_t idesc_half = idesc_bf16_f32(2 * BM, BN / 2, A_MN, B_MN);
+                constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
                 const uint64_t a_desc0 = A_MN ? sdesc_sw128(smem_u32(sA), TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES)
                                               : sdesc_sw128(smem_u32(sA), 16, 1024);
                 const uint64_t b_desc0 = B_MN ? sdesc_sw128(smem_u32(sB), TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES)
@@ -737,14 +707,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 uint32_t phase = 0;
                 int lt = 0;
                 bool ok = true;
-                for (int t = cluster_id; t < p.num_items && ok; t += n_clusters) {
-                    int mb, nb, shard, n0;
-                    bool full_tile;
-                    if (!decode_item(p, t, mb, nb, shard, n0, full_tile)) continue;
-                    const uint32_t idesc = full_tile ? idesc_full : idesc_half;
+                for (int t = cluster_id; t < p.num_tiles && ok; t += n_clusters, ++lt) {
                     const int acc = lt & 1;
                     const uint32_t acc_phase = (lt >> 1) & 1;
-                    ++lt;
                     if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, p.status, p.timeout_ns, kWhereMma)) {
                         ok = false;
                         break;
@@ -782,23 +747,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int half = (warp - FIRST_EPI_WARP) >> 2;
         const uint32_t tempty_leader0 = mapa_shared(smem_u32(tempty), 0);
         int lt = 0;
-        for (int t = cluster_id; t < p.num_items; t += n_clusters) {
-            int mb, nb, shard, n0;
-            bool full_tile;
-            if (!decode_item(p, t, mb, nb, shard, n0, full_tile)) continue;
+        for (int t = cluster_id; t < p.num_tiles; t += n_clusters, ++lt) {
             const int acc = lt & 1;
             const uint32_t acc_phase = (lt >> 1) & 1;
-            ++lt;
             int okw = 0;
             if (lane == 0) okw = mbar_wait_bounded(tfull + acc, acc_phase, p.status, p.timeout_ns, kWhereEpilogue);
             okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
             if (!okw) break;
             tc_fence_after();
+            int mb, nb, shard;
+            decode_tile(p, t, mb, nb, shard);
             const int gm = mb * (2 * BM) + static_cast<int>(rank) * BM + q * 32 + lane;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-            // a whole tile: 128 columns per warp; a half tile: 64
-            if (full_tile) epilogue_tile<EPI>(p, t_row, gm, n0, half * 128, 4, shard);
-            else epilogue_tile<EPI>(p, t_row, gm, n0, half * 64, 2, shard);
+            epilogue_tile<EPI>(p, t_row, gm, nb, half, shard);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader0 + acc * 8);

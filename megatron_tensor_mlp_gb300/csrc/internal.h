@@ -79,9 +79,6 @@ void set_gemm_mode(int mode);
 int get_gemm_mode();
 void set_group_m(int g);
 int get_group_m();
-void set_l2_hints(int a, int b);
-void get_l2_hints(int* a, int* b);
-void set_tail_split(int on);
-int get_tail_split();
+
 
 }  // namespace tpmlp

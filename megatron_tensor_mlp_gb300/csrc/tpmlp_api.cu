@@ -738,24 +738,4 @@ tpmlp_status tpmlp_set_gemm_raster(int group_m) {
 
 int tpmlp_get_gemm_raster(void) { return get_group_m(); }
 
-tpmlp_status tpmlp_set_gemm_tail_split(int on) {
-    if (on != 0 && on != 1) {
-        set_error("tail split must be 0 or 1");
-        return TPMLP_ERR_SHAPE;
-    }
-    set_tail_split(on);
-    return TPMLP_OK;
-}
-
-int tpmlp_get_gemm_tail_split(void) { return get_tail_split(); }
-
-tpmlp_status tpmlp_set_gemm_l2_hints(int a_priority, int b_priority) {
-    if (a_priority < 0 || a_priority > 2 || b_priority < 0 || b_priority > 2) {
-        set_error("L2 priorities must be 0 (normal), 1 (evict first) or 2 (evict last)");
-        return TPMLP_ERR_SHAPE;
-    }
-    set_l2_hints(a_priority, b_priority);
-    return TPMLP_OK;
-}
-
 }  // extern "C"

@@ -49,8 +49,7 @@ _SIGS = {
     "tpmlp_debug_wait_timeout": [_u32, _vp],
     "tpmlp_set_gemm_mode": [_i32],
     "tpmlp_set_gemm_raster": [_i32],
-    "tpmlp_set_gemm_tail_split": [_i32],
-    "tpmlp_set_gemm_l2_hints": [_i32, _i32],
+
 }
 for _name, _args in _SIGS.items():
     _f = getattr(lib, _name)
@@ -62,8 +61,6 @@ lib.tpmlp_status_string.argtypes = [ctypes.c_int]
 lib.tpmlp_status_string.restype = ctypes.c_char_p
 lib.tpmlp_last_error.argtypes = []
 lib.tpmlp_last_error.restype = ctypes.c_char_p
-lib.tpmlp_get_gemm_tail_split.argtypes = []
-lib.tpmlp_get_gemm_tail_split.restype = ctypes.c_int
 lib.tpmlp_get_gemm_raster.argtypes = []
 lib.tpmlp_get_gemm_raster.restype = ctypes.c_int
 lib.tpmlp_get_gemm_mode.argtypes = []
@@ -223,18 +220,6 @@ def tpmlp_set_gemm_raster(group_m, check=True):
 
 def tpmlp_get_gemm_raster() -> int:
     return int(lib.tpmlp_get_gemm_raster())
-
-
-def tpmlp_set_gemm_tail_split(on, check=True):
-    return _done(lib.tpmlp_set_gemm_tail_split(int(on)), check)
-
-
-def tpmlp_set_gemm_l2_hints(a_priority, b_priority, check=True):
-    return _done(lib.tpmlp_set_gemm_l2_hints(a_priority, b_priority), check)
-
-
-def tpmlp_get_gemm_tail_split() -> int:
-    return int(lib.tpmlp_get_gemm_tail_split())
 
 
 def tpmlp_status_string(st: int) -> str:

@@ -17,16 +17,13 @@ def env():
     return harness, synth, tpmlp
 
 
-@pytest.fixture(params=[(1, 0), (2, 0), (2, 1)], ids=["single-cta", "cta-pair", "cta-pair-split-tail"])
+@pytest.fixture(params=[1, 2], ids=["single-cta", "cta-pair"])
 def gemm_mode(request, env):
-    """Force 128x256 single-CTA tiles, or 256x256 CTA-pair tiles with whole or split tail tiles."""
+    """Force 128x256 single-CTA tiles or 256x256 CTA-pair tiles for the test."""
     T = env[2]
-    mode, split = request.param
-    T.tpmlp_set_gemm_mode(mode)
-    T.tpmlp_set_gemm_tail_split(split)
-    yield mode
+    T.tpmlp_set_gemm_mode(request.param)
+    yield request.param
     T.tpmlp_set_gemm_mode(0)
-    T.tpmlp_set_gemm_tail_split(0)
 
 
 # (s, b, h, ffn, p): tiles are 128 (tokens) x 256 (outputs) x 64 (reduction)
@@ -227,16 +224,12 @@ def test_single_and_pair_tiles_agree(env, orc):
         assert torch.equal(a, b_)
 
 
-def test_tail_tiles_split_in_half(env, orc):
-    """A shape whose row and dX GEMMs have 80 pair tiles (76 pairs fit at once): the last 4
-    tiles run as 256x128 halves, and the weight-gradient GEMMs split every tile."""
-    _, synth, T = env
+def test_mixed_wave_shape(env, orc):
+    """A shape whose row and dX GEMMs have 80 pair tiles (76 pairs fit at once), so the
+    last wave holds 4 tiles; the weight-gradient GEMMs have fewer tiles than pairs."""
+    _, synth, _ = env
     wl = synth.custom(320, 8, 2048, 1024, 2, dtype="bf16", sigma_w=0.03, sigma_bias=0.05, seed=77)
-    T.tpmlp_set_gemm_tail_split(1)
-    try:
-        _run_and_check(env, orc, wl)
-    finally:
-        T.tpmlp_set_gemm_tail_split(0)
+    _run_and_check(env, orc, wl)
 
 
 def _random_shapes(n, seed):
