@@ -61,6 +61,20 @@ __device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
     return v;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not yet complete
+// sleeps in hardware (up to hint_ns) instead of re-polling the barrier.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait on the phase with the given parity.  Gives up when the time
 // limit passes (records kStatusTimeout|where) or when another thread has
 // already recorded a status (abort propagation).  Returns true on success.
@@ -70,8 +84,8 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = globaltimer_ns();
     for (uint32_t spin = 1;; ++spin) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((spin & 255u) == 0) {
+        if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+        if ((spin & 7u) == 0) {
             if (watch_status && ld_volatile_u32(status) != 0u) return false;
             if (globaltimer_ns() - t0 > timeout_ns) {
                 atomicCAS(status, 0u, kStatusTimeout | where);
