@@ -629,14 +629,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             const int k_end = p.kb_per_shard * BK;
             const uint32_t full_leader0 = mapa_shared(smem_u32(full), 0);  // the leader's barriers
-            for (int t = cluster_id; t < p.num_tiles && ok; t += n_clusters) {
+            int lt = 0;
+            for (int t = cluster_id; t < p.num_tiles && ok; t += n_clusters, ++lt) {
                 int mb, nb, shard;
                 decode_tile(p, t, mb, nb, shard);
                 const int row0 = mb * (2 * BM) + static_cast<int>(rank) * BM;
                 const int col0 = nb * BN + static_cast<int>(rank) * (BN / 2);
-                int sa = p.sum_shards ? 0 : (p.a_batched ? shard : 0);
-                int sb = p.sum_shards ? 0 : (p.b_batched ? shard : 0);
-                int k0 = 0;
+                // Odd waves walk K backwards: a tile of the next wave usually shares its
+                // A (or B) panel with a tile of this one, and starts on the K range that
+                // this wave read last and the L2 still holds.  (Each tile's accumulation
+                // order is fixed by its index, so results stay deterministic.)
+                const bool rev = (lt & 1) != 0;
+                int sa = p.sum_shards ? (rev ? p.n_shards - 1 : 0) : (p.a_batched ? shard : 0);
+                int sb = p.sum_shards ? (rev ? p.n_shards - 1 : 0) : (p.b_batched ? shard : 0);
+                int k0 = rev ? k_end - BK : 0;
                 for (int it = 0; it < p.k_iters; ++it) {
                     if (!mbar_wait_bounded(empty + stage, phase ^ 1u, p.status, p.timeout_ns, kWhereProducer)) {
                         ok = false;
@@ -672,11 +678,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         stage = 0;
                         phase ^= 1u;
                     }
-                    k0 += BK;
-                    if (k0 == k_end) {
-                        k0 = 0;
-                        ++sa;
-                        ++sb;
+                    if (!rev) {
+                        k0 += BK;
+                        if (k0 == k_end) {
+                            k0 = 0;
+                            ++sa;
+                            ++sb;
+                        }
+                    } else {
+                        k0 -= BK;
+                        if (k0 < 0) {
+                            k0 = k_end - BK;
+                            --sa;
+                            --sb;
+                        }
                     }
                 }
             }
