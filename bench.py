@@ -18,6 +18,7 @@ slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -30,6 +31,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "TP-MLP fwd/bwd TFLOP/s & tokens/s on 1 GB300; % of dense BF16 tensor peak"
 NOMINAL_BF16_TFLOPS = 2250.0
+WARMUP_SECONDS = 2.0  # default warm-up of the GPU arm (see run_gpu)
 MAIN_WORKLOAD = 5      # fwd + bwd
 FWD_WORKLOAD = 4       # forward at the pages' sizing
 
@@ -38,13 +40,14 @@ def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=None,
+                    help="untimed warm-up steps (default: steps for about %.0f s, so that the timed region runs at the steady clock the power cap settles to)" % WARMUP_SECONDS)
     ap.add_argument("--impl", default="tpmlp", choices=["tpmlp", "reference"])
     ap.add_argument("--workload", type=int, default=MAIN_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fwd-pages", action="store_true")
     ap.add_argument("--no-next-rows", action="store_true", help="skip the SwiGLU / attention-projection timings")
-    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--e2e-steps", type=int, default=60)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     return ap.parse_args()
 
@@ -110,25 +113,42 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples while the timed region runs."""
+    """nvidia-smi clock / power / throttle samples; only those stamped inside the
+    timed window (mark_start .. mark_end) are summarised."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
         self.path = f"/tmp/tpmlp_clocks_{os.getpid()}.csv"
+        self.t0 = self.t1 = None
+        power = "power.draw.instant"
+        try:  # older drivers lack the instantaneous reading
+            r = subprocess.run(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={power}",
+                                "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=20)
+            if r.returncode != 0:
+                power = "power.draw"
+        except (OSError, subprocess.SubprocessError):
+            power = "power.draw"
+        self.fields = ("timestamp,clocks.sm,clocks.max.sm," + power + ",clocks_event_reasons.active,"
+                       "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                       "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def start(self):
         try:
             self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.fields}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+
+    def mark_start(self):
+        self.t0 = datetime.datetime.now()
+
+    def mark_end(self):
+        self.t1 = datetime.datetime.now()
 
     def stop(self):
         if self.proc is None:
@@ -139,25 +159,26 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        sm, mx, reasons, power = [], [], set(), []
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-                power.append(float(f[3]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
+                rows.append((ts, float(f[1]), float(f[2]), float(f[3]), f[5:9]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm),
-                "power_w_median": statistics.median(power) if power else None}
+        inside = [r for r in rows if self.t0 is not None and self.t1 is not None and self.t0 <= r[0] <= self.t1]
+        window = "timed region"
+        if len(inside) < 3:  # a very short timed region: fall back to every sample
+            inside, window = rows, "whole run"
+        reasons = sorted({n for r in inside for n, v in zip(self.REASONS, r[4]) if v.lower() == "active"})
+        med = lambda xs: statistics.median(xs) if xs else None  # noqa: E731
+        return {"sm_mhz": med([r[1] for r in inside]), "sm_max_mhz": max((r[2] for r in inside), default=None),
+                "reasons": reasons, "samples": len(inside), "window": window,
+                "power_w_median": med([r[3] for r in inside])}
 
 
 # --------------------------------------------------------------------------- CPU (oracle) arm
@@ -215,6 +236,8 @@ def run_reference(args):
 
     wl = synth.WORKLOADS[args.workload]
     sample = OracleSample(wl)
+    if args.warmup is None:
+        args.warmup = 3
     per_step = min(30.0, 150.0 / max(1, args.steps + args.warmup))  # whole run within a few minutes
     tokens, _ = sample.calibrate(per_step)
     times = []
@@ -344,8 +367,22 @@ def run_gpu(args):
             buf.bwd(stream=stream)
 
     launches_per_step = 2 + (6 if wl.backward else 0)
-    for _ in range(max(3, args.warmup)):
-        step()
+    sampler = ClockSampler(local)
+    sampler.start()
+    # Warm-up: the board's power controller allows a higher clock for the first second
+    # or so of load and then settles; by default warm up for WARMUP_SECONDS so that the
+    # timed region (and the sustained cuBLAS rate it is compared with) sees the settled clock.
+    if args.warmup is None:
+        n_warm, t_w = 0, time.time()
+        while n_warm < 5 or time.time() - t_w < WARMUP_SECONDS:
+            for _ in range(5):
+                step()
+            n_warm += 5
+            torch.cuda.synchronize()
+    else:
+        n_warm = max(3, args.warmup)
+        for _ in range(n_warm):
+            step()
     torch.cuda.synchronize()
     T.tpmlp_device_status()
 
@@ -357,13 +394,11 @@ def run_gpu(args):
     # timed region: per-call events on the launching stream
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
     barrier()
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    sampler.mark_start()
     t_start.record(stream)
     for i in range(K):
         e = ev[i]
@@ -377,6 +412,7 @@ def run_gpu(args):
         e[3].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
+    sampler.mark_end()
     barrier()
     clocks = sampler.stop()
     T.tpmlp_device_status()
@@ -468,8 +504,14 @@ def run_gpu(args):
                 d2h_copy(i)
             stream.wait_stream(copy_stream)
 
-        run_pipeline(3)
-        torch.cuda.synchronize()
+        # warm-up at the settled clock, like the device-timed region (the buffer set-up above
+        # left the GPU idle long enough for the power controller to raise the clock again)
+        t_w = time.time()
+        while True:
+            run_pipeline(5)
+            torch.cuda.synchronize()
+            if args.warmup is not None or time.time() - t_w >= WARMUP_SECONDS:
+                break
         barrier()
         a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -526,7 +568,7 @@ def run_gpu(args):
 
     if rank == 0:
         out = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
-               "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+               "warmup": n_warm, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                "config": {"workload": wl.name, "s": s, "b": b, "h": h, "ffn": f, "p": p,
                           "step": "fwd+bwd" if wl.backward else "fwd",
