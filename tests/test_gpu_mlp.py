@@ -226,10 +226,24 @@ def test_single_and_pair_tiles_agree(env, orc):
 
 def test_mixed_wave_shape(env, orc):
     """A shape whose row and dX GEMMs have 80 pair tiles (76 pairs fit at once), so the
-    last wave holds 4 tiles; the weight-gradient GEMMs have fewer tiles than pairs."""
+    last wave holds 4 tiles, which walk K (and the shard sum) backwards; the
+    weight-gradient GEMMs have fewer tiles than pairs."""
     _, synth, _ = env
     wl = synth.custom(320, 8, 2048, 1024, 2, dtype="bf16", sigma_w=0.03, sigma_bias=0.05, seed=77)
     _run_and_check(env, orc, wl)
+
+
+def test_every_gemm_two_waves(env, orc):
+    """All six GEMMs with more pair tiles than co-resident pairs (80 to 100 tiles), so
+    every GEMM has second-wave tiles that walk K backwards: the batched column, dH,
+    dA and dB GEMMs as well as the shard-summing row and dX GEMMs.  Full parity."""
+    _, synth, T = env
+    T.tpmlp_set_gemm_mode(2)
+    try:
+        wl = synth.custom(512, 4, 2560, 2560, 2, dtype="bf16", sigma_w=0.02, sigma_bias=0.05, seed=78)
+        _run_and_check(env, orc, wl)
+    finally:
+        T.tpmlp_set_gemm_mode(0)
 
 
 def _random_shapes(n, seed):
