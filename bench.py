@@ -77,27 +77,40 @@ def job_throughput(units_per_step_per_rank: float, world: int, slowest_ms_per_st
     return units_per_step_per_rank * world / (slowest_ms_per_step * 1e-3)
 
 
+def kernel_code_digest():
+    """sha256 of the GEMM kernel sources with comments and blank space removed, so that the
+    committed DRAM capture stays valid across comment-only edits but not across code edits."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cuh", "gemm_tc.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "megatron_tensor_mlp_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        lines = [" ".join(line.split()) for line in text.splitlines()]
+        h.update("\n".join(line for line in lines if line).encode())
+    return h.hexdigest()
+
+
 def captured_traffic(kernel_key):
     """DRAM bytes per launch of a forward GEMM at the bench workload, from the committed ncu
-    summary, or None when the kernel sources have changed since that capture."""
-    import hashlib
+    summary, or None when the kernel code has changed since that capture."""
     path = os.path.join(ROOT, "profiles", "dram_traffic_s2048_b4_h5120_ffn20480_p4.txt")
-    srcs = ["gemm_tc.cuh", "gemm_tc.cu", "ptx.cuh"]
     try:
-        h = hashlib.sha256()
-        for f in srcs:
-            with open(os.path.join(ROOT, "megatron_tensor_mlp_gb300", "csrc", f), "rb") as fh:
-                h.update(fh.read())
+        digest = kernel_code_digest()
         recorded, vals = None, {}
         for line in open(path):
-            parts = line.split()
-            if not parts or parts[0].startswith("#"):
+            if line.startswith("#"):
                 continue
-            if parts[0] == "kernel_source_sha256":
+            parts = line.split()
+            if not parts:
+                continue
+            if parts[0] == "kernel_code_sha256":
                 recorded = parts[1]
             elif len(parts) >= 3:
                 vals[parts[0]] = int(parts[1]) + int(parts[2])
-        if recorded != h.hexdigest():
+        if recorded != digest:
             return None
         return vals.get(kernel_key)
     except (OSError, ValueError):

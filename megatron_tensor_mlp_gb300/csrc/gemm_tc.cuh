@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // reads A from each CTA and exchanges the B halves in hardware, and writes
 // rows 128 r .. 128 r + 127 of the tile into CTA r's tensor memory.  So each
 // SM holds half as many B bytes per stage as the single-CTA kernel (32 KiB
-// stages, six in flight) and the pair reads a third fewer bytes from L2.
+// stages, seven in flight) and the pair reads a third fewer bytes from L2.
 //
 //   leader (r = 0)  warp 0: TMA producer, arms its full barrier for both CTAs'
 //                            bytes (the peer's copies complete on it too)
