@@ -267,11 +267,15 @@ tpmlp_status tpmlp_device_status(void* stream);
 tpmlp_status tpmlp_debug_wait_timeout(uint32_t timeout_us, void* stream);
 
 /*
- * Tiling of the bf16 GEMMs, process wide: 0 = automatic (default: 256x256 tiles
- * on CTA pairs when there are enough of them to fill the GPU, else 128x256 tiles
- * on single CTAs), 1 = single-CTA tiles only, 2 = CTA-pair tiles only.  Results
- * agree within rounding in every mode; the control exists for tuning and tests.
- * Returns TPMLP_ERR_SHAPE for other values.
+ * Tiling of the bf16 GEMMs, process wide.  0 = automatic (default): 256x256 tiles
+ * on CTA pairs when there are enough of them to fill the GPU, else single-CTA
+ * tiles (128x256, or 128x128 when 128x256 tiles would leave more than half of the
+ * SMs idle); CTA-pair tiles store their outputs directly from registers, or, when
+ * a tile's K loop is short (at most 40 blocks of 64), through shared memory with
+ * TMA stores.  1 = single-CTA tiles only; 2 = CTA-pair tiles only (epilogue chosen
+ * as in 0); 3 = CTA-pair tiles, direct stores; 4 = CTA-pair tiles, TMA stores (the
+ * SwiGLU epilogues always store directly).  Results agree within rounding in every
+ * mode; the control exists for tuning and tests.  TPMLP_ERR_SHAPE for other values.
  */
 tpmlp_status tpmlp_set_gemm_mode(int mode);
 int tpmlp_get_gemm_mode(void);

@@ -54,7 +54,45 @@ bool make_map(CUtensorMap* map, const Operand& op, uint64_t inner, uint64_t oute
     return true;
 }
 
-std::atomic<int> g_gemm_mode{0};  // 0 automatic, 1 single-CTA tiles, 2 CTA-pair tiles
+// 3-D tensor map over an output [shards][rows][cols] for the staged epilogue's TMA
+// stores: 32 x 32 boxes; bf16 rows of a box are 64 B (64-byte swizzle), fp32 rows 128 B
+// (128-byte swizzle), matching the staging layout in shared memory.
+bool make_out_map(CUtensorMap* map, void* ptr, int64_t ld, int64_t ss, uint64_t cols, uint64_t rows,
+                  uint64_t shards, bool f32) {
+    auto fn = encode_fn();
+    if (!fn) {
+        set_error("cuTensorMapEncodeTiled is not available from the driver");
+        return false;
+    }
+    const uint64_t es = f32 ? 4 : 2;
+    const uint64_t ld_bytes = static_cast<uint64_t>(ld) * es;
+    uint64_t ss_bytes = static_cast<uint64_t>(ss) * es;
+    if (shards <= 1) {
+        shards = 1;
+        ss_bytes = ld_bytes * rows;  // unused extent; any valid multiple of 16
+    }
+    cuuint64_t dims[3] = {cols, rows, shards};
+    cuuint64_t strides[2] = {ld_bytes, ss_bytes};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled (output) failed (%d): dims %llu x %llu x %llu, strides %llu %llu",
+                  static_cast<int>(r), (unsigned long long)cols, (unsigned long long)rows,
+                  (unsigned long long)shards, (unsigned long long)ld_bytes, (unsigned long long)ss_bytes);
+        return false;
+    }
+    return true;
+}
+
+// K blocks per tile up to which the pair kernel uses the staged epilogue: a 256x256 tile's
+// main loop takes ~512 cycles per 64-wide K block, a direct-store epilogue ~10-20 k cycles.
+constexpr int kStagedMaxKBlocks = 40;
+
+std::atomic<int> g_gemm_mode{0};  // 0 auto, 1 single-CTA, 2 pair, 3 pair + direct stores, 4 pair + TMA stores
 std::atomic<int> g_group_m{16};  // M-blocks per raster group
 
 template <typename Kern>
@@ -96,14 +134,15 @@ bool make_map_chunked(CUtensorMap* map, const Operand& op, uint64_t mn, uint64_t
     return true;
 }
 
-template <bool A_MN, bool B_MN, int EPI>
+template <bool A_MN, bool B_MN, int EPI, int SBN>
 tpmlp_status launch_single(const CUtensorMap& ma, const CUtensorMap& mb, const tc::KArgs& k, const DeviceInfo& dev,
                            cudaStream_t st) {
-    auto kern = tc::gemm_kernel<A_MN, B_MN, EPI>;
+    auto kern = tc::gemm_kernel<A_MN, B_MN, EPI, SBN>;
+    constexpr int smem = tc::SingleGeom<SBN>::smem_bytes;
     static bool attr_done[64] = {};
-    if (!set_smem_attr(kern, dev.device, tc::SMEM_BYTES, attr_done)) return TPMLP_ERR_CUDA;
+    if (!set_smem_attr(kern, dev.device, smem, attr_done)) return TPMLP_ERR_CUDA;
     const int grid = k.num_tiles < dev.sm_count ? k.num_tiles : dev.sm_count;
-    kern<<<grid, tc::NUM_THREADS, tc::SMEM_BYTES, st>>>(ma, mb, k);
+    kern<<<grid, tc::NUM_THREADS, smem, st>>>(ma, mb, k);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("tcgen05 GEMM launch: %s", cudaGetErrorString(e));
@@ -113,20 +152,21 @@ tpmlp_status launch_single(const CUtensorMap& ma, const CUtensorMap& mb, const t
 }
 
 // Co-resident CTA pairs of the pair kernel on this device (0 if it cannot run).
-template <bool A_MN, bool B_MN, int EPI>
+template <bool A_MN, bool B_MN, int EPI, bool STAGED>
 int pair_capacity(const DeviceInfo& dev) {
     static int cap[64];
     static bool done[64];
     static bool attr_done[64] = {};
     if (dev.device >= 64) return 0;
     if (done[dev.device]) return cap[dev.device];
-    auto kern = tc::gemm_pair_kernel<A_MN, B_MN, EPI>;
+    auto kern = tc::gemm_pair_kernel<A_MN, B_MN, EPI, STAGED>;
+    constexpr int smem = tc::PairGeom<STAGED>::smem_bytes;
     int n = 0;
-    if (set_smem_attr(kern, dev.device, tc::P_SMEM_BYTES, attr_done)) {
+    if (set_smem_attr(kern, dev.device, smem, attr_done)) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (dev.sm_count / 2));
         cfg.blockDim = dim3(tc::NUM_THREADS);
-        cfg.dynamicSmemBytes = tc::P_SMEM_BYTES;
+        cfg.dynamicSmemBytes = smem;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
@@ -142,14 +182,14 @@ int pair_capacity(const DeviceInfo& dev) {
     return n;
 }
 
-template <bool A_MN, bool B_MN, int EPI>
-tpmlp_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const tc::KArgs& k, int clusters,
-                         cudaStream_t st) {
-    auto kern = tc::gemm_pair_kernel<A_MN, B_MN, EPI>;
+template <bool A_MN, bool B_MN, int EPI, bool STAGED>
+tpmlp_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
+                         const CUtensorMap& mo2, const tc::KArgs& k, int clusters, cudaStream_t st) {
+    auto kern = tc::gemm_pair_kernel<A_MN, B_MN, EPI, STAGED>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
     cfg.blockDim = dim3(tc::NUM_THREADS);
-    cfg.dynamicSmemBytes = tc::P_SMEM_BYTES;
+    cfg.dynamicSmemBytes = tc::PairGeom<STAGED>::smem_bytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -158,7 +198,7 @@ tpmlp_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const tc:
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, k);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mo, mo2, k);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("tcgen05 CTA-pair GEMM launch: %s", cudaGetErrorString(e));
@@ -167,18 +207,21 @@ tpmlp_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const tc:
     return TPMLP_OK;
 }
 
-// Picks single-CTA or CTA-pair tiles and launches.  Pair tiles when there are at
-// least as many 256-row tiles as co-resident pairs (or when forced).
+// Picks the tiling and launches.  CTA-pair 256x256 tiles when there are at least as many
+// of them as co-resident pairs (or when forced); otherwise single-CTA 128x256 tiles, or
+// 128x128 tiles when the 128x256 ones would leave more than half of the SMs idle.
 template <bool A_MN, bool B_MN, int EPI>
 tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& g, tc::KArgs k, const DeviceInfo& dev,
                             cudaStream_t st) {
     const int mode = g_gemm_mode.load(std::memory_order_relaxed);
     const int m_pairs = static_cast<int>((g.M + 2 * tc::BM - 1) / (2 * tc::BM));
     const int pair_tiles = m_pairs * k.n_blocks * k.batch;
-    int cap = (mode == 1) ? 0 : pair_capacity<A_MN, B_MN, EPI>(dev);
-    const bool use_pair = cap > 0 && (mode == 2 || pair_tiles >= cap);
+    int cap = (mode == 1) ? 0 : pair_capacity<A_MN, B_MN, EPI, false>(dev);
+    const bool use_pair = cap > 0 && (mode >= 2 || pair_tiles >= cap);
+    constexpr bool kNarrowOk = EPI != EPI_SWIGLU && EPI != EPI_DSWIGLU;  // packed layouts span 256 columns
+    const bool narrow = kNarrowOk && !use_pair && 2 * k.num_tiles <= dev.sm_count && g.N > 128;
     CUtensorMap ma, mb;
-    const uint32_t b_rows = use_pair ? tc::BN / 2 : tc::BN;
+    const uint32_t b_rows = (use_pair || narrow) ? tc::BN / 2 : tc::BN;
     // MN-major operands: one 4-D box per stage when the MN extent is a multiple of 64
     k.a_chunked = (a.mn_major && g.M % 64 == 0) ? 1 : 0;
     k.b_chunked = (b.mn_major && g.N % 64 == 0) ? 1 : 0;
@@ -189,11 +232,32 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
     if (k.b_chunked) ok = make_map_chunked(&mb, b, g.N, g.K, b_rows / 64);
     else ok = b.mn_major ? make_map(&mb, b, g.N, g.K, 64, tc::BK) : make_map(&mb, b, g.K, g.N, tc::BK, b_rows);
     if (!ok) return TPMLP_ERR_CUDA;
-    if (!use_pair) return launch_single<A_MN, B_MN, EPI>(ma, mb, k, dev, st);
+    if (!use_pair) {
+        if constexpr (kNarrowOk) {
+            if (narrow) {
+                k.n_blocks = static_cast<int>((g.N + 127) / 128);
+                k.num_tiles = k.m_blocks * k.n_blocks * k.batch;
+                return launch_single<A_MN, B_MN, EPI, 128>(ma, mb, k, dev, st);
+            }
+        }
+        return launch_single<A_MN, B_MN, EPI, 256>(ma, mb, k, dev, st);
+    }
     k.m_blocks = m_pairs;
     k.num_tiles = pair_tiles;
     const int clusters = pair_tiles < cap ? pair_tiles : cap;
-    return launch_pair<A_MN, B_MN, EPI>(ma, mb, k, clusters, st);
+    // Short K loops (a tile's main loop shorter than a direct-store epilogue): staged epilogue.
+    if constexpr (kNarrowOk) {
+        const bool staged = mode == 4 || (mode != 3 && k.k_iters <= kStagedMaxKBlocks);
+        if (staged && pair_capacity<A_MN, B_MN, EPI, true>(dev) >= clusters) {
+            CUtensorMap mo, mo2 = ma;
+            const uint64_t oshards = static_cast<uint64_t>(k.batch);
+            if (!make_out_map(&mo, g.out, g.out_ld, g.out_ss, g.N, g.M, oshards, g.out_f32)) return TPMLP_ERR_CUDA;
+            if (g.out2 != nullptr && !make_out_map(&mo2, g.out2, g.out2_ld, g.out2_ss, g.N, g.M, oshards, false))
+                return TPMLP_ERR_CUDA;
+            return launch_pair<A_MN, B_MN, EPI, true>(ma, mb, mo, mo2, k, clusters, st);
+        }
+    }
+    return launch_pair<A_MN, B_MN, EPI, false>(ma, mb, ma, ma, k, clusters, st);
 }
 
 }  // namespace

@@ -36,17 +36,14 @@ namespace tc {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
+constexpr int STAGES = 4;                  // single-CTA 128x256 tiles: 48 KiB stages
 constexpr int A_TILE_BYTES = BM * BK * 2;  // 16 KiB
-constexpr int B_TILE_BYTES = BN * BK * 2;  // 32 KiB
-constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
 constexpr int MN_CHUNK_BYTES = BK * 128;   // one 64-wide MN chunk of an MN-major tile
 constexpr int NUM_THREADS = 384;
 constexpr int FIRST_EPI_WARP = 4;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr uint32_t TMEM_COLS = 512;        // two 256-column fp32 accumulators
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + BAR_BYTES;
 
 #ifndef TPMLP_MN_LBO_BYTES
 #define TPMLP_MN_LBO_BYTES MN_CHUNK_BYTES
@@ -330,9 +327,11 @@ __device__ __forceinline__ void dswiglu_chunk(const KArgs& p, const uint32_t (&r
 }
 
 // One tile's epilogue for this warp: TMEM lane quarter q, column half `half`.
-template <int EPI>
+// NCH = 32-column chunks per column half of the tile: 4 for 256-wide tiles, 2 for 128-wide.
+template <int EPI, int NCH = 4>
 __device__ __forceinline__ void epilogue_tile(const KArgs& p, uint32_t t_row, int gm, int nb, int half, int shard) {
     if constexpr (EPI == EPI_SWIGLU) {
+        static_assert(NCH == 4, "the packed SwiGLU layout needs 256-wide tiles");
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
             const int fo = half * 64 + c * 32;
@@ -344,27 +343,43 @@ __device__ __forceinline__ void epilogue_tile(const KArgs& p, uint32_t t_row, in
         }
     } else {
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-            const int col = half * 128 + c * 32;
+        for (int c = 0; c < NCH; ++c) {
+            const int col = half * (NCH * 32) + c * 32;
             uint32_t r[32];
             tmem_ld_32x32b_x32(t_row + col, r);
             tmem_ld_wait();
+            static_assert(EPI != EPI_DSWIGLU || NCH == 4, "the packed SwiGLU layout needs 256-wide tiles");
             if constexpr (EPI == EPI_DSWIGLU) dswiglu_chunk(p, r, gm, nb * BN + col, shard);
-            else epilogue_chunk<EPI>(p, r, gm, nb * BN + col, shard);
+            else epilogue_chunk<EPI>(p, r, gm, nb * (NCH * 64) + col, shard);
         }
     }
 }
 
-template <bool A_MN, bool B_MN, int EPI>
+// Single-CTA tiles are BM x SBN: SBN = 256 (4-stage ring of 48 KiB), or SBN = 128 for GEMMs
+// with too few 256-wide tiles to fill the SMs (7-stage ring of 32 KiB, 2 x 128 TMEM columns).
+template <int SBN>
+struct SingleGeom {
+    static_assert(SBN == 256 || SBN == 128, "single-CTA tile width");
+    static constexpr int b_bytes = SBN * BK * 2;
+    static constexpr int stage_bytes = A_TILE_BYTES + b_bytes;
+    static constexpr int stages = SBN == 256 ? STAGES : 7;
+    static constexpr uint32_t tmem_cols = 2 * SBN;
+    static constexpr int smem_bytes = 1024 + stages * stage_bytes + BAR_BYTES;
+    static_assert(smem_bytes <= 227 * 1024, "single-CTA kernel shared memory");
+};
+
+template <bool A_MN, bool B_MN, int EPI, int SBN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KArgs p) {
+    using G = SingleGeom<SBN>;
+    constexpr int kStages = G::stages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
-    uint8_t* sB = smem + STAGES * A_TILE_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-    uint64_t* empty = full + STAGES;
-    uint64_t* tfull = empty + STAGES;
+    uint8_t* sB = smem + kStages * A_TILE_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * G::stage_bytes);
+    uint64_t* empty = full + kStages;
+    uint64_t* tfull = empty + kStages;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -373,7 +388,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
         }
@@ -390,7 +405,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_alloc(tmem_slot, G::tmem_cols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -410,7 +425,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
                 int mb, nb, shard;
                 decode_tile(p, t, mb, nb, shard);
-                const int row0 = mb * BM, col0 = nb * BN;
+                const int row0 = mb * BM, col0 = nb * SBN;
                 // sum mode: the K loop walks (shard, k); batched: shard fixed per tile
                 int sa = p.sum_shards ? 0 : (p.a_batched ? shard : 0);
                 int sb = p.sum_shards ? 0 : (p.b_batched ? shard : 0);
@@ -421,11 +436,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     uint64_t* fb = full + stage;
-                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    mbar_arrive_expect_tx(fb, G::stage_bytes);
                     armed |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                     uint8_t* a_dst = sA + stage * A_TILE_BYTES;
-                    uint8_t* b_dst = sB + stage * B_TILE_BYTES;
+                    uint8_t* b_dst = sB + stage * G::b_bytes;
                     if constexpr (!A_MN) {
                         tma_load_3d(a_dst, &tmA, fb, k0, row0, sa);
                     } else if (p.a_chunked) {
@@ -441,10 +456,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tma_load_4d(b_dst, &tmB, fb, 0, k0, col0 / 64, sb);
                     } else {
 #pragma unroll
-                        for (int c = 0; c < BN / 64; ++c)
+                        for (int c = 0; c < SBN / 64; ++c)
                             tma_load_3d(b_dst + c * MN_CHUNK_BYTES, &tmB, fb, col0 + c * 64, k0, sb);
                     }
-                    if (++stage == STAGES) {
+                    if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -458,7 +473,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (!ok) {
                 // Let every copy already issued land before the CTA can exit.
-                for (int s = 0; s < STAGES; ++s)
+                for (int s = 0; s < kStages; ++s)
                     if (armed & (1u << s))
                         mbar_wait_bounded(full + s, (last_parity >> s) & 1u, p.status, p.timeout_ns, kWhereDrain,
                                           /*watch_status=*/false);
@@ -467,7 +482,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------------------ MMA issuer
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, SBN, A_MN, B_MN);
             const uint64_t a_desc0 = A_MN ? sdesc_sw128(smem_u32(sA), TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES)
                                           : sdesc_sw128(smem_u32(sA), 16, 1024);
             const uint64_t b_desc0 = B_MN ? sdesc_sw128(smem_u32(sB), TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES)
@@ -486,7 +501,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * BN;
+                const uint32_t d_tmem = tmem_base + acc * SBN;
                 for (int it = 0; it < p.k_iters; ++it) {
                     if (!mbar_wait_bounded(full + stage, phase, p.status, p.timeout_ns, kWhereMma)) {
                         ok = false;
@@ -495,12 +510,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tc_fence_after();
                     // descriptor start addresses are in 16-byte units in the low bits
                     const uint64_t adesc = a_desc0 + static_cast<uint64_t>(stage * (A_TILE_BYTES >> 4));
-                    const uint64_t bdesc = b_desc0 + static_cast<uint64_t>(stage * (B_TILE_BYTES >> 4));
+                    const uint64_t bdesc = b_desc0 + static_cast<uint64_t>(stage * (G::b_bytes >> 4));
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
                         umma_f16(d_tmem, adesc + kk * a_kstep, bdesc + kk * b_kstep, idesc, (it | kk) != 0 ? 1u : 0u);
                     umma_commit(empty + stage);
-                    if (++stage == STAGES) {
+                    if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -527,8 +542,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int mb, nb, shard;
             decode_tile(p, t, mb, nb, shard);
             const int gm = mb * BM + q * 32 + lane;
-            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-            epilogue_tile<EPI>(p, t_row, gm, nb, half, shard);
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * SBN;
+            epilogue_tile<EPI, SBN / 64>(p, t_row, gm, nb, half, shard);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty + acc);
@@ -541,10 +556,129 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     if (warp == 1) {
         __syncwarp();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        tmem_dealloc(tmem_base, G::tmem_cols);
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// Staged epilogue (CTA-pair kernel, short K loops): through shared memory and TMA
+// stores.
+//
+// Each epilogue warp owns a 4 KiB staging buffer.  Per 32-column chunk its 32
+// threads (one output row each) write the converted values into a 32-row box in
+// the layout a swizzled TMA store expects, and lane 0 stores the box with one
+// cp.async.bulk.tensor (the tensor map clips rows >= M and columns >= N):
+//   bf16 box: 32 rows x 64 B, 64-byte swizzle: 16-byte chunk c of row r at c ^ ((r >> 1) & 3)
+//   fp32 box: 32 rows x 128 B, 128-byte swizzle: chunk c of row r at c ^ (r & 7)
+// Both patterns spread the 32 rows of one warp store over all banks.  Such an
+// epilogue finishes a 256x256 tile in well under half the time of per-row 16-byte
+// global stores (which touch 32 L2 lines per warp instruction), but moves every
+// output byte through shared memory twice, which slows a concurrent main loop
+// per clock; it is the faster choice when the K loop of a tile is short and the
+// epilogue, not the main loop, would set the pace.
+// ---------------------------------------------------------------------------
+constexpr int EPI_WARP_BYTES = 4096;
+
+__device__ __forceinline__ void stage_bf16x32(uint8_t* box, int r, const float* v) {
+    uint8_t* row = box + r * 64;
+    const int sw = (r >> 1) & 3;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint4 u;
+        u.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
+        u.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
+        u.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
+        u.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
+        *reinterpret_cast<uint4*>(row + ((c ^ sw) << 4)) = u;
+    }
+}
+__device__ __forceinline__ void stage_f32x32(uint8_t* box, int r, const float* v) {
+    uint8_t* row = box + r * 128;
+    const int sw = r & 7;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4*>(row + ((c ^ sw) << 4)) =
+            make_float4(v[4 * c + 0], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+}
+
+// Staged epilogue of one warp's 32 rows x 128 columns of a tile (EPI_BIAS_ACT, EPI_DGELU,
+// EPI_STORE).  row0 = the warp's first output row, lane = its row within the box; seq
+// counts the warp's staged chunks across tiles, so that consecutive chunks of a single
+// bf16 output always alternate between the two 2 KiB boxes.
+template <int EPI>
+__device__ __forceinline__ void epilogue_tile_staged(const KArgs& p, const CUtensorMap* tm_out,
+                                                     const CUtensorMap* tm_out2, uint32_t t_row, int row0, int lane,
+                                                     int nb, int half, int shard, uint8_t* ebuf, uint32_t& seq) {
+    if (row0 >= p.M) return;
+    const bool two = (EPI == EPI_BIAS_ACT) && p.out2 != nullptr;  // Y and the pre-activation H
+    const bool f32 = (EPI == EPI_STORE) && p.out_f32;
+    const bool one_buffer = two || f32;  // 4 KiB per chunk; otherwise two 2 KiB boxes alternate
+    const int gm = row0 + lane;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+        const int col = half * 128 + c * 32;
+        const int gn0 = nb * BN + col;
+        if (gn0 >= p.N) break;
+        const int nvalid = p.N - gn0;
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + col, r);
+        tmem_ld_wait();
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+        uint8_t* box = one_buffer ? ebuf : ebuf + (seq & 1u) * 2048;
+        ++seq;
+        // the box may be rewritten once the TMA engine has read its previous contents
+        // (single output: that was the chunk before last, so one group may stay pending)
+        if (lane == 0) {
+            if (one_buffer) bulk_wait_group_read<0>();
+            else bulk_wait_group_read<1>();
+        }
+        __syncwarp();
+        if constexpr (EPI == EPI_BIAS_ACT) {
+            if (p.bias != nullptr) {
+                const __nv_bfloat16* bp = static_cast<const __nv_bfloat16*>(p.bias) + shard * p.bias_ss + gn0;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    if (g * 8 < nvalid) {
+                        float bf[8];
+                        unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(bp + g * 8)), bf);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) v[g * 8 + i] += bf[i];
+                    }
+                }
+            }
+            if (two) stage_bf16x32(ebuf + 2048, lane, v);
+            if (p.act == TPMLP_ACT_GELU_ERF) gelu_inplace32(v);
+            stage_bf16x32(box, lane, v);
+        } else if constexpr (EPI == EPI_DGELU) {
+            if (gm < p.M) {
+                const __nv_bfloat16* hp =
+                    static_cast<const __nv_bfloat16*>(p.aux) + shard * p.aux_ss + (long long)gm * p.aux_ld + gn0;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    if (g * 8 < nvalid) {
+                        float hv[8];
+                        unpack_bf16x8(*reinterpret_cast<const uint4*>(hp + g * 8), hv);
+                        dgelu_mul8(v + g * 8, hv);
+                    }
+                }
+            }
+            stage_bf16x32(box, lane, v);
+        } else {
+            if (f32) stage_f32x32(box, lane, v);
+            else stage_bf16x32(box, lane, v);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_3d(tm_out, box, gn0, row0, shard);
+            if (two) tma_store_3d(tm_out2, ebuf + 2048, gn0, row0, shard);
+            bulk_commit_group();
+        }
+    }
+}
 
 // ============================================================================
 // CTA-pair variant: a cluster of two CTAs on neighbouring SMs computes one
@@ -565,21 +699,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //                   warps 4-11: epilogue of its 128 rows; the accumulator is
 //                            released by 16 arrivals on the leader's barrier
 // ============================================================================
-constexpr int P_STAGES = 7;
 constexpr int P_A_BYTES = BM * BK * 2;        // 16 KiB: this CTA's 128 rows of A
 constexpr int P_B_BYTES = (BN / 2) * BK * 2;  // 16 KiB: this CTA's 128 columns of B
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
-constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + BAR_BYTES;
 
-template <bool A_MN, bool B_MN, int EPI>
+// STAGED = false: direct-store epilogue, 7 stages.  STAGED = true: staged (TMA-store)
+// epilogue, 6 stages + 8 x 4 KiB staging boxes.
+template <bool STAGED>
+struct PairGeom {
+    static constexpr int stages = STAGED ? 6 : 7;
+    static constexpr int epi_bytes = STAGED ? NUM_EPI_WARPS * EPI_WARP_BYTES : 0;
+    static constexpr int smem_bytes = 1024 + stages * P_STAGE_BYTES + epi_bytes + BAR_BYTES;
+    static_assert(smem_bytes <= 227 * 1024, "pair kernel shared memory");
+};
+
+template <bool A_MN, bool B_MN, int EPI, bool STAGED>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2,
                      const KArgs p) {
+    constexpr int P_STAGES = PairGeom<STAGED>::stages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + P_STAGES * P_A_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
+    uint8_t* sE = smem + P_STAGES * P_STAGE_BYTES;  // staging boxes (STAGED), 1 KiB aligned
+    uint64_t* full = reinterpret_cast<uint64_t*>(sE + PairGeom<STAGED>::epi_bytes);
     uint64_t* empty = full + P_STAGES;
     uint64_t* tfull = empty + P_STAGES;
     uint64_t* tempty = tfull + 2;
@@ -609,6 +754,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+    }
+    if constexpr (STAGED) {
+        if (warp == FIRST_EPI_WARP && lane == 0) {
+            tma_prefetch_desc(&tmO);
+            tma_prefetch_desc(&tmO2);
+        }
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, TMEM_COLS);
@@ -761,6 +912,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int q = warp & 3;
         const int half = (warp - FIRST_EPI_WARP) >> 2;
         const uint32_t tempty_leader0 = mapa_shared(smem_u32(tempty), 0);
+        uint8_t* ebuf = sE + (warp - FIRST_EPI_WARP) * EPI_WARP_BYTES;  // STAGED only
+        uint32_t seq = 0;
         int lt = 0;
         for (int t = cluster_id; t < p.num_tiles; t += n_clusters, ++lt) {
             const int acc = lt & 1;
@@ -772,12 +925,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             int mb, nb, shard;
             decode_tile(p, t, mb, nb, shard);
-            const int gm = mb * (2 * BM) + static_cast<int>(rank) * BM + q * 32 + lane;
+            const int row0 = mb * (2 * BM) + static_cast<int>(rank) * BM + q * 32;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-            epilogue_tile<EPI>(p, t_row, gm, nb, half, shard);
+            if constexpr (STAGED)
+                epilogue_tile_staged<EPI>(p, &tmO, &tmO2, t_row, row0, lane, nb, half, shard, ebuf, seq);
+            else
+                epilogue_tile<EPI>(p, t_row, row0 + lane, nb, half, shard);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader0 + acc * 8);
+        }
+        if constexpr (STAGED) {
+            if (lane == 0) bulk_wait_group_all();  // this warp's output stores are complete
         }
     }
 

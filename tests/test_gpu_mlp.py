@@ -17,7 +17,7 @@ def env():
     return harness, synth, tpmlp
 
 
-@pytest.fixture(params=[1, 2], ids=["single-cta", "cta-pair"])
+@pytest.fixture(params=[1, 3, 4], ids=["single-cta", "pair-direct", "pair-staged"])
 def gemm_mode(request, env):
     """Force 128x256 single-CTA tiles or 256x256 CTA-pair tiles for the test."""
     T = env[2]
@@ -207,21 +207,37 @@ def test_empty_batch(env):
 
 
 def test_single_and_pair_tiles_agree(env, orc):
-    """The two tilings accumulate in the same K order per element: results are bit-identical."""
+    """Single-CTA and CTA-pair tiles accumulate in the same K order per element, and the two
+    pair epilogues store the same values: results are bit-identical in every forced mode."""
     import torch
     harness, synth, T = env
     wl = synth.custom(150, 4, 384, 1536, 3, dtype="bf16", seed=9)
     buf = harness.MLPBuffers(wl, backward=True)
     out = {}
-    for mode in (1, 2):
+    for mode in (1, 2, 3, 4):
         T.tpmlp_set_gemm_mode(mode)
         buf.fwd()
         buf.bwd()
         T.tpmlp_device_status()
-        out[mode] = [t.clone() for t in (buf.Z, buf.Y, buf.dX, buf.dA_sh, buf.dB_sh)]
+        out[mode] = [t.clone() for t in (buf.Z, buf.Y, buf.H, buf.dX, buf.dA_sh, buf.dB_sh, buf.dH)]
     T.tpmlp_set_gemm_mode(0)
-    for a, b_ in zip(out[1], out[2]):
-        assert torch.equal(a, b_)
+    for mode in (2, 3, 4):
+        for a, b_ in zip(out[1], out[mode]):
+            assert torch.equal(a, b_), mode
+
+
+@pytest.mark.parametrize("shape", [(40, 6, 192, 768, 3), (320, 8, 1024, 2048, 2)], ids=["narrow", "wide"])
+def test_single_cta_tile_widths(env, orc, shape):
+    """Single-CTA tiles are 128x128 when 128x256 tiles would leave more than half of the
+    SMs idle, else 128x256.  The first shape runs every GEMM on 128x128 tiles; the second
+    runs the column, row, dH and dX GEMMs on 128x256 tiles and dA, dB on 128x128."""
+    _, synth, T = env
+    T.tpmlp_set_gemm_mode(1)
+    try:
+        wl = synth.custom(*shape, dtype="bf16", sigma_w=0.03, sigma_bias=0.05, seed=sum(shape))
+        _run_and_check(env, orc, wl)
+    finally:
+        T.tpmlp_set_gemm_mode(0)
 
 
 def test_mixed_wave_shape(env, orc):
@@ -233,12 +249,14 @@ def test_mixed_wave_shape(env, orc):
     _run_and_check(env, orc, wl)
 
 
-def test_every_gemm_two_waves(env, orc):
+@pytest.mark.parametrize("mode", [3, 4], ids=["pair-direct", "pair-staged"])
+def test_every_gemm_two_waves(env, orc, mode):
     """All six GEMMs with more pair tiles than co-resident pairs (80 to 100 tiles), so
     every GEMM has second-wave tiles that walk K backwards: the batched column, dH,
-    dA and dB GEMMs as well as the shard-summing row and dX GEMMs.  Full parity."""
+    dA and dB GEMMs as well as the shard-summing row and dX GEMMs.  Full parity, with
+    either epilogue of the pair kernel."""
     _, synth, T = env
-    T.tpmlp_set_gemm_mode(2)
+    T.tpmlp_set_gemm_mode(mode)
     try:
         wl = synth.custom(512, 4, 2560, 2560, 2, dtype="bf16", sigma_w=0.02, sigma_bias=0.05, seed=78)
         _run_and_check(env, orc, wl)
