@@ -272,7 +272,60 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------------- GPU arm
-def time_next_rows(stream, steps, peaks):
+def settled_ms(fn, stream, explicit_warmup=None, seconds=0.4):
+    """Milliseconds per call of fn at the settled power-capped clock: warm up for about
+    WARMUP_SECONDS (or explicit_warmup calls when given), then time enough calls for about
+    `seconds` with CUDA events on `stream`."""
+    import torch
+    if explicit_warmup is None:
+        t_w = time.time()
+        while time.time() - t_w < WARMUP_SECONDS:
+            for _ in range(5):
+                fn()
+            torch.cuda.synchronize()
+    else:
+        for _ in range(max(3, explicit_warmup)):
+            fn()
+        torch.cuda.synchronize()
+    a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(5):
+        fn()
+    z.record(stream)
+    torch.cuda.synchronize()
+    n = max(10, int(seconds / max(1e-6, a.elapsed_time(z) / 5e3)))
+    a.record(stream)
+    for _ in range(n):
+        fn()
+    z.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(z) / n, n
+
+
+def time_other_configs(stream, explicit_warmup):
+    """Forward and forward+backward of the parity-test workloads 2 and 3 (their own shapes,
+    seeded synthetic inputs), at the settled clock."""
+    from megatron_tensor_mlp_gb300 import harness, synth
+    from megatron_tensor_mlp_gb300 import tpmlp as T
+    import torch
+    out = {}
+    for cfg in (2, 3):
+        wl = synth.WORKLOADS[cfg]
+        b_ = harness.MLPBuffers(wl, backward=True)
+        ms_f, n_f = settled_ms(lambda: b_.fwd(stream=stream), stream, explicit_warmup)
+        ms_fb, n_fb = settled_ms(lambda: (b_.fwd(stream=stream), b_.bwd(stream=stream)), stream, explicit_warmup)
+        T.tpmlp_device_status()
+        f_fwd, f_bwd = wl.fwd_flops(), wl.bwd_flops()
+        out[wl.name] = {"fwd_ms": round(ms_f, 5), "fwd_TFLOP/s": round(f_fwd / (ms_f * 1e-3) / 1e12, 1),
+                        "fwd_bwd_ms": round(ms_fb, 5),
+                        "fwd_bwd_TFLOP/s": round((f_fwd + f_bwd) / (ms_fb * 1e-3) / 1e12, 1),
+                        "fwd_tokens_per_s": round(wl.M / (ms_f * 1e-3), 1), "steps": [n_f, n_fb]}
+        del b_
+        torch.cuda.empty_cache()
+    return out
+
+
+def time_next_rows(stream, steps, peaks, explicit_warmup=None):
     """Forward+backward timings of the widened rows at the fwd+bwd workload's sizes
     (s=2048, b=4, h=5120, p=4): the SwiGLU block (ffn=20480 per branch) and the attention
     tensor-parallel projections (QKV column projection over the per-head interleave, 40 heads,
@@ -289,17 +342,9 @@ def time_next_rows(stream, steps, peaks):
     out = {}
 
     def timed(fn, n):
-        for _ in range(3):
-            fn()
-        torch.cuda.synchronize()
-        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(n):
-            fn()
-        z.record(stream)
-        torch.cuda.synchronize()
+        ms, _ = settled_ms(fn, stream, explicit_warmup)
         T.tpmlp_device_status()
-        return a.elapsed_time(z) / n
+        return ms
 
     n = max(10, steps // 4)
     # SwiGLU block: gate+up column GEMM (2*2*M*h*f), row GEMM (2*M*f*h); backward twice that
@@ -546,18 +591,9 @@ def run_gpu(args):
         torch.cuda.empty_cache()
         w4 = synth.WORKLOADS[FWD_WORKLOAD]
         b4 = harness.MLPBuffers(w4, backward=False)
-        for _ in range(5):
-            b4.fwd(stream=stream)
-        torch.cuda.synchronize()
-        n4 = max(20, K // 2)
-        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(n4):
-            b4.fwd(stream=stream)
-        z.record(stream)
-        torch.cuda.synchronize()
+        # settled clock: building the inputs above left the GPU idle for a while
+        ms4, n4 = settled_ms(lambda: b4.fwd(stream=stream), stream, args.warmup, seconds=0.5)
         T.tpmlp_device_status()
-        ms4 = a.elapsed_time(z) / n4
         tf4 = w4.fwd_flops() / (ms4 * 1e-3) / 1e12
         fwd_pages = {"workload": w4.name, "ms": round(ms4, 4), "TFLOP/s": round(tf4, 1),
                      "tokens_per_s": round(w4.M / (ms4 * 1e-3), 1),
@@ -567,10 +603,14 @@ def run_gpu(args):
         del b4
         torch.cuda.empty_cache()
 
+    other_configs = None
+    if not args.no_next_rows and args.workload == MAIN_WORKLOAD:
+        other_configs = time_other_configs(stream, args.warmup)
+
     next_rows = None
     if not args.no_next_rows and args.workload == MAIN_WORKLOAD:
         torch.cuda.empty_cache()
-        next_rows = time_next_rows(stream, K, peaks)
+        next_rows = time_next_rows(stream, K, peaks, args.warmup)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -591,7 +631,8 @@ def run_gpu(args):
                "pct_of_nominal_bf16_peak": round(100 * value / ws / NOMINAL_BF16_TFLOPS, 2),
                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                "gpu_launches": launches_per_step * K, "clocks": clocks,
-               "fwd_pages_sizing": fwd_pages, "next_rows": next_rows}
+               "fwd_pages_sizing": fwd_pages, "next_rows": next_rows,
+               "other_configs": other_configs}
         print(json.dumps(out), flush=True)
     if ws > 1:
         import torch.distributed as dist
