@@ -137,15 +137,19 @@ __global__ void __launch_bounds__(256) colsum_kernel(const void* in, long long M
 }
 
 // Column sums of a bf16 [shards][M][N] tensor: a cluster of 8 CTAs shares one
-// 256-column strip, each CTA summing every 8th group of 8 rows; the partial sums
-// are added from the cluster's shared memory in a fixed order, so the result is
-// deterministic and needs no global scratch.  (N is a multiple of 8.)
+// 256-column strip; each CTA has 16 warps, warp w of CTA g summing rows
+// 16 g + w + 128 i, eight 16-byte loads in flight per thread (enough bytes in flight
+// for HBM even with a single shard, i.e. about one CTA per SM).  The partial sums are
+// added in shared memory and then across the cluster's shared memory in a fixed
+// order, so the result is deterministic and needs no global scratch.  (N is a
+// multiple of 8.)
 constexpr int CS_CLUSTER = 8;
+constexpr int CS_WARPS = 16;
 template <bool OUT_F32>
-__global__ void __cluster_dims__(1, CS_CLUSTER, 1) __launch_bounds__(256)
+__global__ void __cluster_dims__(1, CS_CLUSTER, 1) __launch_bounds__(CS_WARPS * 32)
     colsum_bf16_cluster_kernel(const __nv_bfloat16* __restrict__ in, long long M, long long N, void* out) {
     namespace cg = cooperative_groups;
-    __shared__ float part[8][256];
+    __shared__ float part[CS_WARPS][256];
     __shared__ float block_sum[256];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const long long s = blockIdx.z;
@@ -154,9 +158,8 @@ __global__ void __cluster_dims__(1, CS_CLUSTER, 1) __launch_bounds__(256)
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (c < N) {
         const __nv_bfloat16* base = in + s * M * N + c;
-        // rows grp*8 + warp + 64*i
-#pragma unroll 4
-        for (long long m = (long long)grp * 8 + warp; m < M; m += 64) {
+#pragma unroll 8
+        for (long long m = (long long)grp * CS_WARPS + warp; m < M; m += CS_WARPS * CS_CLUSTER) {
             const uint4 u = __ldg(reinterpret_cast<const uint4*>(base + m * N));
             const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -169,14 +172,14 @@ __global__ void __cluster_dims__(1, CS_CLUSTER, 1) __launch_bounds__(256)
 #pragma unroll
     for (int i = 0; i < 8; ++i) part[warp][lane * 8 + i] = acc[i];
     __syncthreads();
-    {
+    if (threadIdx.x < 256) {
         float r = 0.f;
-        for (int w = 0; w < 8; ++w) r += part[w][threadIdx.x];
+        for (int w = 0; w < CS_WARPS; ++w) r += part[w][threadIdx.x];
         block_sum[threadIdx.x] = r;
     }
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();  // every CTA's block_sum is complete
-    if (grp == 0) {
+    if (grp == 0 && threadIdx.x < 256) {
         float r = 0.f;
         for (int g = 0; g < CS_CLUSTER; ++g) r += cluster.map_shared_rank(block_sum, g)[threadIdx.x];
         const long long col = (long long)blockIdx.x * 256 + threadIdx.x;
@@ -307,8 +310,9 @@ tpmlp_status launch_colsum(const void* in, bool in_f32, int64_t shards, int64_t 
                            cudaStream_t st) {
     if (!in_f32) {
         dim3 g((unsigned)((N + 255) / 256), CS_CLUSTER, (unsigned)shards);
-        if (out_f32) colsum_bf16_cluster_kernel<true><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(in), M, N, out);
-        else colsum_bf16_cluster_kernel<false><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(in), M, N, out);
+        const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(in);
+        if (out_f32) colsum_bf16_cluster_kernel<true><<<g, CS_WARPS * 32, 0, st>>>(src, M, N, out);
+        else colsum_bf16_cluster_kernel<false><<<g, CS_WARPS * 32, 0, st>>>(src, M, N, out);
         return check_launch("column sum");
     }
     dim3 grid((unsigned)((N + 63) / 64), (unsigned)shards);
