@@ -142,8 +142,18 @@ tpmlp_status launch_single(const CUtensorMap& ma, const CUtensorMap& mb, const t
     static bool attr_done[64] = {};
     if (!set_smem_attr(kern, dev.device, smem, attr_done)) return TPMLP_ERR_CUDA;
     const int grid = k.num_tiles < dev.sm_count ? k.num_tiles : dev.sm_count;
-    kern<<<grid, tc::NUM_THREADS, smem, st>>>(ma, mb, k);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(tc::NUM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddep_wait
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, k);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("tcgen05 GEMM launch: %s", cudaGetErrorString(e));
         return TPMLP_ERR_CUDA;
@@ -191,13 +201,15 @@ tpmlp_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
     cfg.blockDim = dim3(tc::NUM_THREADS);
     cfg.dynamicSmemBytes = tc::PairGeom<STAGED>::smem_bytes;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddep_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mo, mo2, k);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {

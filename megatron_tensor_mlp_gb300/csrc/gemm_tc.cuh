@@ -412,6 +412,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Set-up above overlaps the previous launch's tail; no global memory is touched before
+    // the previous grid has completed.
+    griddep_wait();
+    if (threadIdx.x == 0) griddep_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -770,6 +774,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     cluster_sync_all();  // the peer may signal the leader's barriers from here on
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Set-up above overlaps the previous launch's tail; no global memory is touched before
+    // the previous grid has completed.
+    griddep_wait();
+    if (threadIdx.x == 0) griddep_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {

@@ -263,6 +263,14 @@ __device__ __forceinline__ void bulk_wait_group_read() {
 // Wait until all of this thread's committed bulk groups have completed (writes performed).
 __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Programmatic dependent launch.  wait: block until the grid this launch depends on has
+// completed and its memory operations are visible (a no-op without such a dependency).
+// launch_dependents: let the next launch in the stream start its CTAs (they still wait).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Busy-wait for about `ns` nanoseconds.
 __device__ __forceinline__ void spin_ns(uint64_t ns) {
     const uint64_t t0 = globaltimer_ns();
