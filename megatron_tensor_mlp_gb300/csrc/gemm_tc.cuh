@@ -5,15 +5,23 @@
 //   D_s[M,N] = A_s[M,K] B_s[K,N]           (batched over shards s), or
 //   D  [M,N] = sum_s A_s[M,K] B_s[K,N]     (shard sum inside the K loop)
 //
-// CTA layout (384 threads, one CTA per SM, persistent over output tiles):
-//   warp 0        TMA producer: fills a STAGES-deep ring of (A, B) tiles
-//   warp 1        TMEM allocator + MMA issuer (one thread): 4 x (128x256x16)
-//                 UMMAs per 64-wide K block into one of two 256-column
-//                 fp32 accumulators (double buffered across tiles)
+// Two kernels share one structure: gemm_pair_kernel (a cluster of two CTAs,
+// 256x256 tiles with tcgen05.mma.cta_group::2; the main path) and gemm_kernel
+// (one CTA, 128x256 or 128x128 tiles; GEMMs too small to fill the GPU with
+// pair tiles).  CTA layout (384 threads, one CTA per SM, persistent over
+// output tiles):
+//   warp 0        TMA producer: fills a ring of (A, B) stages
+//   warp 1        TMEM allocator + MMA issuer (one thread): 4 UMMAs per
+//                 64-wide K block into one of two fp32 accumulators
+//                 (double buffered across tiles)
 //   warps 2-3     idle
 //   warps 4-11    epilogue: tcgen05.ld 32 columns at a time, fused
-//                 bias / GeLU / GeLU' / conversion, vectorised global stores;
+//                 bias / GeLU / GeLU' / conversion, then either 16-byte
+//                 global stores per row or (pair kernel, short K loops)
+//                 swizzled shared-memory boxes written with TMA stores;
 //                 warp w reads TMEM lanes 32*(w%4).. and column half (w-4)/4.
+// Every wait on an mbarrier is bounded (a status word records a timeout).
+// Set-up runs before griddepcontrol.wait, so it overlaps the previous launch.
 //
 // Shared-memory operand layouts are the canonical 128-byte-swizzled ones:
 //   K-major tile  : rows of 64 K-elements (128 B), 8-row atoms of 1 KiB,
