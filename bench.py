@@ -325,6 +325,45 @@ def time_other_configs(stream, explicit_warmup):
     return out
 
 
+def time_torch_context(stream, explicit_warmup):
+    """Context only: the same fwd+bwd block at the bench workload written with plain PyTorch
+    ops on the same GPU -- unsharded torch.matmul (cuBLAS, bf16 in / fp32 accumulate / bf16
+    out), bias adds, erf-GeLU and its derivative as separate elementwise kernels -- timed
+    like the main line.  Weight gradients come out in bf16 here (fp32 in tpmlp)."""
+    import torch
+    from megatron_tensor_mlp_gb300 import synth
+    wl = synth.WORKLOADS[MAIN_WORKLOAD]
+    M, h, f = wl.M, wl.h, wl.ffn
+    bf = torch.bfloat16
+    gen = lambda sid, shp, sig: torch.from_numpy(  # noqa: E731
+        synth.normal(wl.seed, sid, shp, sig, "bf16").view("int16")).view(bf).cuda()
+    X, A, B, dZ = gen(1, (M, h), 1.0), gen(2, (h, f), 0.02), gen(3, (f, h), 0.02), gen(6, (M, h), 1.0)
+    b1, b2 = torch.zeros(f, dtype=bf, device="cuda"), torch.zeros(h, dtype=bf, device="cuda")
+    inv_sqrt_2pi = 0.3989422804014327
+
+    def step():
+        H = torch.addmm(b1, X, A)
+        Y = torch.nn.functional.gelu(H)
+        torch.addmm(b2, Y, B)
+        dY = dZ @ B.t()
+        Hf = H.float()
+        dH = (dY.float() * (torch.special.ndtr(Hf) + Hf * torch.exp(-0.5 * Hf * Hf) * inv_sqrt_2pi)).to(bf)
+        Y.t() @ dZ
+        X.t() @ dH
+        dH @ A.t()
+        dH.sum(0, dtype=torch.float32)
+        dZ.sum(0, dtype=torch.float32)
+
+    ms, n = settled_ms(step, stream, explicit_warmup, seconds=1.0)  # torch ops run on `stream` (current)
+    flops = wl.fwd_flops() + wl.bwd_flops()
+    out = {"workload": wl.name, "fwd_bwd_ms": round(ms, 4), "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1),
+           "steps": n, "what": "torch.matmul (cuBLAS) + unfused bias / erf-GeLU / GeLU' / column sums, "
+                               "one unsharded GPU; context, not a target"}
+    del X, A, B, dZ
+    torch.cuda.empty_cache()
+    return out
+
+
 def time_next_rows(stream, steps, peaks, explicit_warmup=None):
     """Forward+backward timings of the widened rows at the fwd+bwd workload's sizes
     (s=2048, b=4, h=5120, p=4): the SwiGLU block (ffn=20480 per branch) and the attention
@@ -612,6 +651,20 @@ def run_gpu(args):
         torch.cuda.empty_cache()
         next_rows = time_next_rows(stream, K, peaks, args.warmup)
 
+    torch_context = None
+    if not args.no_next_rows and args.workload == MAIN_WORKLOAD:
+        torch_context = time_torch_context(stream, args.warmup)
+
+    props = torch.cuda.get_device_properties(local)
+    device = {"name": props.name, "sm_count": props.multi_processor_count, "cc": f"{props.major}.{props.minor}",
+              "torch": torch.__version__, "cuda_runtime": torch.version.cuda}
+    try:
+        r = subprocess.run(["nvidia-smi", "-i", str(local), "--query-gpu=driver_version", "--format=csv,noheader"],
+                           capture_output=True, text=True, timeout=20)
+        device["driver"] = r.stdout.strip() or None
+    except (OSError, subprocess.SubprocessError):
+        device["driver"] = None
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         sample = OracleSample(wl)
@@ -632,7 +685,7 @@ def run_gpu(args):
                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                "gpu_launches": launches_per_step * K, "clocks": clocks,
                "fwd_pages_sizing": fwd_pages, "next_rows": next_rows,
-               "other_configs": other_configs}
+               "other_configs": other_configs, "context_torch": torch_context, "device": device}
         print(json.dumps(out), flush=True)
     if ws > 1:
         import torch.distributed as dist
