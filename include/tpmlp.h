@@ -28,7 +28,10 @@
  *     synchronises inside these calls; workspaces are passed in with the sizes
  *     stated.  Calls are stream ordered and asynchronous: they return after
  *     the kernels are enqueued on `stream` (a cudaStream_t; NULL = legacy
- *     default stream).
+ *     default stream).  The GEMM kernels are launched with programmatic
+ *     dependent launch: their set-up may overlap the end of the preceding
+ *     kernel in the stream, but they touch no global memory before that
+ *     kernel has completed, so stream order holds as for any launch.
  *   Validation.  Arguments are checked on the host before anything is
  *     enqueued, in this order: NULL pointers (TPMLP_ERR_NULL), shapes
  *     (TPMLP_ERR_SHAPE: s, b >= 0; h, ffn, p >= 1; sizes below 2^31 rows),
