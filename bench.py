@@ -77,20 +77,27 @@ def job_throughput(units_per_step_per_rank: float, world: int, slowest_ms_per_st
     return units_per_step_per_rank * world / (slowest_ms_per_step * 1e-3)
 
 
-def kernel_code_digest():
-    """sha256 of the GEMM kernel sources with comments and blank space removed, so that the
-    committed DRAM capture stays valid across comment-only edits but not across code edits."""
+def code_digest(texts):
+    """sha256 of source texts with comments and blank space removed."""
     import hashlib
     import re
     h = hashlib.sha256()
-    for f in ("gemm_tc.cuh", "gemm_tc.cu", "ptx.cuh"):
-        with open(os.path.join(ROOT, "megatron_tensor_mlp_gb300", "csrc", f)) as fh:
-            text = fh.read()
+    for text in texts:
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
         lines = [" ".join(line.split()) for line in text.splitlines()]
         h.update("\n".join(line for line in lines if line).encode())
     return h.hexdigest()
+
+
+def kernel_code_digest():
+    """Digest of the GEMM kernel sources (code_digest), so that the committed DRAM capture stays
+    valid across comment-only edits but not across code edits."""
+    texts = []
+    for f in ("gemm_tc.cuh", "gemm_tc.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "megatron_tensor_mlp_gb300", "csrc", f)) as fh:
+            texts.append(fh.read())
+    return code_digest(texts)
 
 
 def captured_traffic(kernel_key):

@@ -1,0 +1,35 @@
+"""Host-side helpers of the benchmark (CPU only)."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_code_digest_ignores_comments_and_blank_space():
+    a = "int f(int x) {\n    return x + 1;  // add one\n}\n"
+    b = "/* header */\nint f(int x) {\n\n        return x + 1;\n}   // trailing\n"
+    assert bench.code_digest([a]) == bench.code_digest([b])
+
+
+def test_code_digest_follows_code_changes():
+    a = "int f(int x) { return x + 1; }\n"
+    b = "int f(int x) { return x + 2; }\n"
+    assert bench.code_digest([a]) != bench.code_digest([b])
+    # file boundaries and order matter
+    assert bench.code_digest([a, b]) != bench.code_digest([b, a])
+
+
+def test_captured_traffic_matches_committed_kernel():
+    """The committed DRAM capture names the kernel code it was taken on; the bench reports its
+    bytes only for that code (None otherwise)."""
+    v = bench.captured_traffic("row_fwd")
+    path = os.path.join(ROOT, "profiles", "dram_traffic_s2048_b4_h5120_ffn20480_p4.txt")
+    recorded = [line.split()[1] for line in open(path) if line.startswith("kernel_code_sha256")]
+    assert len(recorded) == 1
+    if recorded[0] == bench.kernel_code_digest():
+        assert isinstance(v, int) and v > 0
+    else:
+        assert v is None
