@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-fwd-pages", action="store_true")
     ap.add_argument("--no-next-rows", action="store_true", help="skip the SwiGLU / attention-projection timings")
     ap.add_argument("--e2e-steps", type=int, default=60)
+    ap.add_argument("--bwd", action="store_true",
+                    help="run forward + backward on a forward-only workload (for profiling its backward GEMMs)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     return ap.parse_args()
 
@@ -459,6 +461,9 @@ def run_gpu(args):
 
     peaks, peak_kind = load_peaks()
     wl = synth.WORKLOADS[args.workload]
+    if args.bwd and not wl.backward:
+        import dataclasses
+        wl = dataclasses.replace(wl, backward=True, name=wl.name.replace("-fwd ", "-fwd-bwd "))
     buf = harness.MLPBuffers(wl)
     s, b, h, f, p = buf.dims()
     M = wl.M
