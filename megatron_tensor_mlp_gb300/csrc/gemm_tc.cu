@@ -306,6 +306,24 @@ tpmlp_status launch_tc_gemm(const Operand& a, const Operand& b, const GemmSpec& 
     k.aux_ss = g.aux_ss;
     k.status = dev.status;
     k.timeout_ns = 2000000000ull;  // 2 s per wait
+    {
+        // 32-byte epilogue accesses need every row of out, out2 and aux to start on a 32-byte
+        // boundary: base address, row pitch and shard stride all multiples of 32 bytes (the
+        // column offsets inside a row are multiples of 32 elements).
+        const int64_t shards = g.sum_shards ? 1 : g.n_shards;
+        auto rows32 = [shards](const void* ptr, int64_t ld, int64_t ss, int64_t es) {
+            if (ptr == nullptr) return true;
+            return reinterpret_cast<uintptr_t>(ptr) % 32 == 0 && (ld * es) % 32 == 0 &&
+                   (shards <= 1 || (ss * es) % 32 == 0);
+        };
+        const int64_t es_out = g.out_f32 ? 4 : 2;
+        const int64_t es_out2 = g.epi == EPI_SWIGLU ? 4 : 2;  // fp32 SwiGLU pre-activations, else bf16 H
+        const int64_t es_aux = g.epi == EPI_DSWIGLU ? 4 : 2;
+        k.st32 = rows32(g.out, g.out_ld, g.out_ss, es_out) && rows32(g.out2, g.out2_ld, g.out2_ss, es_out2) &&
+                         rows32(g.aux, g.aux_ld, g.aux_ss, es_aux)
+                     ? 1
+                     : 0;
+    }
     if (k.num_tiles == 0) return TPMLP_OK;
 
     const bool amn = a.mn_major, bmn = b.mn_major;

@@ -66,6 +66,7 @@ struct KArgs {
     int m_blocks, n_blocks, batch, num_tiles, kb_per_shard, k_iters, group_m;
     int act, out_f32;
     int a_chunked, b_chunked;  // MN-major operand loaded with one 4-D box per stage (MN extent % 64 == 0)
+    int st32;                  // out, out2 and aux rows are 32-byte aligned: 32-byte global accesses
     void* out; long long out_ld, out_ss;
     void* out2; long long out2_ld, out2_ss;
     const void* bias; long long bias_ss;
@@ -196,8 +197,45 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* f) {
     }
 }
 
-// Store 32 values (nvalid is a multiple of 8) as bf16.
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v, int nvalid) {
+// 32-byte global accesses (Blackwell): half as many store / load instructions per row as
+// 16-byte ones, so the epilogue puts half as many requests through the SM's load/store
+// data pipe, which the tensor cores' shared-memory operand reads also use.  Addresses must
+// be 32-byte aligned (KArgs::st32).
+__device__ __forceinline__ void st_v8(void* p, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
+                                      uint32_t a5, uint32_t a6, uint32_t a7) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0), "r"(a1), "r"(a2),
+                 "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+                 : "memory");
+}
+__device__ __forceinline__ void ld_v8(const void* p, uint32_t (&w)[8]) {
+    asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(p)
+                 : "memory");
+}
+
+// Store 32 values (nvalid is a multiple of 8) as bf16: with st32 in 32-byte groups of 16
+// (a trailing group of 8 as one 16-byte store), else in 16-byte groups of 8.
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v, int nvalid, bool st32) {
+    if (st32) {
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            const float* w = v + g * 16;
+            if ((g + 1) * 16 <= nvalid) {
+                st_v8(dst + g * 16, pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]),
+                      pack_bf16x2(w[6], w[7]), pack_bf16x2(w[8], w[9]), pack_bf16x2(w[10], w[11]),
+                      pack_bf16x2(w[12], w[13]), pack_bf16x2(w[14], w[15]));
+            } else if (g * 16 < nvalid) {
+                uint4 u;
+                u.x = pack_bf16x2(w[0], w[1]);
+                u.y = pack_bf16x2(w[2], w[3]);
+                u.z = pack_bf16x2(w[4], w[5]);
+                u.w = pack_bf16x2(w[6], w[7]);
+                *reinterpret_cast<uint4*>(dst + g * 16) = u;
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
         if (g * 8 < nvalid) {
@@ -210,13 +248,49 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v
         }
     }
 }
-__device__ __forceinline__ void store_f32x32(float* dst, const float* v, int nvalid) {
+// Store 32 fp32 values (nvalid is a multiple of 4): 32-byte groups of 8 with st32, else 16-byte.
+__device__ __forceinline__ void store_f32x32(float* dst, const float* v, int nvalid, bool st32) {
+    if (st32) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const float* w = v + g * 8;
+            if ((g + 1) * 8 <= nvalid) {
+                st_v8(dst + g * 8, __float_as_uint(w[0]), __float_as_uint(w[1]), __float_as_uint(w[2]),
+                      __float_as_uint(w[3]), __float_as_uint(w[4]), __float_as_uint(w[5]), __float_as_uint(w[6]),
+                      __float_as_uint(w[7]));
+            } else if (g * 8 < nvalid) {
+                *reinterpret_cast<float4*>(dst + g * 8) = make_float4(w[0], w[1], w[2], w[3]);
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int g = 0; g < 8; ++g) {
         if (g * 4 < nvalid) {
             *reinterpret_cast<float4*>(dst + g * 4) = make_float4(v[g * 4], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]);
         }
     }
+}
+// Load 32 bf16 values of a row (nvalid a multiple of 8) widened to fp32; values past nvalid
+// are left untouched.
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* f, int nvalid, bool st32) {
+    if (st32) {
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            if ((g + 1) * 16 <= nvalid) {
+                uint32_t w[8];
+                ld_v8(src + g * 16, w);
+                unpack_bf16x8(make_uint4(w[0], w[1], w[2], w[3]), f + g * 16);
+                unpack_bf16x8(make_uint4(w[4], w[5], w[6], w[7]), f + g * 16 + 8);
+            } else if (g * 16 < nvalid) {
+                unpack_bf16x8(*reinterpret_cast<const uint4*>(src + g * 16), f + g * 16);
+            }
+        }
+        return;
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+        if (g * 8 < nvalid) unpack_bf16x8(*reinterpret_cast<const uint4*>(src + g * 8), f + g * 8);
 }
 
 template <int EPI>
@@ -242,31 +316,28 @@ __device__ __forceinline__ void epilogue_chunk(const KArgs& p, const uint32_t (&
         }
         if (p.out2 != nullptr) {
             __nv_bfloat16* d2 = static_cast<__nv_bfloat16*>(p.out2) + shard * p.out2_ss + (long long)gm * p.out2_ld + gn0;
-            store_bf16x32(d2, v, nvalid);
+            store_bf16x32(d2, v, nvalid, p.st32);
         }
         if (p.act == TPMLP_ACT_GELU_ERF) gelu_inplace32(v);
         __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.out) + shard * p.out_ss + (long long)gm * p.out_ld + gn0;
-        store_bf16x32(d, v, nvalid);
+        store_bf16x32(d, v, nvalid, p.st32);
     } else if constexpr (EPI == EPI_DGELU) {
         const __nv_bfloat16* hp =
             static_cast<const __nv_bfloat16*>(p.aux) + shard * p.aux_ss + (long long)gm * p.aux_ld + gn0;
+        float hv[32];
+        load_bf16x32(hp, hv, nvalid, p.st32);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            if (g * 8 < nvalid) {
-                float hv[8];
-                unpack_bf16x8(*reinterpret_cast<const uint4*>(hp + g * 8), hv);
-                dgelu_mul8(v + g * 8, hv);
-            }
-        }
+        for (int g = 0; g < 4; ++g)
+            if (g * 8 < nvalid) dgelu_mul8(v + g * 8, hv + g * 8);
         __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.out) + shard * p.out_ss + (long long)gm * p.out_ld + gn0;
-        store_bf16x32(d, v, nvalid);
+        store_bf16x32(d, v, nvalid, p.st32);
     } else {
         if (p.out_f32) {
             float* d = static_cast<float*>(p.out) + shard * p.out_ss + (long long)gm * p.out_ld + gn0;
-            store_f32x32(d, v, nvalid);
+            store_f32x32(d, v, nvalid, p.st32);
         } else {
             __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.out) + shard * p.out_ss + (long long)gm * p.out_ld + gn0;
-            store_bf16x32(d, v, nvalid);
+            store_bf16x32(d, v, nvalid, p.st32);
         }
     }
 }
@@ -299,14 +370,14 @@ __device__ __forceinline__ void swiglu_chunk(const KArgs& p, const uint32_t (&rg
     }
     if (p.out2 != nullptr) {  // fp32 pre-activations: the backward multiplies by u itself
         float* d2 = static_cast<float*>(p.out2) + shard * p.out2_ss + (long long)gm * p.out2_ld + pg;
-        store_f32x32(d2, g, 32);
-        store_f32x32(d2 + 128, u, 32);
+        store_f32x32(d2, g, 32, p.st32);
+        store_f32x32(d2 + 128, u, 32, p.st32);
     }
 #pragma unroll
     for (int j = 0; j < 32; ++j) g[j] = g[j] * sigmoid_approx(g[j]) * u[j];
     __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.out) + shard * p.out_ss + (long long)gm * p.out_ld +
                        (long long)nb * 128 + fo;
-    store_bf16x32(d, g, 32);
+    store_bf16x32(d, g, 32, p.st32);
 }
 
 // SwiGLU dgrad: acc = dY for features f0..f0+31; packed fp32 (g, u) pre-activations from aux,
@@ -316,22 +387,37 @@ __device__ __forceinline__ void dswiglu_chunk(const KArgs& p, const uint32_t (&r
     const long long pg = (long long)(f0 >> 7) * 256 + (f0 & 127);
     const float* hp = static_cast<const float*>(p.aux) + shard * p.aux_ss + (long long)gm * p.aux_ld + pg;
     __nv_bfloat16* op = static_cast<__nv_bfloat16*>(p.out) + shard * p.out_ss + (long long)gm * p.out_ld + pg;
-    float dg[32], du[32];
+    float gv[32], uv[32];
+    if (p.st32) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const float4 g4 = *reinterpret_cast<const float4*>(hp + q * 4);
-        const float4 u4 = *reinterpret_cast<const float4*>(hp + 128 + q * 4);
-        const float g[4] = {g4.x, g4.y, g4.z, g4.w}, u[4] = {u4.x, u4.y, u4.z, u4.w};
+        for (int q = 0; q < 4; ++q) {
+            uint32_t w[8];
+            ld_v8(hp + q * 8, w);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float dy = __uint_as_float(r[q * 4 + i]);
-            const float sg = sigmoid_approx(g[i]);
-            dg[q * 4 + i] = dy * u[i] * (sg * (1.0f + g[i] * (1.0f - sg)));
-            du[q * 4 + i] = dy * g[i] * sg;
+            for (int i = 0; i < 8; ++i) gv[q * 8 + i] = __uint_as_float(w[i]);
+            ld_v8(hp + 128 + q * 8, w);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) uv[q * 8 + i] = __uint_as_float(w[i]);
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 g4 = *reinterpret_cast<const float4*>(hp + q * 4);
+            const float4 u4 = *reinterpret_cast<const float4*>(hp + 128 + q * 4);
+            gv[q * 4 + 0] = g4.x; gv[q * 4 + 1] = g4.y; gv[q * 4 + 2] = g4.z; gv[q * 4 + 3] = g4.w;
+            uv[q * 4 + 0] = u4.x; uv[q * 4 + 1] = u4.y; uv[q * 4 + 2] = u4.z; uv[q * 4 + 3] = u4.w;
         }
     }
-    store_bf16x32(op, dg, 32);
-    store_bf16x32(op + 128, du, 32);
+    float dg[32], du[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float dy = __uint_as_float(r[j]);
+        const float sg = sigmoid_approx(gv[j]);
+        dg[j] = dy * uv[j] * (sg * (1.0f + gv[j] * (1.0f - sg)));
+        du[j] = dy * gv[j] * sg;
+    }
+    store_bf16x32(op, dg, 32, p.st32);
+    store_bf16x32(op + 128, du, 32, p.st32);
 }
 
 // One tile's epilogue for this warp: TMEM lane quarter q, column half `half`.
@@ -668,14 +754,11 @@ __device__ __forceinline__ void epilogue_tile_staged(const KArgs& p, const CUten
             if (gm < p.M) {
                 const __nv_bfloat16* hp =
                     static_cast<const __nv_bfloat16*>(p.aux) + shard * p.aux_ss + (long long)gm * p.aux_ld + gn0;
+                float hv[32];
+                load_bf16x32(hp, hv, nvalid, p.st32);
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    if (g * 8 < nvalid) {
-                        float hv[8];
-                        unpack_bf16x8(*reinterpret_cast<const uint4*>(hp + g * 8), hv);
-                        dgelu_mul8(v + g * 8, hv);
-                    }
-                }
+                for (int g = 0; g < 4; ++g)
+                    if (g * 8 < nvalid) dgelu_mul8(v + g * 8, hv + g * 8);
             }
             stage_bf16x32(box, lane, v);
         } else {
