@@ -240,6 +240,15 @@ def test_single_cta_tile_widths(env, orc, shape):
         T.tpmlp_set_gemm_mode(0)
 
 
+@pytest.mark.parametrize("shape", [(10, 4, 256, 1024, 16), (6, 5, 512, 2048, 32)], ids=["p16", "p32"])
+def test_many_shards(env, orc, shape, gemm_mode):
+    """More shards than any page sizing uses (p = 16, 32; f/p = 64): the column GEMM has one
+    narrow N-block per shard and the row / dX shard sums run 16-32 shards in one K loop."""
+    _, synth, _ = env
+    wl = synth.custom(*shape, dtype="bf16", sigma_w=0.03, sigma_bias=0.05, seed=sum(shape) + 3)
+    _run_and_check(env, orc, wl)
+
+
 def test_mixed_wave_shape(env, orc):
     """A shape whose row and dX GEMMs have 80 pair tiles (76 pairs fit at once), so the
     last wave holds 4 tiles, which walk K (and the shard sum) backwards; the
