@@ -74,3 +74,41 @@ def test_workload_sampled(env, orc, cfg):
     U.assert_close(harness.to_host(buf.dX[torch.from_numpy(xr).cuda()]), dXr, "bf16", "dX rows")
     for t in (buf.dX, buf.dA_sh, buf.dB_sh):
         assert bool(torch.isfinite(t).all())
+
+
+def test_offsets_past_2_31_elements_sampled(env, orc):
+    """s = 2^17, b = 4 (M = 2^19 tokens), h = 128, ffn = 8192, p = 4: Y, H and dH hold 2^32
+    elements each (8 GB), so element offsets past the first shards exceed 2^31 and every
+    32-bit overflow in index or address arithmetic would show.  Sampled rows and columns, the
+    last rows of the last shard included.  (K of the weight-gradient GEMMs is 2^19 tokens:
+    the tensor cores' fp32 accumulation error grows about 1.9e-8 per 16-deep step, 6e-4 here;
+    at 2^21 tokens it alone reaches 2.5e-3 of the 3e-3 bound.)"""
+    import torch
+    harness, synth, T = env
+    wl = synth.custom(1 << 17, 4, 128, 8192, 4, dtype="bf16", sigma_w=0.03, sigma_bias=0.05, seed=2019)
+    buf = harness.MLPBuffers(wl, backward=True)
+    buf.fwd()
+    buf.bwd()
+    T.tpmlp_device_status()
+    M, h, f, p = wl.M, wl.h, wl.ffn, wl.p
+    rng = np.random.default_rng(5)
+    rows = np.array(sorted({0, M // 2, M - 2, M - 1} | set(rng.integers(0, M, 8).tolist())), dtype=np.int64)
+    widen = synth.widen
+    X, A, B = widen(buf.host["X"]), widen(buf.host["A"]), widen(buf.host["B"])
+    b1, b2, dZ = widen(buf.host["b1"]), widen(buf.host["b2"]), widen(buf.host["dZ"])
+    Hr, Yr, Zr = orc.mlp_fwd(X[rows], A, b1, B, b2)
+    ridx = torch.from_numpy(rows).cuda()
+    U.assert_close(harness.to_host(buf.Z[ridx]), Zr, "bf16", "Z rows")
+    U.assert_close(harness.to_host(buf.Y_full()[ridx]), Yr, "bf16", "Y rows")
+    U.assert_close(harness.to_host(buf.H_full()[ridx]), Hr, "bf16", "H rows")
+    fs = f // p
+    cols = np.array([0, fs - 1, fs, 2 * fs + 5, 3 * fs, f - 1], dtype=np.int64)   # shard boundaries
+    dAc, dBr, db1c = orc.bwd_ffn_cols(X, A, b1, B, dZ, cols)
+    cidx = torch.from_numpy(cols).cuda()
+    U.assert_close(harness.to_host(buf.dA_full()[:, cidx]), dAc, "bf16", "dA cols")
+    U.assert_close(harness.to_host(buf.dB_full()[cidx]), dBr, "bf16", "dB rows")
+    U.assert_close(harness.to_host(buf.db1_sh.reshape(-1)[cidx]), db1c, "bf16", "db1")
+    U.assert_close(harness.to_host(buf.db2), orc.bwd_db2(dZ), "bf16", "db2")
+    xr = rows[-4:]
+    U.assert_close(harness.to_host(buf.dX[torch.from_numpy(xr).cuda()]), orc.bwd_dX_rows(X, A, b1, B, dZ, xr),
+                   "bf16", "dX rows")
