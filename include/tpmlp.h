@@ -275,10 +275,14 @@ tpmlp_status tpmlp_debug_wait_timeout(uint32_t timeout_us, void* stream);
  * tiles (128x256, or 128x128 when 128x256 tiles would leave more than half of the
  * SMs idle); CTA-pair tiles store their outputs directly from registers, or, when
  * a tile's K loop is short (at most 40 blocks of 64), through shared memory with
- * TMA stores.  1 = single-CTA tiles only; 2 = CTA-pair tiles only (epilogue chosen
+ * TMA stores; long-K GEMMs run on clusters of two CTA pairs (as in 5) when those
+ * fill their last wave at least 2 points better than single pairs.  1 = single-CTA tiles only; 2 = CTA-pair tiles only (epilogue chosen
  * as in 0); 3 = CTA-pair tiles, direct stores; 4 = CTA-pair tiles, TMA stores (the
- * SwiGLU epilogues always store directly).  Results agree within rounding in every
- * mode; the control exists for tuning and tests.  TPMLP_ERR_SHAPE for other values.
+ * SwiGLU epilogues always store directly); 5 = clusters of two CTA pairs that
+ * compute neighbouring 256-column tiles and share each A tile through TMA
+ * multicast (direct stores; GEMMs with an odd number of 256-column blocks fall back
+ * to 2).  Results agree within rounding in every mode; the control exists for
+ * tuning and tests.  TPMLP_ERR_SHAPE for other values.
  */
 tpmlp_status tpmlp_set_gemm_mode(int mode);
 int tpmlp_get_gemm_mode(void);

@@ -92,7 +92,8 @@ bool make_out_map(CUtensorMap* map, void* ptr, int64_t ld, int64_t ss, uint64_t 
 // main loop takes ~512 cycles per 64-wide K block, a direct-store epilogue ~10-20 k cycles.
 constexpr int kStagedMaxKBlocks = 40;
 
-std::atomic<int> g_gemm_mode{0};  // 0 auto, 1 single-CTA, 2 pair, 3 pair + direct stores, 4 pair + TMA stores
+// 0 auto, 1 single-CTA, 2 pair, 3 pair + direct stores, 4 pair + TMA stores, 5 two pairs per cluster
+std::atomic<int> g_gemm_mode{0};
 std::atomic<int> g_group_m{16};  // M-blocks per raster group
 
 template <typename Kern>
@@ -161,25 +162,25 @@ tpmlp_status launch_single(const CUtensorMap& ma, const CUtensorMap& mb, const t
     return TPMLP_OK;
 }
 
-// Co-resident CTA pairs of the pair kernel on this device (0 if it cannot run).
-template <bool A_MN, bool B_MN, int EPI, bool STAGED>
+// Co-resident clusters (of CL / 2 CTA pairs) of the pair kernel on this device (0 if it cannot run).
+template <bool A_MN, bool B_MN, int EPI, bool STAGED, int CL = 2>
 int pair_capacity(const DeviceInfo& dev) {
     static int cap[64];
     static bool done[64];
     static bool attr_done[64] = {};
     if (dev.device >= 64) return 0;
     if (done[dev.device]) return cap[dev.device];
-    auto kern = tc::gemm_pair_kernel<A_MN, B_MN, EPI, STAGED>;
+    auto kern = tc::gemm_pair_kernel<A_MN, B_MN, EPI, STAGED, CL>;
     constexpr int smem = tc::PairGeom<STAGED>::smem_bytes;
     int n = 0;
     if (set_smem_attr(kern, dev.device, smem, attr_done)) {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2 * (dev.sm_count / 2));
+        cfg.gridDim = dim3(CL * (dev.sm_count / CL));
         cfg.blockDim = dim3(tc::NUM_THREADS);
         cfg.dynamicSmemBytes = smem;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.x = CL;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
@@ -192,18 +193,18 @@ int pair_capacity(const DeviceInfo& dev) {
     return n;
 }
 
-template <bool A_MN, bool B_MN, int EPI, bool STAGED>
+template <bool A_MN, bool B_MN, int EPI, bool STAGED, int CL = 2>
 tpmlp_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
                          const CUtensorMap& mo2, const tc::KArgs& k, int clusters, cudaStream_t st) {
-    auto kern = tc::gemm_pair_kernel<A_MN, B_MN, EPI, STAGED>;
+    auto kern = tc::gemm_pair_kernel<A_MN, B_MN, EPI, STAGED, CL>;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * clusters);
+    cfg.gridDim = dim3(CL * clusters);
     cfg.blockDim = dim3(tc::NUM_THREADS);
     cfg.dynamicSmemBytes = tc::PairGeom<STAGED>::smem_bytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddep_wait
@@ -232,14 +233,33 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
     const bool use_pair = cap > 0 && (mode >= 2 || pair_tiles >= cap);
     constexpr bool kNarrowOk = EPI != EPI_SWIGLU && EPI != EPI_DSWIGLU;  // packed layouts span 256 columns
     const bool narrow = kNarrowOk && !use_pair && 2 * k.num_tiles <= dev.sm_count && g.N > 128;
+    // Two CTA pairs per cluster sharing A (multicast): needs an even number of 256-wide
+    // N-blocks and runs the direct-store epilogue.  Forced by mode 5; chosen automatically
+    // for long K loops when its waves are fuller.  Under the power cap the four-CTA clusters
+    // clock higher but leave 8 of 152 SMs idle, and measured per tile the two tilings cost the
+    // same, so only the fill of the last wave decides (e.g. the row GEMM at 640 pair tiles:
+    // 8.42 waves of 76 pairs against 8.89 waves of 36 clusters).
+    bool quad = false;
+    if (use_pair && k.n_blocks % 2 == 0 && (mode == 5 || (mode == 0 && k.k_iters > kStagedMaxKBlocks))) {
+        const int cap4 = pair_capacity<A_MN, B_MN, EPI, false, 4>(dev);
+        if (cap4 > 0) {
+            const int quad_tiles = pair_tiles / 2;
+            auto fill = [](int tiles, int slots) {
+                const int waves = (tiles + slots - 1) / slots;
+                return static_cast<double>(tiles) / (static_cast<double>(waves) * slots);
+            };
+            quad = mode == 5 || fill(quad_tiles, cap4) >= fill(pair_tiles, cap) + 0.02;
+        }
+    }
     CUtensorMap ma, mb;
     const uint32_t b_rows = (use_pair || narrow) ? tc::BN / 2 : tc::BN;
     // MN-major operands: one 4-D box per stage when the MN extent is a multiple of 64
-    k.a_chunked = (a.mn_major && g.M % 64 == 0) ? 1 : 0;
+    k.a_chunked = (a.mn_major && g.M % 64 == 0 && !quad) ? 1 : 0;
     k.b_chunked = (b.mn_major && g.N % 64 == 0) ? 1 : 0;
+    const uint32_t a_rows = quad ? tc::BM / 2 : tc::BM;  // K-major A box: half a slice per CTA when shared
     bool ok;
     if (k.a_chunked) ok = make_map_chunked(&ma, a, g.M, g.K, tc::BM / 64);
-    else ok = a.mn_major ? make_map(&ma, a, g.M, g.K, 64, tc::BK) : make_map(&ma, a, g.K, g.M, tc::BK, tc::BM);
+    else ok = a.mn_major ? make_map(&ma, a, g.M, g.K, 64, tc::BK) : make_map(&ma, a, g.K, g.M, tc::BK, a_rows);
     if (!ok) return TPMLP_ERR_CUDA;
     if (k.b_chunked) ok = make_map_chunked(&mb, b, g.N, g.K, b_rows / 64);
     else ok = b.mn_major ? make_map(&mb, b, g.N, g.K, 64, tc::BK) : make_map(&mb, b, g.K, g.N, tc::BK, b_rows);
@@ -256,6 +276,13 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
     }
     k.m_blocks = m_pairs;
     k.num_tiles = pair_tiles;
+    if (quad) {
+        k.n_blocks /= 2;  // the kernel decodes 256x512 blocks; pair q takes N-block 2 nb + q
+        k.num_tiles = m_pairs * k.n_blocks * k.batch;
+        const int cap4 = pair_capacity<A_MN, B_MN, EPI, false, 4>(dev);
+        return launch_pair<A_MN, B_MN, EPI, false, 4>(ma, mb, ma, ma, k, k.num_tiles < cap4 ? k.num_tiles : cap4,
+                                                      st);
+    }
     const int clusters = pair_tiles < cap ? pair_tiles : cap;
     // Short K loops (a tile's main loop shorter than a direct-store epilogue): staged epilogue.
     if constexpr (kNarrowOk) {

@@ -717,9 +717,9 @@ const char* tpmlp_last_error(void) { return t_err; }
 int tpmlp_version(void) { return 100; }
 
 tpmlp_status tpmlp_set_gemm_mode(int mode) {
-    if (mode < 0 || mode > 4) {
+    if (mode < 0 || mode > 5) {
         set_error("gemm mode must be 0 (automatic), 1 (single-CTA tiles), 2 (CTA-pair tiles), 3 (CTA-pair tiles, "
-                  "direct stores) or 4 (CTA-pair tiles, TMA stores)");
+                  "direct stores), 4 (CTA-pair tiles, TMA stores) or 5 (two CTA pairs per cluster sharing A)");
         return TPMLP_ERR_SHAPE;
     }
     set_gemm_mode(mode);

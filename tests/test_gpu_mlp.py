@@ -17,9 +17,10 @@ def env():
     return harness, synth, tpmlp
 
 
-@pytest.fixture(params=[1, 3, 4], ids=["single-cta", "pair-direct", "pair-staged"])
+@pytest.fixture(params=[1, 3, 4, 5], ids=["single-cta", "pair-direct", "pair-staged", "two-pairs"])
 def gemm_mode(request, env):
-    """Force 128x256 single-CTA tiles or 256x256 CTA-pair tiles for the test."""
+    """Force 128x256 single-CTA tiles, 256x256 CTA-pair tiles (either epilogue), or clusters of
+    two CTA pairs sharing A by multicast (GEMMs with an even number of 256-wide N-blocks)."""
     T = env[2]
     T.tpmlp_set_gemm_mode(request.param)
     yield request.param
@@ -214,14 +215,14 @@ def test_single_and_pair_tiles_agree(env, orc):
     wl = synth.custom(150, 4, 384, 1536, 3, dtype="bf16", seed=9)
     buf = harness.MLPBuffers(wl, backward=True)
     out = {}
-    for mode in (1, 2, 3, 4):
+    for mode in (1, 2, 3, 4, 5):
         T.tpmlp_set_gemm_mode(mode)
         buf.fwd()
         buf.bwd()
         T.tpmlp_device_status()
         out[mode] = [t.clone() for t in (buf.Z, buf.Y, buf.H, buf.dX, buf.dA_sh, buf.dB_sh, buf.dH)]
     T.tpmlp_set_gemm_mode(0)
-    for mode in (2, 3, 4):
+    for mode in (2, 3, 4, 5):
         for a, b_ in zip(out[1], out[mode]):
             assert torch.equal(a, b_), mode
 
@@ -258,7 +259,7 @@ def test_mixed_wave_shape(env, orc):
     _run_and_check(env, orc, wl)
 
 
-@pytest.mark.parametrize("mode", [3, 4], ids=["pair-direct", "pair-staged"])
+@pytest.mark.parametrize("mode", [3, 4, 5], ids=["pair-direct", "pair-staged", "two-pairs"])
 def test_every_gemm_two_waves(env, orc, mode):
     """All six GEMMs with more pair tiles than co-resident pairs (80 to 100 tiles), so
     every GEMM has second-wave tiles that walk K backwards: the batched column, dH,
@@ -268,6 +269,21 @@ def test_every_gemm_two_waves(env, orc, mode):
     T.tpmlp_set_gemm_mode(mode)
     try:
         wl = synth.custom(512, 4, 2560, 2560, 2, dtype="bf16", sigma_w=0.02, sigma_bias=0.05, seed=78)
+        _run_and_check(env, orc, wl)
+    finally:
+        T.tpmlp_set_gemm_mode(0)
+
+
+def test_two_pair_clusters_every_gemm(env, orc):
+    """Clusters of two CTA pairs in all six GEMMs: every GEMM has an even number of 256-wide
+    N-blocks with a ragged last one (h = 1800: 8 blocks, f/p = 1480: 6 blocks), ragged M and K
+    (M = 2400, K = 1800, 1480 per shard, 2400), and 40-60 256x512 cluster tiles, more than the
+    36 co-resident clusters, so second-wave tiles walk K (and the shard sums) backwards while
+    both pairs of a cluster share every A tile."""
+    _, synth, T = env
+    T.tpmlp_set_gemm_mode(5)
+    try:
+        wl = synth.custom(600, 4, 1800, 2960, 2, dtype="bf16", sigma_w=0.02, sigma_bias=0.05, seed=79)
         _run_and_check(env, orc, wl)
     finally:
         T.tpmlp_set_gemm_mode(0)
