@@ -296,6 +296,18 @@ int tpmlp_get_gemm_mode(void);
 tpmlp_status tpmlp_set_gemm_raster(int group_m);
 int tpmlp_get_gemm_raster(void);
 
+/*
+ * Longest contraction, in blocks of 64, that one GEMM launch accumulates in the tensor
+ * cores, process wide.  The tensor cores' fp32 accumulation error grows about linearly
+ * with the number of MMA steps, so GEMMs with an fp32 output and a longer K (the weight
+ * gradients dA, dB and the projections' dW over more tokens than 64 * k_blocks) run as
+ * one launch per K chunk, each later one adding its partial product to the fp32 output
+ * (deterministic order).  Default 4096 (262144 tokens); 0 restores it; 1..2^24, else
+ * TPMLP_ERR_SHAPE.  bf16-output GEMMs are never split.
+ */
+tpmlp_status tpmlp_set_k_chunk(int k_blocks);
+int tpmlp_get_k_chunk(void);
+
 /* Human-readable name of a status code. */
 const char* tpmlp_status_string(tpmlp_status st);
 

@@ -95,6 +95,9 @@ constexpr int kStagedMaxKBlocks = 40;
 // 0 auto, 1 single-CTA, 2 pair, 3 pair + direct stores, 4 pair + TMA stores, 5 two pairs per cluster
 std::atomic<int> g_gemm_mode{0};
 std::atomic<int> g_group_m{16};  // M-blocks per raster group
+// K blocks per launch of a split fp32 contraction (see launch_tc_gemm)
+constexpr int kDefaultKChunkBlocks = 4096;
+std::atomic<int> g_k_chunk_blocks{kDefaultKChunkBlocks};
 
 template <typename Kern>
 bool set_smem_attr(Kern kern, int device, int bytes, bool* done) {
@@ -286,7 +289,8 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
     const int clusters = pair_tiles < cap ? pair_tiles : cap;
     // Short K loops (a tile's main loop shorter than a direct-store epilogue): staged epilogue.
     if constexpr (kNarrowOk) {
-        const bool staged = mode == 4 || (mode != 3 && k.k_iters <= kStagedMaxKBlocks);
+        // (TMA stores overwrite: a launch that adds to its output stores directly)
+        const bool staged = !k.accumulate && (mode == 4 || (mode != 3 && k.k_iters <= kStagedMaxKBlocks));
         if (staged && pair_capacity<A_MN, B_MN, EPI, true>(dev) >= clusters) {
             CUtensorMap mo, mo2 = ma;
             const uint64_t oshards = static_cast<uint64_t>(k.batch);
@@ -299,11 +303,10 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
     return launch_pair<A_MN, B_MN, EPI, false>(ma, mb, ma, ma, k, clusters, st);
 }
 
-}  // namespace
-
-tpmlp_status launch_tc_gemm(const Operand& a, const Operand& b, const GemmSpec& g, const DeviceInfo& dev,
-                            cudaStream_t st) {
+tpmlp_status launch_one(const Operand& a, const Operand& b, const GemmSpec& g, const DeviceInfo& dev,
+                        cudaStream_t st, bool accumulate) {
     tc::KArgs k{};
+    k.accumulate = accumulate ? 1 : 0;
     k.M = static_cast<int>(g.M);
     k.N = static_cast<int>(g.N);
     k.K = static_cast<int>(g.K);
@@ -363,6 +366,41 @@ tpmlp_status launch_tc_gemm(const Operand& a, const Operand& b, const GemmSpec& 
     set_error("internal: no tcgen05 GEMM variant for epi=%d a_mn=%d b_mn=%d", g.epi, (int)amn, (int)bmn);
     return TPMLP_ERR_CUDA;
 }
+
+// The operand with its K origin moved to element k0 (K-major: a column offset; MN-major: a row
+// offset).  bf16 operands only.
+Operand shift_k(Operand o, int64_t k0) {
+    o.ptr = static_cast<const char*>(o.ptr) + (o.mn_major ? k0 * o.ld : k0) * 2;
+    return o;
+}
+
+}  // namespace
+
+// The tensor cores' fp32 accumulation loses accuracy roughly in proportion to the number of
+// 16-deep MMA steps it chains (measured: rel. Frobenius error 1.5e-4 at 2^13 steps, 2.5e-3 at
+// 2^17), so an fp32-output contraction longer than the K chunk (default 4096 blocks of 64:
+// the weight gradients of more than 262144 tokens) runs as one launch per K chunk: the first
+// stores, each later one adds its partial product to the output in its epilogue (in fp32,
+// rounded to nearest).  Each launch waits for the previous one's writes (griddepcontrol.wait
+// before any global access), and the chunk order is fixed, so results stay deterministic.
+tpmlp_status launch_tc_gemm(const Operand& a, const Operand& b, const GemmSpec& g, const DeviceInfo& dev,
+                            cudaStream_t st) {
+    const int64_t chunk = static_cast<int64_t>(g_k_chunk_blocks.load(std::memory_order_relaxed)) * tc::BK;
+    if (g.epi != EPI_STORE || !g.out_f32 || g.sum_shards || g.K <= chunk)
+        return launch_one(a, b, g, dev, st, false);
+    for (int64_t k0 = 0; k0 < g.K; k0 += chunk) {
+        GemmSpec gc = g;
+        gc.K = g.K - k0 < chunk ? g.K - k0 : chunk;
+        const tpmlp_status r = launch_one(shift_k(a, k0), shift_k(b, k0), gc, dev, st, k0 > 0);
+        if (r != TPMLP_OK) return r;
+    }
+    return TPMLP_OK;
+}
+
+void set_k_chunk_blocks(int blocks) {
+    g_k_chunk_blocks.store(blocks > 0 ? blocks : kDefaultKChunkBlocks, std::memory_order_relaxed);
+}
+int get_k_chunk_blocks() { return g_k_chunk_blocks.load(std::memory_order_relaxed); }
 
 void set_gemm_mode(int mode) { g_gemm_mode.store(mode, std::memory_order_relaxed); }
 void set_group_m(int g) { g_group_m.store(g, std::memory_order_relaxed); }

@@ -67,6 +67,7 @@ struct KArgs {
     int act, out_f32;
     int a_chunked, b_chunked;  // MN-major operand loaded with one 4-D box per stage (MN extent % 64 == 0)
     int st32;                  // out, out2 and aux rows are 32-byte aligned: 32-byte global accesses
+    int accumulate;            // EPI_STORE, fp32 out: out += acc (a later K chunk of a split contraction)
     void* out; long long out_ld, out_ss;
     void* out2; long long out2_ld, out2_ss;
     const void* bias; long long bias_ss;
@@ -271,6 +272,37 @@ __device__ __forceinline__ void store_f32x32(float* dst, const float* v, int nva
         }
     }
 }
+// v[j] += src[j] for the first nvalid (a multiple of 4) of 32 fp32 values of a row.
+__device__ __forceinline__ void add_f32x32(const float* src, float* v, int nvalid, bool st32) {
+    if (st32) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            if ((g + 1) * 8 <= nvalid) {
+                uint32_t w[8];
+                ld_v8(src + g * 8, w);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[g * 8 + i] += __uint_as_float(w[i]);
+            } else if (g * 8 < nvalid) {
+                const float4 f = *reinterpret_cast<const float4*>(src + g * 8);
+                v[g * 8 + 0] += f.x;
+                v[g * 8 + 1] += f.y;
+                v[g * 8 + 2] += f.z;
+                v[g * 8 + 3] += f.w;
+            }
+        }
+        return;
+    }
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        if (g * 4 < nvalid) {
+            const float4 f = *reinterpret_cast<const float4*>(src + g * 4);
+            v[g * 4 + 0] += f.x;
+            v[g * 4 + 1] += f.y;
+            v[g * 4 + 2] += f.z;
+            v[g * 4 + 3] += f.w;
+        }
+    }
+}
 // Load 32 bf16 values of a row (nvalid a multiple of 8) widened to fp32; values past nvalid
 // are left untouched.
 __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* f, int nvalid, bool st32) {
@@ -334,6 +366,7 @@ __device__ __forceinline__ void epilogue_chunk(const KArgs& p, const uint32_t (&
     } else {
         if (p.out_f32) {
             float* d = static_cast<float*>(p.out) + shard * p.out_ss + (long long)gm * p.out_ld + gn0;
+            if (p.accumulate) add_f32x32(d, v, nvalid, p.st32);  // the earlier K chunks' sum, in fp32
             store_f32x32(d, v, nvalid, p.st32);
         } else {
             __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.out) + shard * p.out_ss + (long long)gm * p.out_ld + gn0;

@@ -79,6 +79,9 @@ void set_gemm_mode(int mode);
 int get_gemm_mode();
 void set_group_m(int g);
 int get_group_m();
+// K blocks (of 64) per launch of a split fp32-output contraction (see launch_tc_gemm); <= 0 restores the default.
+void set_k_chunk_blocks(int blocks);
+int get_k_chunk_blocks();
 
 
 }  // namespace tpmlp

@@ -739,4 +739,15 @@ tpmlp_status tpmlp_set_gemm_raster(int group_m) {
 
 int tpmlp_get_gemm_raster(void) { return get_group_m(); }
 
+tpmlp_status tpmlp_set_k_chunk(int k_blocks) {
+    if (k_blocks < 0 || k_blocks > (1 << 24)) {
+        set_error("k_blocks must be 0 (default) or in 1..2^24");
+        return TPMLP_ERR_SHAPE;
+    }
+    set_k_chunk_blocks(k_blocks);
+    return TPMLP_OK;
+}
+
+int tpmlp_get_k_chunk(void) { return get_k_chunk_blocks(); }
+
 }  // extern "C"

@@ -49,6 +49,7 @@ _SIGS = {
     "tpmlp_debug_wait_timeout": [_u32, _vp],
     "tpmlp_set_gemm_mode": [_i32],
     "tpmlp_set_gemm_raster": [_i32],
+    "tpmlp_set_k_chunk": [_i32],
 
 }
 for _name, _args in _SIGS.items():
@@ -63,6 +64,8 @@ lib.tpmlp_last_error.argtypes = []
 lib.tpmlp_last_error.restype = ctypes.c_char_p
 lib.tpmlp_get_gemm_raster.argtypes = []
 lib.tpmlp_get_gemm_raster.restype = ctypes.c_int
+lib.tpmlp_get_k_chunk.argtypes = []
+lib.tpmlp_get_k_chunk.restype = ctypes.c_int
 lib.tpmlp_get_gemm_mode.argtypes = []
 lib.tpmlp_get_gemm_mode.restype = ctypes.c_int
 lib.tpmlp_version.argtypes = []
@@ -220,6 +223,14 @@ def tpmlp_set_gemm_raster(group_m, check=True):
 
 def tpmlp_get_gemm_raster() -> int:
     return int(lib.tpmlp_get_gemm_raster())
+
+
+def tpmlp_set_k_chunk(k_blocks, check=True):
+    return _done(lib.tpmlp_set_k_chunk(k_blocks), check)
+
+
+def tpmlp_get_k_chunk() -> int:
+    return int(lib.tpmlp_get_k_chunk())
 
 
 def tpmlp_status_string(st: int) -> str:

@@ -93,6 +93,17 @@ def test_gemm_mode_control():
         assert T.tpmlp_get_gemm_mode() == m
 
 
+def test_k_chunk_control():
+    assert T.tpmlp_set_k_chunk(-1, check=False) == T.ERR_SHAPE
+    assert T.tpmlp_set_k_chunk((1 << 24) + 1, check=False) == T.ERR_SHAPE
+    assert T.tpmlp_get_k_chunk() == 4096
+    for c in (1, 7, 4096):
+        assert T.tpmlp_set_k_chunk(c) == T.OK
+        assert T.tpmlp_get_k_chunk() == c
+    assert T.tpmlp_set_k_chunk(0) == T.OK
+    assert T.tpmlp_get_k_chunk() == 4096
+
+
 def test_qkv_src_col_matches_oracle(orc):
     for (h, n) in [(12, 4), (64, 8), (24, 3), (8, 8), (16, 1)]:
         for c in range(3 * h):

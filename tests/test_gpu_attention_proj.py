@@ -27,8 +27,18 @@ def _bf16(rng_seed, stream, shape, sigma, synth):
     return synth.normal(rng_seed, stream, shape, sigma, "bf16")
 
 
+@pytest.fixture(params=[0, 5], ids=["auto", "two-pairs"])
+def gemm_mode(request, env):
+    """Automatic tiling, or clusters of two CTA pairs wherever a GEMM has an even number of
+    256-wide N-blocks (the h = 384 case: QKV shards and the output projection both 384 wide)."""
+    T = env[2]
+    T.tpmlp_set_gemm_mode(request.param)
+    yield request.param
+    T.tpmlp_set_gemm_mode(0)
+
+
 @pytest.mark.parametrize("s,b,h,n_heads,p", [(25, 8, 256, 8, 4), (50, 3, 384, 6, 3), (16, 4, 512, 16, 8)])
-def test_qkv_and_output_projection(env, orc, s, b, h, n_heads, p):
+def test_qkv_and_output_projection(env, orc, s, b, h, n_heads, p, gemm_mode):
     import torch
     harness, synth, T = env
     M = s * b

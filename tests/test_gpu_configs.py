@@ -112,3 +112,33 @@ def test_offsets_past_2_31_elements_sampled(env, orc):
     xr = rows[-4:]
     U.assert_close(harness.to_host(buf.dX[torch.from_numpy(xr).cuda()]), orc.bwd_dX_rows(X, A, b1, B, dZ, xr),
                    "bf16", "dX rows")
+
+
+def test_two_million_token_weight_gradients_sampled(env, orc):
+    """s = 2^19, b = 4: M = 2^21 tokens, so the weight gradients contract over 32768 blocks of
+    64 tokens.  In one accumulation the tensor cores' fp32 error alone reaches 2.5e-3 (rel.
+    Frobenius) at this length; split into K chunks of 4096 blocks added in fp32 the sampled dA
+    columns and dB rows meet the bf16 bound.  h = 128, ffn = 1024, p = 4 (Y, H, dH 4 GB each)."""
+    import torch
+    harness, synth, T = env
+    assert T.tpmlp_get_k_chunk() == 4096
+    wl = synth.custom(1 << 19, 4, 128, 1024, 4, dtype="bf16", sigma_w=0.03, sigma_bias=0.05, seed=2021)
+    buf = harness.MLPBuffers(wl, backward=True)
+    buf.fwd()
+    buf.bwd()
+    T.tpmlp_device_status()
+    M, f, p = wl.M, wl.ffn, wl.p
+    widen = synth.widen
+    X, A, B = widen(buf.host["X"]), widen(buf.host["A"]), widen(buf.host["B"])
+    b1, b2, dZ = widen(buf.host["b1"]), widen(buf.host["b2"]), widen(buf.host["dZ"])
+    rows = np.array([0, 1, M // 2, M - 1], dtype=np.int64)
+    Hr, Yr, Zr = orc.mlp_fwd(X[rows], A, b1, B, b2)
+    U.assert_close(harness.to_host(buf.Z[torch.from_numpy(rows).cuda()]), Zr, "bf16", "Z rows")
+    fs = f // p
+    cols = np.array([0, fs - 1, fs, 2 * fs + 5, 3 * fs, f - 1], dtype=np.int64)
+    dAc, dBr, db1c = orc.bwd_ffn_cols(X, A, b1, B, dZ, cols)
+    cidx = torch.from_numpy(cols).cuda()
+    U.assert_close(harness.to_host(buf.dA_full()[:, cidx]), dAc, "bf16", "dA cols")
+    U.assert_close(harness.to_host(buf.dB_full()[cidx]), dBr, "bf16", "dB rows")
+    U.assert_close(harness.to_host(buf.db1_sh.reshape(-1)[cidx]), db1c, "bf16", "db1")
+    U.assert_close(harness.to_host(buf.db2), orc.bwd_db2(dZ), "bf16", "db2")

@@ -289,6 +289,31 @@ def test_two_pair_clusters_every_gemm(env, orc):
         T.tpmlp_set_gemm_mode(0)
 
 
+@pytest.mark.parametrize("mode", [1, 3, 5], ids=["single-cta", "pair-direct", "two-pairs"])
+def test_split_contraction(env, orc, mode):
+    """Weight gradients split into K chunks of 64 and 128 tokens (M = 200: four and two
+    launches, the last one ragged), each later launch adding its partial product to the fp32
+    dA / dB: full parity, and within fp32 rounding of the unsplit run (the other outputs are
+    bit-identical: only fp32-output contractions are split)."""
+    import torch
+    harness, synth, T = env
+    T.tpmlp_set_gemm_mode(mode)
+    try:
+        wl = synth.custom(50, 4, 320, 2048, 2, dtype="bf16", sigma_w=0.03, sigma_bias=0.05, seed=80)
+        whole = _run_and_check(env, orc, wl)
+        ref = [t.clone() for t in (whole.Z, whole.dX, whole.dA_sh, whole.dB_sh, whole.dH)]
+        for chunk in (1, 2):
+            T.tpmlp_set_k_chunk(chunk)
+            buf = _run_and_check(env, orc, wl)
+            assert torch.equal(buf.Z, ref[0]) and torch.equal(buf.dX, ref[1]) and torch.equal(buf.dH, ref[4])
+            for got, want in ((buf.dA_sh, ref[2]), (buf.dB_sh, ref[3])):
+                err = (got.double() - want.double()).norm() / want.double().norm()
+                assert float(err) < 1e-6, float(err)
+    finally:
+        T.tpmlp_set_k_chunk(0)
+        T.tpmlp_set_gemm_mode(0)
+
+
 def _random_shapes(n, seed):
     """Random (s, b, h, ffn, p) with h % p == 0, h % 8 == 0 and ffn/p % 8 == 0."""
     rng = np.random.default_rng(seed)
