@@ -714,7 +714,7 @@ const char* tpmlp_status_string(tpmlp_status st) {
 
 const char* tpmlp_last_error(void) { return t_err; }
 
-int tpmlp_version(void) { return 100; }
+int tpmlp_version(void) { return 200; }
 
 tpmlp_status tpmlp_set_gemm_mode(int mode) {
     if (mode < 0 || mode > 5) {

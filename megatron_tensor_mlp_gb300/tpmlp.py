@@ -206,7 +206,8 @@ def tpmlp_debug_wait_timeout(timeout_us, stream=None, check=True):
     return _done(lib.tpmlp_debug_wait_timeout(timeout_us, _stream(stream)), check)
 
 
-GEMM_AUTO, GEMM_SINGLE, GEMM_PAIR = 0, 1, 2
+# tpmlp_set_gemm_mode values
+GEMM_AUTO, GEMM_SINGLE, GEMM_PAIR, GEMM_PAIR_DIRECT, GEMM_PAIR_STAGED, GEMM_TWO_PAIRS = 0, 1, 2, 3, 4, 5
 
 
 def tpmlp_set_gemm_mode(mode, check=True):

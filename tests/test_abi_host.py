@@ -28,7 +28,7 @@ def test_exports_every_declared_symbol():
 
 
 def test_version_and_strings():
-    assert T.tpmlp_version() >= 100
+    assert T.tpmlp_version() >= 200
     for code, name in T.STATUS.items():
         assert T.tpmlp_status_string(code) == name
 
