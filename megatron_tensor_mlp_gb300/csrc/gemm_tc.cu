@@ -179,7 +179,7 @@ int pair_capacity(const DeviceInfo& dev) {
     if (set_smem_attr(kern, dev.device, smem, attr_done)) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(CL * (dev.sm_count / CL));
-        cfg.blockDim = dim3(tc::NUM_THREADS);
+        cfg.blockDim = dim3(tc::PairGeom<STAGED>::threads);
         cfg.dynamicSmemBytes = smem;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -202,7 +202,7 @@ tpmlp_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
     auto kern = tc::gemm_pair_kernel<A_MN, B_MN, EPI, STAGED, CL>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CL * clusters);
-    cfg.blockDim = dim3(tc::NUM_THREADS);
+    cfg.blockDim = dim3(tc::PairGeom<STAGED>::threads);
     cfg.dynamicSmemBytes = tc::PairGeom<STAGED>::smem_bytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];

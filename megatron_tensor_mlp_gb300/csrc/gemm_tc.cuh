@@ -8,18 +8,19 @@
 // Two kernels share one structure: gemm_pair_kernel (a cluster of two CTAs,
 // 256x256 tiles with tcgen05.mma.cta_group::2; the main path) and gemm_kernel
 // (one CTA, 128x256 or 128x128 tiles; GEMMs too small to fill the GPU with
-// pair tiles).  CTA layout (384 threads, one CTA per SM, persistent over
-// output tiles):
+// pair tiles).  CTA layout (384 threads, or 256 for the pair kernel's
+// direct-store variant; one CTA per SM, persistent over output tiles):
 //   warp 0        TMA producer: fills a ring of (A, B) stages
 //   warp 1        TMEM allocator + MMA issuer (one thread): 4 UMMAs per
 //                 64-wide K block into one of two fp32 accumulators
 //                 (double buffered across tiles)
 //   warps 2-3     idle
 //   warps 4-11    epilogue: tcgen05.ld 32 columns at a time, fused
-//                 bias / GeLU / GeLU' / conversion, then either 16-byte
+//                 bias / GeLU / GeLU' / conversion, then either 16/32-byte
 //                 global stores per row or (pair kernel, short K loops)
 //                 swizzled shared-memory boxes written with TMA stores;
-//                 warp w reads TMEM lanes 32*(w%4).. and column half (w-4)/4.
+//                 warp w reads TMEM lanes 32*(w%4).. and column half (w-4)/4
+//                 (pair kernel, direct stores: warps 4-7, both halves).
 // Every wait on an mbarrier is bounded (a status word records a timeout).
 // Set-up runs before griddepcontrol.wait, so it overlaps the previous launch.
 //
@@ -824,8 +825,8 @@ __device__ __forceinline__ void epilogue_tile_staged(const KArgs& p, const CUten
 //                            empty / tmem-full barriers
 //   peer   (r = 1)  warp 0: TMA producer (gated by its own empty barrier)
 //   both            warp 1: TMEM allocation (collective for the pair)
-//                   warps 4-11: epilogue of its 128 rows; the accumulator is
-//                            released by 16 arrivals on the leader's barrier
+//                   warps 4-11 (4-7): epilogue of its 128 rows; the accumulator
+//                            is released by 16 (8) arrivals on the leader's barrier
 //
 // CL = 4 (two pairs per cluster, direct-store epilogue only): pair q = r / 2
 // computes N-block 2 nbs + q of the cluster's 256x512 output block, so both
@@ -842,8 +843,18 @@ constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 
 // STAGED = false: direct-store epilogue, 7 stages.  STAGED = true: staged (TMA-store)
 // epilogue, 6 stages + 8 x 4 KiB staging boxes.
+//
+// Epilogue warps: the staged epilogue (short K loops, where the epilogue sets the pace) runs
+// on 8 warps, two per TMEM lane quarter, each taking one 128-column half of the tile; the
+// direct-store epilogue runs on 4, one per lane quarter, each taking both halves in turn.
+// Its work per tile is the same, spread over twice the time behind a K loop long enough to
+// hide it, and the main loop it overlaps runs ~1 % faster at the power cap (interleaved A/B
+// of the fwd+bwd step, bit-identical results): fewer concurrent epilogue warps leave more of
+// the SM's issue slots and load/store data path to the producer and the UMMA issuer.
 template <bool STAGED>
 struct PairGeom {
+    static constexpr int epi_warps = STAGED ? NUM_EPI_WARPS : 4;
+    static constexpr int threads = 32 * (FIRST_EPI_WARP + epi_warps);
     static constexpr int stages = STAGED ? 6 : 7;
     static constexpr int epi_bytes = STAGED ? NUM_EPI_WARPS * EPI_WARP_BYTES : 0;
     static constexpr int smem_bytes = 1024 + stages * P_STAGE_BYTES + epi_bytes + BAR_BYTES;
@@ -851,7 +862,7 @@ struct PairGeom {
 };
 
 template <bool A_MN, bool B_MN, int EPI, bool STAGED, int CL>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(PairGeom<STAGED>::threads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2,
                      const KArgs p) {
@@ -888,7 +899,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull + a, 1);
-            mbar_init(tempty + a, 2 * NUM_EPI_WARPS);
+            mbar_init(tempty + a, 2 * PairGeom<STAGED>::epi_warps);
         }
         mbar_init(drain, 1);
         fence_mbarrier_init();
@@ -1085,9 +1096,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp >= FIRST_EPI_WARP) {
         // ---------------------------------------------------------------- epilogue (both CTAs)
         const int q = warp & 3;
-        const int half = (warp - FIRST_EPI_WARP) >> 2;
+        [[maybe_unused]] const int half = (warp - FIRST_EPI_WARP) >> 2;  // STAGED only
         const uint32_t tempty_leader0 = mapa_shared(smem_u32(tempty), pleader);
-        uint8_t* ebuf = sE + (warp - FIRST_EPI_WARP) * EPI_WARP_BYTES;  // STAGED only
+        [[maybe_unused]] uint8_t* ebuf = sE + (warp - FIRST_EPI_WARP) * EPI_WARP_BYTES;  // STAGED only
         uint32_t seq = 0;
         int lt = 0;
         for (int t = cluster_id; t < p.num_tiles; t += n_clusters, ++lt) {
@@ -1103,10 +1114,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if constexpr (QUAD) nb = 2 * nb + pq;
             const int row0 = mb * (2 * BM) + static_cast<int>(prank) * BM + q * 32;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-            if constexpr (STAGED)
+            if constexpr (STAGED) {
                 epilogue_tile_staged<EPI>(p, &tmO, &tmO2, t_row, row0, lane, nb, half, shard, ebuf, seq);
-            else
-                epilogue_tile<EPI>(p, t_row, row0 + lane, nb, half, shard);
+            } else {
+                static_assert(STAGED || PairGeom<STAGED>::epi_warps == 4, "direct epilogue: one warp per lane quarter");
+                epilogue_tile<EPI>(p, t_row, row0 + lane, nb, 0, shard);
+                epilogue_tile<EPI>(p, t_row, row0 + lane, nb, 1, shard);
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader0 + acc * 8);
