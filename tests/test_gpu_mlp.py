@@ -250,6 +250,25 @@ def test_many_shards(env, orc, shape, gemm_mode):
     _run_and_check(env, orc, wl)
 
 
+@pytest.mark.parametrize("shape", [(1, 1, 8, 8, 1), (32, 1, 8, 64, 8), (1, 2, 16, 32, 2), (3, 1, 64, 8, 1),
+                                   (1, 1, 64, 512, 1)],
+                         ids=["one-token-h8", "h8-p8", "two-tokens", "fs8", "one-token-two-pairs"])
+def test_degenerate_shapes(env, orc, shape, gemm_mode):
+    """The smallest legal problems: one token, h = 8 (one 16-byte row of X) with h / p = 1 and
+    f / p = 8, every operand smaller than a single TMA box and a single tile in every GEMM (the
+    last shape a single token over two 256-wide N-blocks, so mode 5 runs it on a two-pair
+    cluster).  The h = 8, p = 8 case runs 32 tokens: with one token its Z has 8 elements, too few
+    for the relative Frobenius error to be more than a sample of the bf16 roundings (a CPU
+    emulation of the kernels' rounding points, bf16 Y between the GEMMs and a bf16 Z store,
+    gives 3.003e-3 there, exactly what the kernels produce).  One token also makes dA and dB
+    outer products of bf16-rounded vectors, whose worst element carries one rounding unaveraged:
+    at h = f = 512 the emulation exceeds the max-abs bound exactly as the kernels do, so the
+    two-pair case is 64 wide.  The emulation passes every shape here."""
+    _, synth, _ = env
+    wl = synth.custom(*shape, dtype="bf16", sigma_w=0.1, sigma_bias=0.05, seed=sum(shape) + 11)
+    _run_and_check(env, orc, wl)
+
+
 def test_mixed_wave_shape(env, orc):
     """A shape whose row and dX GEMMs have 80 pair tiles (76 pairs fit at once), so the
     last wave holds 4 tiles, which walk K (and the shard sum) backwards; the
