@@ -1,0 +1,130 @@
+"""The kernels round where reading r7 of the tolerance says they do (GPU).
+
+Reading r7 fixes the precision of every intermediate: fp32 accumulation, H = XA + b1 in fp32,
+Y = GeLU(H) from that fp32 H rounded to bf16, H stored as bf16, Z = YB + b2 rounded to bf16;
+dH = (dZ Bᵀ) · GeLU'(H) from the stored bf16 H, rounded to bf16; dX = dH Aᵀ rounded to bf16;
+dA = Xᵀ dH, dB = Yᵀ dZ and db1 = 1ᵀdH in fp32 from the bf16 dH and Y.  This file builds those
+steps on the CPU (numpy in fp64, scipy's erfc, torch's CPU bf16 rounding, nothing from the CUDA
+path) and compares the kernels' outputs with them element by element.  The two differ only
+through fp32 accumulation order and the kernels' erfc approximation (|error| <= 1.5e-7), which
+move a bf16 rounding by one unit where the exact value sits that close to a rounding boundary:
+a small fraction of the elements, never more than one unit.  A different rounding protocol
+(GeLU of the bf16 H, GeLU' of an fp32 H, a missing or doubled rounding) changes a large
+fraction of the elements, which the tolerance against the fp64 oracle cannot tell apart.
+"""
+import numpy as np
+import pytest
+from scipy import special
+
+import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+# At most this fraction of a bf16 tensor's elements may differ from the emulation, each by one
+# bf16 unit.  The expected fraction is about 2 * (relative fp32 error) * 2^8 per element: below
+# 0.2 % for the sums of a few thousand terms here.
+MAX_FLIP_FRACTION = 0.01
+# Outputs computed from an earlier bf16 stage (Z from Y; dX, dA, db1 from dH; dB from Y): the
+# earlier stage's one-unit differences propagate, giving a relative Frobenius difference of
+# about sqrt(flip fraction) * 2^-8 (1-2e-4 at the fractions expected here).  A rounding out of
+# place (a bias added after a bf16 rounding, a second rounding) adds ~1e-3, a third of the
+# tolerance against the fp64 oracle.
+REL_F_DOWNSTREAM = 1e-3
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from megatron_tensor_mlp_gb300 import harness, synth, tpmlp
+    return harness, synth, tpmlp
+
+
+def _bf16(a):
+    """Round to bf16, nearest even (torch's CPU conversion), returned as fp64."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).bfloat16().double().numpy()
+
+
+def _f32(a):
+    return np.asarray(a, dtype=np.float32).astype(np.float64)
+
+
+def _gelu(x):
+    return x * 0.5 * special.erfc(-x / np.sqrt(2.0))
+
+
+def _gelu_grad(x):
+    return 0.5 * special.erfc(-x / np.sqrt(2.0)) + x * np.exp(-0.5 * x * x) / np.sqrt(2.0 * np.pi)
+
+
+def _emulate(X, A, b1, B, b2, dZ, gelu_of_saved_h=False, grad_of_fp32_h=False):
+    """The rounding points of reading r7 on exact (fp64) sums.  The two flags build the
+    plausible wrong protocols that the host test shows this comparison tells apart."""
+    Hf = _f32(X @ A + b1)              # fp32 pre-activation
+    H = _bf16(Hf)                       # the saved pre-activation
+    Y = _bf16(_gelu(H if gelu_of_saved_h else Hf))  # GeLU of the fp32 value
+    Z = _bf16(Y @ B + b2)
+    dY = _f32(dZ @ B.T)
+    dH = _bf16(dY * _gelu_grad(Hf if grad_of_fp32_h else H))  # GeLU' of the stored bf16 H
+    dX = _bf16(dH @ A.T)
+    return {"H": H, "Y": Y, "Z": Z, "dH": dH, "dX": dX,
+            "dA": X.T @ dH, "dB": Y.T @ dZ, "db1": dH.sum(0), "db2": dZ.sum(0)}
+
+
+def _flip_fraction(got, emu, name):
+    """The fraction of a bf16 tensor's elements that differ from the emulation, bounded."""
+    assert got.shape == emu.shape, (name, got.shape, emu.shape)
+    assert U.stored_as_bf16(got), f"{name}: not bf16 values"
+    flips = float(np.mean(got != emu))
+    assert flips <= MAX_FLIP_FRACTION, f"{name}: {100 * flips:.2f} % of elements differ from the emulation"
+    return flips
+
+
+def _check_bf16(got, emu, name):
+    """Every element equal to the emulation or one bf16 unit away; few of them away.  Units
+    are measured at max(|value|, 2^-10 RMS): where a sum nearly cancels, the absolute error of
+    fp32 accumulation (a few 1e-7 of the terms here) exceeds the tiny result's own bf16 unit,
+    whatever the rounding protocol."""
+    assert got.shape == emu.shape, (name, got.shape, emu.shape)
+    assert U.stored_as_bf16(got), f"{name}: not bf16 values"
+    floor = 2.0 ** -10 * float(np.sqrt(np.mean(emu * emu)))
+    unit = 2.0 * U.bf16_half_spacing(np.maximum(np.maximum(np.abs(got), np.abs(emu)), floor))
+    units = np.abs(got - emu) / unit
+    assert float(np.max(units)) <= 1.0, f"{name}: {float(np.max(units)):.1f} bf16 units from the emulation"
+    return _flip_fraction(got, emu, name)
+
+
+@pytest.mark.parametrize("mode", [1, 3, 5], ids=["single-cta", "pair-direct", "two-pairs"])
+def test_rounding_points_match_emulation(env, mode):
+    harness, synth, T = env
+    T.tpmlp_set_gemm_mode(mode)
+    try:
+        wl = synth.custom(64, 4, 512, 2048, 4, dtype="bf16", sigma_w=0.03, sigma_bias=0.05, seed=96)
+        buf = harness.MLPBuffers(wl, backward=True)
+        buf.fwd()
+        buf.bwd()
+        T.tpmlp_device_status()
+    finally:
+        T.tpmlp_set_gemm_mode(0)
+    x = U.host_inputs_f64(buf)
+    emu = _emulate(x["X"], x["A"], x["b1"], x["B"], x["b2"], x["dZ"])
+    M, f = wl.M, wl.ffn
+    # the stage whose inputs are exact: element by element, in bf16 units
+    flips = {k: _check_bf16(harness.to_host(t), emu[k], k) for k, t in (("H", buf.H_full()), ("Y", buf.Y_full()))}
+    # dH takes GeLU' of the saved H, so H's one-unit differences reach it, and near GeLU's
+    # inflection (GeLU'(h) = 0 at h = -0.752) one unit of H moves GeLU' by ~1e-3 absolute, many
+    # units of a small dH: its elements are counted, not bounded one by one
+    dH = harness.to_host(buf.dH.permute(1, 0, 2).reshape(M, f))
+    flips["dH"] = _flip_fraction(dH, emu["dH"], "dH")
+    # stages fed by an earlier bf16 stage
+    rel = {"dH": float(np.linalg.norm(dH - emu["dH"]) / np.linalg.norm(emu["dH"]))}
+    assert rel["dH"] <= REL_F_DOWNSTREAM, f"dH: rel Frobenius {rel['dH']:.2e} from the emulation"
+    for k, t in (("Z", buf.Z), ("dX", buf.dX), ("dA", buf.dA_full()), ("dB", buf.dB_full()),
+                 ("db1", buf.db1_sh.reshape(-1)), ("db2", buf.db2)):
+        g = harness.to_host(t)
+        rel[k] = float(np.linalg.norm(g - emu[k]) / np.linalg.norm(emu[k]))
+        assert rel[k] <= REL_F_DOWNSTREAM, f"{k}: rel Frobenius {rel[k]:.2e} from the emulation"
+    print("one-unit fraction:", {k: f"{v:.2e}" for k, v in flips.items()},
+          "rel. Frobenius from the emulation:", {k: f"{v:.1e}" for k, v in rel.items()})
