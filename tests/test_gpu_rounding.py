@@ -128,3 +128,81 @@ def test_rounding_points_match_emulation(env, mode):
         assert rel[k] <= REL_F_DOWNSTREAM, f"{k}: rel Frobenius {rel[k]:.2e} from the emulation"
     print("one-unit fraction:", {k: f"{v:.2e}" for k, v in flips.items()},
           "rel. Frobenius from the emulation:", {k: f"{v:.1e}" for k, v in rel.items()})
+
+
+# ---------------------------------------------------------------------------- SwiGLU (reading r14)
+def _silu(x):
+    return x * special.expit(x)
+
+
+def _silu_grad(x):
+    s = special.expit(x)
+    return s * (1.0 + x * (1.0 - s))
+
+
+def _emulate_swiglu(X, G, Uw, bg, bu, B, b2, dZ, bf16_saves=False):
+    """Reading r14's rounding points: fp32 gate and up pre-activations (saved in fp32),
+    Y = bf16(silu(g) u), Z = bf16(Y B + b2); dY in fp32, dg = bf16(dY u silu'(g)),
+    du = bf16(dY silu(g)), dX = bf16(dg Gᵀ + du Uᵀ); fp32 weight and bias gradients."""
+    Hg, Hu = _f32(X @ G + bg), _f32(X @ Uw + bu)
+    Y = _bf16(_silu(Hg) * Hu)
+    Z = _bf16(Y @ B + b2)
+    dY = _f32(dZ @ B.T)
+    if bf16_saves:  # the wrong protocol the host test separates: pre-activations saved in bf16
+        Hg, Hu = _bf16(Hg), _bf16(Hu)
+    dHg, dHu = _bf16(dY * Hu * _silu_grad(Hg)), _bf16(dY * _silu(Hg))
+    return {"Hg": Hg, "Hu": Hu, "Y": Y, "Z": Z, "dHg": dHg, "dHu": dHu, "dX": _bf16(dHg @ G.T + dHu @ Uw.T),
+            "dG": X.T @ dHg, "dU": X.T @ dHu, "dB": Y.T @ dZ, "dbg": dHg.sum(0), "dbu": dHu.sum(0),
+            "db2": dZ.sum(0)}
+
+
+@pytest.mark.parametrize("mode", [1, 2, 5], ids=["single-cta", "cta-pair", "two-pairs"])
+def test_swiglu_rounding_points_match_emulation(env, orc, mode):
+    import torch
+    harness, synth, T = env
+    s, b, h, f, p = 64, 4, 512, 2048, 4
+    M, fs = s * b, f // p
+    gen = lambda stream, shp, sig: synth.normal(97, stream, shp, sig, "bf16")  # noqa: E731
+    X, G, Uw, B = gen(1, (M, h), 1.0), gen(2, (h, f), 0.05), gen(9, (h, f), 0.05), gen(3, (f, h), 0.05)
+    bg, bu, b2, dZ = gen(4, (f,), 0.05), gen(10, (f,), 0.05), gen(5, (h,), 0.05), gen(6, (M, h), 1.0)
+    d = harness.to_torch
+    T.tpmlp_set_gemm_mode(mode)
+    try:
+        W = torch.empty((p, h, 2 * fs), dtype=torch.bfloat16, device="cuda")
+        T.tpmlp_swiglu_pack(d(G), d(Uw), W, h, f, p)
+        bw = torch.empty((p, 2 * fs), dtype=torch.bfloat16, device="cuda")
+        T.tpmlp_swiglu_pack(d(bg), d(bu), bw, 1, f, p)
+        Bd = d(B).view(p, fs, h)
+        Z = torch.empty((M, h), dtype=torch.bfloat16, device="cuda")
+        Y = torch.empty((p, M, fs), dtype=torch.bfloat16, device="cuda")
+        H = torch.empty((p, M, 2 * fs), dtype=torch.float32, device="cuda")
+        T.tpmlp_swiglu_mlp_fwd(d(X), W, bw, Bd, d(b2), Z, Y, H, s, b, h, f, p)
+        dX = torch.empty((M, h), dtype=torch.bfloat16, device="cuda")
+        dW = torch.empty((p, h, 2 * fs), dtype=torch.float32, device="cuda")
+        dB = torch.empty((p, fs, h), dtype=torch.float32, device="cuda")
+        dbw = torch.empty((p, 2 * fs), dtype=torch.float32, device="cuda")
+        db2 = torch.empty((h,), dtype=torch.float32, device="cuda")
+        dH = torch.empty((p, M, 2 * fs), dtype=torch.bfloat16, device="cuda")
+        T.tpmlp_swiglu_mlp_bwd(d(X), W, Bd, H, Y, d(dZ), dX, dW, dB, dbw, db2, dH, s, b, h, f, p)
+        T.tpmlp_device_status()
+    finally:
+        T.tpmlp_set_gemm_mode(0)
+    x = synth.widen
+    emu = _emulate_swiglu(x(X), x(G), x(Uw), x(bg), x(bu), x(B), x(b2), x(dZ))
+    host = harness.to_host
+    Hg, Hu = orc.swiglu_unpack(host(H.permute(1, 0, 2)).transpose(1, 0, 2).copy(), p)
+    for k, v in (("Hg", Hg), ("Hu", Hu)):  # saved in fp32: the fp32 sums themselves
+        assert np.max(np.abs(v - emu[k])) <= 1e-5 * max(1.0, float(np.max(np.abs(emu[k])))), k
+    dHg, dHu = orc.swiglu_unpack(host(dH), p)
+    # stages whose inputs are fp32 sums: element by element, in bf16 units
+    flips = {k: _check_bf16(v, emu[k], k)
+             for k, v in (("Y", host(Y.permute(1, 0, 2).reshape(M, f))), ("dHg", dHg), ("dHu", dHu))}
+    dG, dU = orc.swiglu_unpack(host(dW), p)
+    dbg, dbu = orc.swiglu_unpack(host(dbw).reshape(p, 1, 2 * fs), p)
+    rel = {}
+    for k, v in (("Z", host(Z)), ("dX", host(dX)), ("dG", dG), ("dU", dU), ("dB", host(dB.reshape(f, h))),
+                 ("dbg", dbg.reshape(-1)), ("dbu", dbu.reshape(-1)), ("db2", host(db2))):
+        rel[k] = float(np.linalg.norm(v - emu[k]) / np.linalg.norm(emu[k]))
+        assert rel[k] <= REL_F_DOWNSTREAM, f"{k}: rel Frobenius {rel[k]:.2e} from the emulation"
+    print("one-unit fraction:", {k: f"{v:.2e}" for k, v in flips.items()},
+          "rel. Frobenius from the emulation:", {k: f"{v:.1e}" for k, v in rel.items()})

@@ -2,9 +2,10 @@
 
 The GPU test allows at most MAX_FLIP_FRACTION of a bf16 output's elements to sit one unit from
 the emulation of reading r7.  Here the emulation is compared with the same emulation under the
-two plausible wrong protocols, on the GPU test's own inputs: GeLU taken of the saved bf16 H
-instead of the fp32 one, and GeLU' taken of the fp32 H instead of the saved one.  Each moves
-many times that fraction of Y or dH, so neither could pass the GPU test.
+plausible wrong protocols, on the GPU tests' own inputs: GeLU taken of the saved bf16 H instead
+of the fp32 one, GeLU' taken of the fp32 H instead of the saved one, and (SwiGLU) the gate and up
+pre-activations saved in bf16 instead of fp32.  Each moves many times that fraction of Y, dH or
+(dg, du), so none could pass the GPU test.
 """
 import numpy as np
 
@@ -40,3 +41,14 @@ def test_emulation_meets_the_oracle_tolerance():
     for k, ref in (("Z", Z), ("Y", Y), ("H", H), ("dX", g["dX"]), ("dA", g["dA"]), ("dB", g["dB"]),
                    ("db1", g["db1"]), ("db2", g["db2"])):
         U.assert_close(emu[k], ref, "bf16", k)
+
+
+def test_swiglu_bf16_saves_move_many_elements():
+    gen = lambda stream, shp, sig: synth.widen(synth.normal(97, stream, shp, sig, "bf16"))  # noqa: E731
+    M, h, f = 256, 512, 2048
+    X, G, Uw, B = gen(1, (M, h), 1.0), gen(2, (h, f), 0.05), gen(9, (h, f), 0.05), gen(3, (f, h), 0.05)
+    bg, bu, b2, dZ = gen(4, (f,), 0.05), gen(10, (f,), 0.05), gen(5, (h,), 0.05), gen(6, (M, h), 1.0)
+    ok = R._emulate_swiglu(X, G, Uw, bg, bu, B, b2, dZ)
+    bad = R._emulate_swiglu(X, G, Uw, bg, bu, B, b2, dZ, bf16_saves=True)
+    frac = float(np.mean(np.concatenate([(bad[k] != ok[k]).ravel() for k in ("dHg", "dHu")])))
+    assert frac > 5 * R.MAX_FLIP_FRACTION, frac
