@@ -278,7 +278,8 @@ tpmlp_status tpmlp_debug_wait_timeout(uint32_t timeout_us, void* stream);
  * TMA stores; long-K GEMMs run on clusters of two CTA pairs (as in 5) when those
  * fill their last wave at least 2 points better than single pairs.  1 = single-CTA tiles only; 2 = CTA-pair tiles only (epilogue chosen
  * as in 0); 3 = CTA-pair tiles, direct stores; 4 = CTA-pair tiles, TMA stores (the
- * SwiGLU epilogues always store directly); 5 = clusters of two CTA pairs that
+ * SwiGLU epilogues, and the later launches of a split contraction that add to their
+ * output, always store directly); 5 = clusters of two CTA pairs that
  * compute neighbouring 256-column tiles and share each A tile through TMA
  * multicast (direct stores; GEMMs with an odd number of 256-column blocks fall back
  * to 2).  Results agree within rounding in every mode; the control exists for
