@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fwd-pages", action="store_true")
     ap.add_argument("--no-next-rows", action="store_true", help="skip the SwiGLU / attention-projection timings")
+    ap.add_argument("--next-rows-only", action="store_true",
+                    help="time only the SwiGLU and attention-projection steps (for profiling their launches)")
     ap.add_argument("--e2e-steps", type=int, default=60)
     ap.add_argument("--bwd", action="store_true",
                     help="run forward + backward on a forward-only workload (for profiling its backward GEMMs)")
@@ -460,6 +462,12 @@ def run_gpu(args):
     from megatron_tensor_mlp_gb300 import tpmlp as T
 
     peaks, peak_kind = load_peaks()
+    if args.next_rows_only:
+        rows = time_next_rows(torch.cuda.current_stream(), args.steps, peaks, args.warmup)
+        if rank == 0:
+            print(json.dumps({"metric": "widened rows, fwd+bwd TFLOP/s on 1 GB300", "next_rows": rows,
+                              "steps": args.steps, "warmup": args.warmup}), flush=True)
+        return
     wl = synth.WORKLOADS[args.workload]
     if args.bwd and not wl.backward:
         import dataclasses
