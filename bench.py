@@ -235,8 +235,11 @@ class OracleSample:
         return time.perf_counter() - t0
 
     def calibrate(self, target_seconds):
-        """Largest power-of-two token count whose pass stays near target_seconds."""
+        """Largest power-of-two token count whose pass stays near target_seconds.  One untimed
+        pass first: the first call also pays for the oracle's thread start-up and first touches
+        of its output arrays, which would otherwise stop the doubling at one token."""
         tokens = 1
+        self.run(tokens)
         dt = self.run(tokens)
         while tokens * 2 <= self.wl.M and dt * 2 <= target_seconds:
             tokens *= 2
