@@ -33,3 +33,14 @@ def test_captured_traffic_matches_committed_kernel():
         assert isinstance(v, int) and v > 0
     else:
         assert v is None
+
+
+def test_default_and_profiling_flags(monkeypatch):
+    """Without flags the bench runs one GPU with a time-based warm-up; --next-rows-only is an
+    opt-in profiling mode and never the default."""
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    a = bench.parse()
+    assert a.gpus == 1 and a.warmup is None and a.impl == "tpmlp" and not a.next_rows_only
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--next-rows-only", "--steps", "8", "--warmup", "2"])
+    a = bench.parse()
+    assert a.next_rows_only and a.steps == 8 and a.warmup == 2
