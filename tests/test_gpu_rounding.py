@@ -257,3 +257,59 @@ def test_full_workload_rounding_points_sampled(env, wi):
         assert rel[k] <= 2e-3, f"{k}: rel Frobenius {rel[k]:.2e} from the emulation"
     print("one-unit fraction:", {k: f"{v:.2e}" for k, v in flips.items()},
           "rel. Frobenius from the emulation:", {k: f"{v:.1e}" for k, v in rel.items()})
+
+
+# ---------------------------------------------------------------------- attention projections
+@pytest.mark.parametrize("mode", [1, 3, 5], ids=["single-cta", "pair-direct", "two-pairs"])
+def test_attention_projection_rounding_points(env, orc, mode):
+    """QKV = bf16(X W + b) over the per-head interleave, Z = bf16(ctx W_o + b_o) summed over the
+    ranks' head blocks, dctx = bf16(dZ W_oᵀ), dX = bf16(dQKV Wᵀ) summed over ranks: each a single
+    rounding of an fp32 sum of exact inputs, so every element is checked in bf16 units; the fp32
+    weight and bias gradients have no bf16 stage before them (rel. Frobenius <= 1e-5)."""
+    import torch
+    harness, synth, T = env
+    s, b, h, heads, p = 64, 4, 512, 8, 4
+    M, hq = s * b, 3 * h // p
+    gen = lambda stream, shp, sig: synth.normal(98, stream, shp, sig, "bf16")  # noqa: E731
+    X, Wq, bq = gen(1, (M, h), 1.0), gen(2, (h, 3 * h), 0.05), gen(4, (3 * h,), 0.05)
+    dQ, ctx, Wo, bo, dZ = gen(6, (M, 3 * h), 1.0), gen(7, (M, h), 1.0), gen(3, (h, h), 0.05), gen(5, (h,), 0.05), \
+        gen(8, (M, h), 1.0)
+    d, host, x = harness.to_torch, harness.to_host, synth.widen
+    T.tpmlp_set_gemm_mode(mode)
+    try:
+        Wi = torch.empty((h, 3 * h), dtype=torch.bfloat16, device="cuda")
+        T.tpmlp_qkv_interleave(d(Wq), Wi, h, h, heads, p)
+        bi = torch.empty((3 * h,), dtype=torch.bfloat16, device="cuda")
+        T.tpmlp_qkv_interleave(d(bq), bi, 1, h, heads, p)
+        W_sh = torch.empty((p, h, hq), dtype=torch.bfloat16, device="cuda")
+        T.tpmlp_shard_columns(Wi, W_sh, h, 3 * h, p)
+        QKV = torch.empty((p, M, hq), dtype=torch.bfloat16, device="cuda")
+        T.tpmlp_column_fwd(d(X), W_sh, bi, QKV, None, s, b, h, 3 * h, p, act=T.ACT_NONE)
+        dQd = d(dQ).view(M, p, hq).permute(1, 0, 2).contiguous()
+        dX = torch.empty((M, h), dtype=torch.bfloat16, device="cuda")
+        dW = torch.empty((p, h, hq), dtype=torch.float32, device="cuda")
+        db = torch.empty((p, hq), dtype=torch.float32, device="cuda")
+        T.tpmlp_column_bwd(d(X), W_sh, dQd, dX, dW, db, s, b, h, 3 * h, p)
+        ctx_sh = d(ctx).view(M, p, h // p).permute(1, 0, 2).contiguous()
+        Z = torch.empty((M, h), dtype=torch.bfloat16, device="cuda")
+        T.tpmlp_row_fwd(ctx_sh, d(Wo), d(bo), Z, s, b, h, h, p)
+        dctx = torch.empty((p, M, h // p), dtype=torch.bfloat16, device="cuda")
+        dWo = torch.empty((p, h // p, h), dtype=torch.float32, device="cuda")
+        dbo = torch.empty((h,), dtype=torch.float32, device="cuda")
+        T.tpmlp_row_bwd(ctx_sh, d(Wo), d(dZ), None, dctx, dWo, dbo, s, b, h, h, p, act=T.ACT_NONE)
+        T.tpmlp_device_status()
+    finally:
+        T.tpmlp_set_gemm_mode(0)
+    Wih = orc.qkv_interleave(x(Wq), h, heads)          # layout map only
+    bih = orc.qkv_interleave(x(bq)[None, :], h, heads)[0]
+    Xf, dQf, ctxf, Wof, dZf = x(X), x(dQ), x(ctx), x(Wo), x(dZ)
+    bf16_out = {"QKV": (host(QKV.permute(1, 0, 2).reshape(M, 3 * h)), _bf16(_f32(Xf @ Wih + bih))),
+                "dX": (host(dX), _bf16(_f32(dQf @ Wih.T))),
+                "Z": (host(Z), _bf16(_f32(ctxf @ Wof + x(bo)))),
+                "dctx": (host(dctx.permute(1, 0, 2).reshape(M, h)), _bf16(_f32(dZf @ Wof.T)))}
+    flips = {k: _check_bf16(g, e, k) for k, (g, e) in bf16_out.items()}
+    for k, g, e in (("dW", host(dW.permute(1, 0, 2).reshape(h, 3 * h)), Xf.T @ dQf), ("db", host(db.reshape(-1)), dQf.sum(0)),
+                    ("dWo", host(dWo.reshape(h, h)), ctxf.T @ dZf), ("dbo", host(dbo), dZf.sum(0))):
+        err = float(np.linalg.norm(g - e) / np.linalg.norm(e))
+        assert err <= 1e-5, f"{k}: rel Frobenius {err:.2e} from the exact sum"
+    print("one-unit fraction:", {k: f"{v:.2e}" for k, v in flips.items()})
