@@ -24,9 +24,10 @@
  *     bytes as B [f, h] row-major), b1_sh [p][f/p] (the same bytes as b1 [f]),
  *     Y_sh / H_sh / dH [p][M][f/p].  All matrices are row-major.
  *   Memory.  Every pointer is caller-owned device memory (for example
- *     allocated by PyTorch).  The library never allocates, frees or
- *     synchronises inside these calls; workspaces are passed in with the sizes
- *     stated.  Calls are stream ordered and asynchronous: they return after
+ *     allocated by PyTorch).  The library never allocates device memory,
+ *     frees or synchronises inside these calls; workspaces are passed in with
+ *     the sizes stated.  (tpmlp_mlp_bwd creates, once per host thread and
+ *     device, one non-blocking stream and two events, and keeps them.)  Calls are stream ordered and asynchronous: they return after
  *     the kernels are enqueued on `stream` (a cudaStream_t; NULL = legacy
  *     default stream).  The GEMM kernels are launched with programmatic
  *     dependent launch: their set-up may overlap the end of the preceding
@@ -126,6 +127,12 @@ tpmlp_status tpmlp_mlp_fwd(const void* X, const void* A_sh, const void* b1_sh, c
  *          db2 [h] (or NULL), all grad_dt (fp32 recommended for bf16 inputs).
  * Workspace: dH_ws [p][M][ffn/p] dt, holds dH on return.
  * Requires ffn % p == 0 and h % p == 0; grad_dt must be TPMLP_F32 when dt is TPMLP_F32.
+ * Launch order on `stream`: dH, dB, dA, dX.  For bf16, db1 and db2 run on a second
+ * stream that waits for the dA launch (an event recorded on `stream`) and that
+ * `stream` waits for after dX, so they run beside the dX GEMM (whose clusters of
+ * two CTA pairs leave SMs free) and everything is complete, in stream order, when
+ * the work enqueued on `stream` is.  The fork and join are events, so the call can
+ * be captured into a CUDA graph.
  */
 tpmlp_status tpmlp_mlp_bwd(const void* X, const void* A_sh, const void* B_sh, const void* H_sh, const void* Y_sh,
                            const void* dZ, void* dX, void* dA_sh, void* dB_sh, void* db1_sh, void* db2,
@@ -187,6 +194,7 @@ tpmlp_status tpmlp_swiglu_mlp_fwd(const void* X, const void* W_sh, const void* b
  * Inputs: X, W_sh, B_sh, Y_ws and dZ (bf16); H_ws (packed fp32 pre-activations from the forward).
  * Outputs: dX bf16; dW_sh [p][h][2 ffn/p], dB_sh, dbw_sh [p][2 ffn/p] (or NULL), db2 (or NULL) grad_dt.
  * Workspace: dH_ws [p][M][2 ffn/p] bf16 (holds the packed dHg, dHu on return).
+ * As in tpmlp_mlp_bwd, dbw and db2 run on the second stream beside the dX GEMM.
  */
 tpmlp_status tpmlp_swiglu_mlp_bwd(const void* X, const void* W_sh, const void* B_sh, const void* H_ws,
                                   const void* Y_ws, const void* dZ, void* dX, void* dW_sh, void* dB_sh, void* dbw_sh,

@@ -65,6 +65,8 @@ tpmlp_status launch_simt_gemm(const Operand& a, const Operand& b, const GemmSpec
 // out[s][n] = sum_m in[s][m][n]; in bf16 or f32 (in_f32), out f32 or bf16 (out_f32)
 tpmlp_status launch_colsum(const void* in, bool in_f32, int64_t shards, int64_t M, int64_t N, void* out,
                            bool out_f32, cudaStream_t st);
+tpmlp_status launch_colsum_any_sm(const void* in, int64_t shards, int64_t M, int64_t N, void* out, bool out_f32,
+                                  cudaStream_t st);
 tpmlp_status launch_shard_columns(const void* src, void* dst, int64_t rows, int64_t cols, int p, int esize,
                                   bool inverse, cudaStream_t st);
 tpmlp_status launch_qkv_interleave(const void* src, void* dst, int64_t rows, int64_t h, int64_t n_heads,

@@ -191,6 +191,54 @@ __global__ void __cluster_dims__(1, CS_CLUSTER, 1) __launch_bounds__(CS_WARPS * 
     cluster.sync();  // peers stay resident until CTA 0 has read their shared memory
 }
 
+// The same column sums without a cluster: one CTA per 256-column strip and shard does the work
+// of the 8-CTA cluster above in the same order (accumulator set g holds what CTA g of the
+// cluster sums: warp w takes rows 16 g + w + 128 i in increasing order; then each set is added
+// over the 16 warps, and the sets over g), so the results are bit-identical to that kernel's,
+// and any free SM can run it, e.g. beside a GEMM whose clusters leave SMs idle.
+template <bool OUT_F32>
+__global__ void __launch_bounds__(CS_WARPS * 32)
+    colsum_bf16_strip_kernel(const __nv_bfloat16* __restrict__ in, long long M, long long N, void* out) {
+    __shared__ float part[CS_WARPS][256];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const long long s = blockIdx.z;
+    const long long c = (long long)blockIdx.x * 256 + lane * 8;
+    const __nv_bfloat16* base = in + s * M * N + c;
+    float r = 0.f;
+    // one accumulator set at a time (eight registers, as in the cluster kernel), so that
+    // several CTAs fit on an SM and keep enough loads in flight
+#pragma unroll 1
+    for (int g = 0; g < CS_CLUSTER; ++g) {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (c < N) {
+#pragma unroll 8
+            for (long long m = (long long)g * CS_WARPS + warp; m < M; m += CS_WARPS * CS_CLUSTER) {
+                const uint4 u = __ldg(reinterpret_cast<const uint4*>(base + m * N));
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] += __uint_as_float(w[i] << 16);
+                    acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) part[warp][lane * 8 + k] = acc[k];
+        __syncthreads();
+        if (threadIdx.x < 256) {
+            float bs = 0.f;
+            for (int w = 0; w < CS_WARPS; ++w) bs += part[w][threadIdx.x];
+            r += bs;
+        }
+        __syncthreads();
+    }
+    const long long col = (long long)blockIdx.x * 256 + threadIdx.x;
+    if (threadIdx.x < 256 && col < N) {
+        if (OUT_F32) static_cast<float*>(out)[s * N + col] = r;
+        else static_cast<__nv_bfloat16*>(out)[s * N + col] = __float2bfloat16_rn(r);
+    }
+}
+
 // ------------------------------------------------------------------ layouts
 // Column shard: dst[i][r][c] = src[r][i*cs + c] in 16-byte units (rows of cs*esize bytes).
 __global__ void shard_columns_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long rows,
@@ -320,6 +368,17 @@ tpmlp_status launch_colsum(const void* in, bool in_f32, int64_t shards, int64_t 
     else if (in_f32) colsum_kernel<true, false><<<grid, 256, 0, st>>>(in, M, N, out);
     else if (out_f32) colsum_kernel<false, true><<<grid, 256, 0, st>>>(in, M, N, out);
     else colsum_kernel<false, false><<<grid, 256, 0, st>>>(in, M, N, out);
+    return check_launch("column sum");
+}
+
+// bf16 column sums without clusters, bit-identical to launch_colsum's: schedulable on any
+// free SM, e.g. beside a GEMM that leaves SMs idle.
+tpmlp_status launch_colsum_any_sm(const void* in, int64_t shards, int64_t M, int64_t N, void* out, bool out_f32,
+                                  cudaStream_t st) {
+    dim3 g((unsigned)((N + 255) / 256), 1, (unsigned)shards);
+    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(in);
+    if (out_f32) colsum_bf16_strip_kernel<true><<<g, CS_WARPS * 32, 0, st>>>(src, M, N, out);
+    else colsum_bf16_strip_kernel<false><<<g, CS_WARPS * 32, 0, st>>>(src, M, N, out);
     return check_launch("column sum");
 }
 

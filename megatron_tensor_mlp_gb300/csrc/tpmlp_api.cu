@@ -216,9 +216,11 @@ tpmlp_status do_row_bwd(const void* Y_sh, const void* B_sh, const void* dZ, cons
 }
 
 // Column layer backward: dA_i = X^T dY_i, db1_i = 1^T dY_i, dX = sum_i dY_i A_i^T.
+struct SideWork;  // column sums run beside the dX GEMM (see tpmlp_mlp_bwd)
+tpmlp_status side_fork(SideWork* w, cudaStream_t st);
 tpmlp_status do_column_bwd(const void* X, const void* A_sh, const void* dY_sh, void* dX, void* dA_sh, void* db1_sh,
                            int64_t M, int64_t h, int64_t ffn, int p, tpmlp_dtype dt, bool grad_f32,
-                           const DeviceInfo& dev, cudaStream_t st) {
+                           const DeviceInfo& dev, cudaStream_t st, SideWork* side = nullptr) {
     const int64_t fs = ffn / p;
     if (db1_sh) TP_TRY(launch_colsum(dY_sh, dt == TPMLP_F32, p, M, fs, db1_sh, grad_f32, st));
     {
@@ -231,6 +233,7 @@ tpmlp_status do_column_bwd(const void* X, const void* A_sh, const void* dY_sh, v
         g.out = dA_sh; g.out_ld = fs; g.out_ss = h * fs;
         TP_TRY(run_gemm(a, bb, g, dt, dev, st));
     }
+    if (side) TP_TRY(side_fork(side, st));
     {
         Operand a{dY_sh, fs, M * fs, p, false};      // dY_i [M][fs], K-major
         Operand bb{A_sh, fs, h * fs, p, false};      // A_i [h][fs]: [N][K], K-major
@@ -240,6 +243,59 @@ tpmlp_status do_column_bwd(const void* X, const void* A_sh, const void* dY_sh, v
         g.epi = EPI_STORE; g.out_f32 = (dt == TPMLP_F32);
         g.out = dX; g.out_ld = h; g.out_ss = 0;
         TP_TRY(run_gemm(a, bb, g, dt, dev, st));
+    }
+    return TPMLP_OK;
+}
+
+// The bias-gradient column sums of tpmlp_mlp_bwd run on a second stream, forked after the dA
+// GEMM is enqueued and joined after dX: they become ready together with the dX GEMM, whose
+// two-pair clusters leave SMs idle that the (cluster-free) column sums can use.
+struct SideWork {
+    const void* dZ; void* db2; const void* dH; void* db1; int64_t M, h, fs, p; bool f32;
+    cudaStream_t side; cudaEvent_t fork, join;
+};
+struct SideHandles { cudaStream_t s = nullptr; cudaEvent_t fork = nullptr, join = nullptr; };
+thread_local SideHandles t_side[64];
+tpmlp_status side_handles(int device, SideHandles** out) {
+    if (device < 0 || device >= 64) { set_error("device index %d out of range", device); return TPMLP_ERR_CUDA; }
+    SideHandles& h = t_side[device];
+    if (!h.s) {
+        cudaError_t e = cudaStreamCreateWithFlags(&h.s, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.join, cudaEventDisableTiming);
+        if (e != cudaSuccess) { set_error("side stream: %s", cudaGetErrorString(e)); return TPMLP_ERR_CUDA; }
+    }
+    *out = &h;
+    return TPMLP_OK;
+}
+tpmlp_status side_fork(SideWork* w, cudaStream_t st) {
+    cudaError_t e = cudaEventRecord(w->fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(w->side, w->fork, 0);
+    if (e != cudaSuccess) { set_error("side stream fork: %s", cudaGetErrorString(e)); return TPMLP_ERR_CUDA; }
+    if (w->db2) TP_TRY(launch_colsum_any_sm(w->dZ, 1, w->M, w->h, w->db2, w->f32, w->side));
+    if (w->db1) TP_TRY(launch_colsum_any_sm(w->dH, w->p, w->M, w->fs, w->db1, w->f32, w->side));
+    e = cudaEventRecord(w->join, w->side);
+    if (e != cudaSuccess) { set_error("side stream: %s", cudaGetErrorString(e)); return TPMLP_ERR_CUDA; }
+    return TPMLP_OK;
+}
+
+// The column layer backward of a block (do_column_bwd) with the block's bias-gradient column
+// sums, db1 of dY_sh and db2 of dZ (either may be NULL), on the side stream for bf16 inputs.
+tpmlp_status column_bwd_side_sums(const void* X, const void* A_sh, const void* dY_sh, void* dX, void* dA_sh,
+                                  void* db1_sh, const void* dZ, void* db2, int64_t M, int64_t h, int64_t ffn, int p,
+                                  tpmlp_dtype dt, bool grad_f32, const DeviceInfo& dev, cudaStream_t st) {
+    if (dt != TPMLP_BF16 || (!db1_sh && !db2)) {
+        if (db2) TP_TRY(launch_colsum(dZ, dt == TPMLP_F32, 1, M, h, db2, grad_f32, st));
+        return do_column_bwd(X, A_sh, dY_sh, dX, dA_sh, db1_sh, M, h, ffn, p, dt, grad_f32, dev, st);
+    }
+    SideHandles* sh = nullptr;
+    TP_TRY(side_handles(dev.device, &sh));
+    SideWork w{dZ, db2, dY_sh, db1_sh, M, h, ffn / p, p, grad_f32, sh->s, sh->fork, sh->join};
+    TP_TRY(do_column_bwd(X, A_sh, dY_sh, dX, dA_sh, nullptr, M, h, ffn, p, dt, grad_f32, dev, st, &w));
+    const cudaError_t e = cudaStreamWaitEvent(st, sh->join, 0);
+    if (e != cudaSuccess) {
+        set_error("side stream join: %s", cudaGetErrorString(e));
+        return TPMLP_ERR_CUDA;
     }
     return TPMLP_OK;
 }
@@ -403,9 +459,10 @@ tpmlp_status tpmlp_mlp_bwd(const void* X, const void* A_sh, const void* B_sh, co
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool gf32 = grad_dt == TPMLP_F32;
     // row layer backward with GeLU' fused: dH_i = (dZ B_i^T) * GeLU'(H_i); dB_i; db2
-    TP_TRY(do_row_bwd(Y_sh, B_sh, dZ, H_sh, dH_ws, dB_sh, db2, M, h, ffn, p, dt, gf32, TPMLP_ACT_GELU_ERF, *dev, st));
-    // column layer backward from dH: dA_i; db1_i; dX = sum_i dH_i A_i^T
-    return do_column_bwd(X, A_sh, dH_ws, dX, dA_sh, db1_sh, M, h, ffn, p, dt, gf32, *dev, st);
+    TP_TRY(do_row_bwd(Y_sh, B_sh, dZ, H_sh, dH_ws, dB_sh, nullptr, M, h, ffn, p, dt, gf32, TPMLP_ACT_GELU_ERF,
+                      *dev, st));
+    // column layer backward from dH: dA_i, dX = sum_i dH_i A_i^T; db1_i and db2 beside dX
+    return column_bwd_side_sums(X, A_sh, dH_ws, dX, dA_sh, db1_sh, dZ, db2, M, h, ffn, p, dt, gf32, *dev, st);
 }
 
 tpmlp_status tpmlp_row_bwd(const void* Y_sh, const void* B_sh, const void* dZ, const void* H_sh, void* dY_sh,
@@ -538,7 +595,6 @@ tpmlp_status tpmlp_swiglu_mlp_bwd(const void* X, const void* W_sh, const void* B
         g.out = dH_ws; g.out_ld = 2 * fs; g.out_ss = M * 2 * fs;
         TP_TRY(run_gemm(a, bb, g, dt, *dev, st));
     }
-    if (db2) TP_TRY(launch_colsum(dZ, false, 1, M, h, db2, gf32, st));
     {
         Operand a{Y_ws, fs, M * fs, p, true};          // dB_i = Y_i^T dZ
         Operand bb{dZ, h, 0, 1, true};
@@ -549,8 +605,9 @@ tpmlp_status tpmlp_swiglu_mlp_bwd(const void* X, const void* W_sh, const void* B
         g.out = dB_sh; g.out_ld = h; g.out_ss = fs * h;
         TP_TRY(run_gemm(a, bb, g, dt, *dev, st));
     }
-    // the packed gate/up layer is a column layer of width 2 ffn: dW = X^T dH, dbw, dX = sum_i dH_i W_i^T
-    return do_column_bwd(X, W_sh, dH_ws, dX, dW_sh, dbw_sh, M, h, 2 * ffn, p, dt, gf32, *dev, st);
+    // the packed gate/up layer is a column layer of width 2 ffn: dW = X^T dH, dX = sum_i dH_i W_i^T;
+    // dbw and db2 beside dX
+    return column_bwd_side_sums(X, W_sh, dH_ws, dX, dW_sh, dbw_sh, dZ, db2, M, h, 2 * ffn, p, dt, gf32, *dev, st);
 }
 
 tpmlp_status tpmlp_swiglu_pack(void* G, void* U, void* W_sh, int64_t rows, int64_t ffn, int p, tpmlp_dtype dt,
