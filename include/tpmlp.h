@@ -127,12 +127,13 @@ tpmlp_status tpmlp_mlp_fwd(const void* X, const void* A_sh, const void* b1_sh, c
  *          db2 [h] (or NULL), all grad_dt (fp32 recommended for bf16 inputs).
  * Workspace: dH_ws [p][M][ffn/p] dt, holds dH on return.
  * Requires ffn % p == 0 and h % p == 0; grad_dt must be TPMLP_F32 when dt is TPMLP_F32.
- * Launch order on `stream`: dH, dB, dA, dX.  For bf16, db1 and db2 run on a second
- * stream that waits for the dA launch (an event recorded on `stream`) and that
- * `stream` waits for after dX, so they run beside the dX GEMM (whose clusters of
- * two CTA pairs leave SMs free) and everything is complete, in stream order, when
- * the work enqueued on `stream` is.  The fork and join are events, so the call can
- * be captured into a CUDA graph.
+ * Launch order on `stream`: dH, dB, then db2 and db1, dA, dX.  For bf16 problems whose
+ * dX GEMM runs on clusters of two CTA pairs (which leave SMs free) and is long enough
+ * (the sums' bytes at most 2.6e-4 per dX flop), db1 and db2 instead run on a second
+ * stream that waits for the dA launch (an event recorded on `stream`) and that `stream`
+ * waits for after dX, so they run beside dX; either way everything is complete, in
+ * stream order, when the work enqueued on `stream` is, and the values are the same bit
+ * for bit.  The fork and join are events, so the call can be captured into a CUDA graph.
  */
 tpmlp_status tpmlp_mlp_bwd(const void* X, const void* A_sh, const void* B_sh, const void* H_sh, const void* Y_sh,
                            const void* dZ, void* dX, void* dA_sh, void* dB_sh, void* db1_sh, void* db2,

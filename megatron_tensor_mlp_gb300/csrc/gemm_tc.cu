@@ -223,6 +223,25 @@ tpmlp_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
     return TPMLP_OK;
 }
 
+// Two CTA pairs per cluster sharing A (multicast): needs an even number of 256-wide N-blocks
+// and runs the direct-store epilogue.  Forced by mode 5; chosen automatically for long K
+// loops when its waves are fuller.  Under the power cap the four-CTA clusters clock higher but
+// leave 8 of 152 SMs idle, and measured per tile the two tilings cost the same, so only the
+// fill of the last wave decides (e.g. the row GEMM at 640 pair tiles: 8.42 waves of 76 pairs
+// against 8.89 waves of 36 clusters).
+template <bool A_MN, bool B_MN, int EPI>
+bool plan_two_pairs(int mode, bool use_pair, int n_blocks, int k_iters, int pair_tiles, int cap,
+                    const DeviceInfo& dev) {
+    if (!use_pair || n_blocks % 2 != 0 || !(mode == 5 || (mode == 0 && k_iters > kStagedMaxKBlocks))) return false;
+    const int cap4 = pair_capacity<A_MN, B_MN, EPI, false, 4>(dev);
+    if (cap4 <= 0) return false;
+    auto fill = [](int tiles, int slots) {
+        const int waves = (tiles + slots - 1) / slots;
+        return static_cast<double>(tiles) / (static_cast<double>(waves) * slots);
+    };
+    return mode == 5 || fill(pair_tiles / 2, cap4) >= fill(pair_tiles, cap) + 0.02;
+}
+
 // Picks the tiling and launches.  CTA-pair 256x256 tiles when there are at least as many
 // of them as co-resident pairs (or when forced); otherwise single-CTA 128x256 tiles, or
 // 128x128 tiles when the 128x256 ones would leave more than half of the SMs idle.
@@ -236,24 +255,7 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
     const bool use_pair = cap > 0 && (mode >= 2 || pair_tiles >= cap);
     constexpr bool kNarrowOk = EPI != EPI_SWIGLU && EPI != EPI_DSWIGLU;  // packed layouts span 256 columns
     const bool narrow = kNarrowOk && !use_pair && 2 * k.num_tiles <= dev.sm_count && g.N > 128;
-    // Two CTA pairs per cluster sharing A (multicast): needs an even number of 256-wide
-    // N-blocks and runs the direct-store epilogue.  Forced by mode 5; chosen automatically
-    // for long K loops when its waves are fuller.  Under the power cap the four-CTA clusters
-    // clock higher but leave 8 of 152 SMs idle, and measured per tile the two tilings cost the
-    // same, so only the fill of the last wave decides (e.g. the row GEMM at 640 pair tiles:
-    // 8.42 waves of 76 pairs against 8.89 waves of 36 clusters).
-    bool quad = false;
-    if (use_pair && k.n_blocks % 2 == 0 && (mode == 5 || (mode == 0 && k.k_iters > kStagedMaxKBlocks))) {
-        const int cap4 = pair_capacity<A_MN, B_MN, EPI, false, 4>(dev);
-        if (cap4 > 0) {
-            const int quad_tiles = pair_tiles / 2;
-            auto fill = [](int tiles, int slots) {
-                const int waves = (tiles + slots - 1) / slots;
-                return static_cast<double>(tiles) / (static_cast<double>(waves) * slots);
-            };
-            quad = mode == 5 || fill(quad_tiles, cap4) >= fill(pair_tiles, cap) + 0.02;
-        }
-    }
+    const bool quad = plan_two_pairs<A_MN, B_MN, EPI>(mode, use_pair, k.n_blocks, k.k_iters, pair_tiles, cap, dev);
     CUtensorMap ma, mb;
     const uint32_t b_rows = (use_pair || narrow) ? tc::BN / 2 : tc::BN;
     // MN-major operands: one 4-D box per stage when the MN extent is a multiple of 64
@@ -395,6 +397,18 @@ tpmlp_status launch_tc_gemm(const Operand& a, const Operand& b, const GemmSpec& 
         if (r != TPMLP_OK) return r;
     }
     return TPMLP_OK;
+}
+
+bool shard_sum_gemm_uses_two_pairs(int64_t M, int64_t N, int64_t K, int64_t shards, const DeviceInfo& dev) {
+    const int mode = g_gemm_mode.load(std::memory_order_relaxed);
+    if (mode == 1 || M <= 0) return false;
+    const int cap = pair_capacity<false, false, EPI_STORE, false>(dev);
+    const int m_pairs = static_cast<int>((M + 2 * tc::BM - 1) / (2 * tc::BM));
+    const int n_blocks = static_cast<int>((N + tc::BN - 1) / tc::BN);
+    const int pair_tiles = m_pairs * n_blocks;
+    const bool use_pair = cap > 0 && (mode >= 2 || pair_tiles >= cap);
+    const int k_iters = static_cast<int>((K + tc::BK - 1) / tc::BK * shards);
+    return plan_two_pairs<false, false, EPI_STORE>(mode, use_pair, n_blocks, k_iters, pair_tiles, cap, dev);
 }
 
 void set_k_chunk_blocks(int blocks) {

@@ -77,6 +77,10 @@ tpmlp_status launch_swiglu_pack(void* G, void* U, void* W_sh, int64_t rows, int6
                                 bool inverse, cudaStream_t st);
 
 // Process-wide GEMM tiling mode (see tpmlp_set_gemm_mode).
+// Whether a shard-summing GEMM with K-major operands and a store epilogue (dX = sum_s A_s B_s of
+// the backwards: per-shard K, `shards` shards) runs on clusters of two CTA pairs, whose launch
+// leaves SMs free (the same decision launch_tc_gemm takes).
+bool shard_sum_gemm_uses_two_pairs(int64_t M, int64_t N, int64_t K, int64_t shards, const DeviceInfo& dev);
 void set_gemm_mode(int mode);
 int get_gemm_mode();
 void set_group_m(int g);

@@ -284,13 +284,21 @@ tpmlp_status side_fork(SideWork* w, cudaStream_t st) {
 tpmlp_status column_bwd_side_sums(const void* X, const void* A_sh, const void* dY_sh, void* dX, void* dA_sh,
                                   void* db1_sh, const void* dZ, void* db2, int64_t M, int64_t h, int64_t ffn, int p,
                                   tpmlp_dtype dt, bool grad_f32, const DeviceInfo& dev, cudaStream_t st) {
-    if (dt != TPMLP_BF16 || (!db1_sh && !db2)) {
+    // Beside dX only where that pays: dX must run on two-pair clusters (which leave SMs free),
+    // and long enough for the sums to finish on those SMs.  Measured: 419 MB of sums beside a
+    // 1.72 TFLOP dX (2.4e-4 byte/flop) finish inside it; 168 MB beside 0.55 TFLOP (3.1e-4) do
+    // not, and the join then delays the step.
+    const int64_t fs = ffn / p;
+    const double sum_bytes = 2.0 * ((db1_sh ? p * M * fs : 0) + (db2 ? M * h : 0));
+    const bool beside = dt == TPMLP_BF16 && (db1_sh || db2) && sum_bytes <= 2.6e-4 * (2.0 * M * h * ffn) &&
+                        shard_sum_gemm_uses_two_pairs(M, h, fs, p, dev);
+    if (!beside) {
         if (db2) TP_TRY(launch_colsum(dZ, dt == TPMLP_F32, 1, M, h, db2, grad_f32, st));
         return do_column_bwd(X, A_sh, dY_sh, dX, dA_sh, db1_sh, M, h, ffn, p, dt, grad_f32, dev, st);
     }
     SideHandles* sh = nullptr;
     TP_TRY(side_handles(dev.device, &sh));
-    SideWork w{dZ, db2, dY_sh, db1_sh, M, h, ffn / p, p, grad_f32, sh->s, sh->fork, sh->join};
+    SideWork w{dZ, db2, dY_sh, db1_sh, M, h, fs, p, grad_f32, sh->s, sh->fork, sh->join};
     TP_TRY(do_column_bwd(X, A_sh, dY_sh, dX, dA_sh, nullptr, M, h, ffn, p, dt, grad_f32, dev, st, &w));
     const cudaError_t e = cudaStreamWaitEvent(st, sh->join, 0);
     if (e != cudaSuccess) {
