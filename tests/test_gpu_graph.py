@@ -3,21 +3,26 @@
 Calls only enqueue kernels on the caller's stream (no allocation, no
 synchronisation), so a forward + backward step captured once replays with
 results identical to eager calls.  Per-device set-up (kernel attributes, the
-pair-kernel occupancy query) happens on the first eager call, before capture.
+pair-kernel occupancy query, the backward's second stream and its two events) happens on
+the first eager call, before capture.  The second shape is large enough for the backward to
+fork its bias-gradient column sums onto the second stream beside the dX GEMM, so the graph
+holds that fork and join too.
 """
 import pytest
 
 pytestmark = pytest.mark.gpu
 
 
-def test_fwd_bwd_step_replays_in_a_cuda_graph():
+@pytest.mark.parametrize("shape", [(64, 8, 512, 2048, 4), (512, 4, 5120, 20480, 4)],
+                         ids=["sums-in-line", "sums-beside-dX"])
+def test_fwd_bwd_step_replays_in_a_cuda_graph(shape):
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from megatron_tensor_mlp_gb300 import harness, synth
     from megatron_tensor_mlp_gb300 import tpmlp as T
 
-    wl = synth.custom(64, 8, 512, 2048, 4, dtype="bf16", seed=5)
+    wl = synth.custom(*shape, dtype="bf16", sigma_w=0.02, seed=5)
     buf = harness.MLPBuffers(wl, backward=True)
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
