@@ -247,9 +247,10 @@ tpmlp_status do_column_bwd(const void* X, const void* A_sh, const void* dY_sh, v
     return TPMLP_OK;
 }
 
-// The bias-gradient column sums of tpmlp_mlp_bwd run on a second stream, forked after the dA
-// GEMM is enqueued and joined after dX: they become ready together with the dX GEMM, whose
-// two-pair clusters leave SMs idle that the (cluster-free) column sums can use.
+// The bias-gradient column sums of the fused backwards (tpmlp_mlp_bwd, tpmlp_swiglu_mlp_bwd) can
+// run on a second stream, forked after the dA GEMM is enqueued and joined after dX: they become
+// ready together with the dX GEMM, whose two-pair clusters leave SMs idle that the cluster-free
+// column sums can use.  One stream and two events per host thread and device, kept.
 struct SideWork {
     const void* dZ; void* db2; const void* dH; void* db1; int64_t M, h, fs, p; bool f32;
     cudaStream_t side; cudaEvent_t fork, join;
@@ -257,13 +258,19 @@ struct SideWork {
 struct SideHandles { cudaStream_t s = nullptr; cudaEvent_t fork = nullptr, join = nullptr; };
 thread_local SideHandles t_side[64];
 tpmlp_status side_handles(int device, SideHandles** out) {
-    if (device < 0 || device >= 64) { set_error("device index %d out of range", device); return TPMLP_ERR_CUDA; }
+    if (device < 0 || device >= 64) {
+        set_error("device index %d out of range", device);
+        return TPMLP_ERR_CUDA;
+    }
     SideHandles& h = t_side[device];
     if (!h.s) {
         cudaError_t e = cudaStreamCreateWithFlags(&h.s, cudaStreamNonBlocking);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.fork, cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.join, cudaEventDisableTiming);
-        if (e != cudaSuccess) { set_error("side stream: %s", cudaGetErrorString(e)); return TPMLP_ERR_CUDA; }
+        if (e != cudaSuccess) {
+            set_error("side stream: %s", cudaGetErrorString(e));
+            return TPMLP_ERR_CUDA;
+        }
     }
     *out = &h;
     return TPMLP_OK;
@@ -271,11 +278,17 @@ tpmlp_status side_handles(int device, SideHandles** out) {
 tpmlp_status side_fork(SideWork* w, cudaStream_t st) {
     cudaError_t e = cudaEventRecord(w->fork, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(w->side, w->fork, 0);
-    if (e != cudaSuccess) { set_error("side stream fork: %s", cudaGetErrorString(e)); return TPMLP_ERR_CUDA; }
+    if (e != cudaSuccess) {
+        set_error("side stream fork: %s", cudaGetErrorString(e));
+        return TPMLP_ERR_CUDA;
+    }
     if (w->db2) TP_TRY(launch_colsum_any_sm(w->dZ, 1, w->M, w->h, w->db2, w->f32, w->side));
     if (w->db1) TP_TRY(launch_colsum_any_sm(w->dH, w->p, w->M, w->fs, w->db1, w->f32, w->side));
     e = cudaEventRecord(w->join, w->side);
-    if (e != cudaSuccess) { set_error("side stream: %s", cudaGetErrorString(e)); return TPMLP_ERR_CUDA; }
+    if (e != cudaSuccess) {
+        set_error("side stream join: %s", cudaGetErrorString(e));
+        return TPMLP_ERR_CUDA;
+    }
     return TPMLP_OK;
 }
 
