@@ -65,3 +65,23 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch):
     class A:
         impl, workload, steps, warmup = "reference", 5, 1, 0
     assert bench.run_reference(A()) is None  # returns immediately, prints nothing
+
+
+def test_reference_arm_line_on_rank_0(monkeypatch, capsys):
+    """Rank 0 prints one JSON line with the contract's keys: the oracle timed on the host cores
+    on a sample of the workload (here the tiny fp32 one, so that the pass is instant)."""
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+
+    class A:
+        impl, workload, steps, warmup = "reference", 1, 2, 1
+    bench.run_reference(A())
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["value"] > 0
+    assert line["steps"] == 2 and line["warmup"] == 1 and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
