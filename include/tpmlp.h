@@ -25,9 +25,10 @@
  *     Y_sh / H_sh / dH [p][M][f/p].  All matrices are row-major.
  *   Memory.  Every pointer is caller-owned device memory (for example
  *     allocated by PyTorch).  The library never allocates device memory,
- *     frees or synchronises inside these calls; workspaces are passed in with
- *     the sizes stated.  (tpmlp_mlp_bwd creates, once per host thread and
- *     device, one non-blocking stream and two events, and keeps them.)  Calls are stream ordered and asynchronous: they return after
+ *     frees or synchronises inside these calls, and creates no streams or
+ *     events: every kernel of a call goes to `stream`, or to a side stream the
+ *     caller has registered (tpmlp_set_side_stream).  Workspaces are passed
+ *     in with the sizes stated.  Calls are stream ordered and asynchronous: they return after
  *     the kernels are enqueued on `stream` (a cudaStream_t; NULL = legacy
  *     default stream).  The GEMM kernels are launched with programmatic
  *     dependent launch: their set-up may overlap the end of the preceding
@@ -127,18 +128,62 @@ tpmlp_status tpmlp_mlp_fwd(const void* X, const void* A_sh, const void* b1_sh, c
  *          db2 [h] (or NULL), all grad_dt (fp32 recommended for bf16 inputs).
  * Workspace: dH_ws [p][M][ffn/p] dt, holds dH on return.
  * Requires ffn % p == 0 and h % p == 0; grad_dt must be TPMLP_F32 when dt is TPMLP_F32.
- * Launch order on `stream`: dH, dB, then db2 and db1, dA, dX.  For bf16 problems whose
- * dX GEMM runs on clusters of two CTA pairs (which leave SMs free) and is long enough
- * (the sums' bytes at most 2.6e-4 per dX flop), db1 and db2 instead run on a second
- * stream that waits for the dA launch (an event recorded on `stream`) and that `stream`
- * waits for after dX, so they run beside dX; either way everything is complete, in
- * stream order, when the work enqueued on `stream` is, and the values are the same bit
- * for bit.  The fork and join are events, so the call can be captured into a CUDA graph.
+ * Launch order on `stream`: dH, dB, db2, db1, dA, dX (db1 and db2 beside dX on a side stream
+ * of the caller's where one is registered: tpmlp_set_side_stream).
  */
 tpmlp_status tpmlp_mlp_bwd(const void* X, const void* A_sh, const void* B_sh, const void* H_sh, const void* Y_sh,
                            const void* dZ, void* dX, void* dA_sh, void* dB_sh, void* db1_sh, void* db2,
                            void* dH_ws, int64_t s, int64_t b, int64_t h, int64_t ffn, int p,
                            tpmlp_dtype dt, tpmlp_dtype grad_dt, void* stream);
+
+/*
+ * The block with its shards spread over several GPUs: what one rank computes
+ * ("分布式并行训练全景", 考点 2: each card holds a column slice A_i of the first
+ * weight and the matching row slice B_i of the second, computes GeLU(X A_i) B_i
+ * with no exchange in between, and one All-Reduce sums the partials; Level 2,
+ * M025 追问: in the backward the weight gradients stay local and the dX
+ * contributions are summed by an All-Reduce; M027: the sum comes once, at the
+ * end of the block).  The exchange itself is the caller's (NCCL or any other
+ * collective); these calls compute the rank-local parts on this GPU and the
+ * step after the sum.
+ *
+ * tpmlp_mlp_fwd_partial: this rank's p local shards (its slice of A's columns,
+ * b1 and B's rows, laid out as in tpmlp_mlp_fwd with ffn = the rank's FFN width)
+ *   H_i = X A_i + b1_i,  Y_i = GeLU(H_i),  Z_part = sum_{local i} Y_i B_i
+ *   Z_part [M, h] fp32 output (no b2: it is added once, after the All-Reduce,
+ *   by tpmlp_sum_finish); Y_ws, H_sh and the requirements as in tpmlp_mlp_fwd.
+ *   With every shard on one rank, Z = round(Z_part + b2) is tpmlp_mlp_fwd's
+ *   result up to the fp32 summation order.
+ */
+tpmlp_status tpmlp_mlp_fwd_partial(const void* X, const void* A_sh, const void* b1_sh, const void* B_sh,
+                                   float* Z_part, void* Y_ws, void* H_sh,
+                                   int64_t s, int64_t b, int64_t h, int64_t ffn, int p,
+                                   tpmlp_dtype dt, void* stream);
+
+/*
+ * tpmlp_mlp_bwd_partial: the rank-local backward.  As tpmlp_mlp_bwd on this
+ * rank's shards (dH, dA_i, dB_i, db1_i all local; db2 = 1^T dZ needs only the
+ * replicated dZ, so every rank gets the whole of it), except that dX_part
+ * [M, h] fp32 receives this rank's contribution sum_{local i} dH_i A_i^T, to be
+ * summed over the ranks by the caller's All-Reduce and rounded by
+ * tpmlp_sum_finish (bias NULL).  Launch order on `stream`: dH, dB, db2, db1,
+ * dA, dX_part (the sums on a registered side stream as in tpmlp_mlp_bwd).
+ */
+tpmlp_status tpmlp_mlp_bwd_partial(const void* X, const void* A_sh, const void* B_sh, const void* H_sh,
+                                   const void* Y_sh, const void* dZ, float* dX_part, void* dA_sh, void* dB_sh,
+                                   void* db1_sh, void* db2, void* dH_ws, int64_t s, int64_t b, int64_t h,
+                                   int64_t ffn, int p, tpmlp_dtype dt, tpmlp_dtype grad_dt, void* stream);
+
+/*
+ * The step after the All-Reduce of fp32 partial sums (考点 2; M026: b2 is added
+ * once, to the sum, never per rank):
+ *   out[r][c] = round_dt(S[r][c] + bias[c])
+ *   S [rows, cols] fp32 (the summed partials), bias [cols] dt or NULL,
+ *   out [rows, cols] dt (bf16: rounded to nearest even; fp32: the sum itself).
+ * cols must be a multiple of 8 (bf16) or 4 (fp32); out must not overlap S or bias.
+ */
+tpmlp_status tpmlp_sum_finish(const float* S, const void* bias, void* out, int64_t rows, int64_t cols,
+                              tpmlp_dtype dt, void* stream);
 
 /*
  * Row-parallel layer backward (Level 2, M026: the row layer's input gradient is
@@ -195,7 +240,8 @@ tpmlp_status tpmlp_swiglu_mlp_fwd(const void* X, const void* W_sh, const void* b
  * Inputs: X, W_sh, B_sh, Y_ws and dZ (bf16); H_ws (packed fp32 pre-activations from the forward).
  * Outputs: dX bf16; dW_sh [p][h][2 ffn/p], dB_sh, dbw_sh [p][2 ffn/p] (or NULL), db2 (or NULL) grad_dt.
  * Workspace: dH_ws [p][M][2 ffn/p] bf16 (holds the packed dHg, dHu on return).
- * As in tpmlp_mlp_bwd, dbw and db2 run on the second stream beside the dX GEMM.
+ * Launch order on `stream`: the dY GEMM with the SwiGLU' epilogue, dB, db2, dbw, dW, dX (db2
+ * and dbw beside dX where a side stream is registered, as in tpmlp_mlp_bwd).
  */
 tpmlp_status tpmlp_swiglu_mlp_bwd(const void* X, const void* W_sh, const void* B_sh, const void* H_ws,
                                   const void* Y_ws, const void* dZ, void* dX, void* dW_sh, void* dB_sh, void* dbw_sh,
@@ -224,7 +270,13 @@ tpmlp_status tpmlp_swiglu_pack(void* G, void* U, void* W_sh, int64_t rows, int64
  *   This call allocates nothing (no cudaMalloc, no allocating library routine).
  *   The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current) and caches it; make that
- *   first call before any stream capture.
+ *   first call before any stream capture.  Under CUDA's lazy module loading
+ *   (the default) that first look-up, or the first launch of a kernel of this
+ *   library, may load the library's code onto the device, and loading creates
+ *   the array there: device memory that the driver takes at that moment.  A
+ *   caller that must not see any allocation after start-up makes one call at
+ *   start-up (or sets CUDA_MODULE_LOADING=EAGER) before its no-allocation
+ *   region; later calls take no device memory.
  *   Every call shares the one array per device and it keeps the last call's
  *   contents; each call overwrites all of the Y it reads, so nothing needs
  *   clearing.  Calls whose kernels overlap on the GPU (different streams, or
@@ -279,20 +331,37 @@ tpmlp_status tpmlp_device_status(void* stream);
 tpmlp_status tpmlp_debug_wait_timeout(uint32_t timeout_us, void* stream);
 
 /*
+ * Optional side stream for the fused backwards (tpmlp_mlp_bwd, tpmlp_mlp_bwd_partial,
+ * tpmlp_swiglu_mlp_bwd).  Their bias-gradient column sums (db1 = 1^T dH, db2 = 1^T dZ) need
+ * no tensor cores; with a stream and two events of the caller's registered here, they run
+ * on that stream beside the dX GEMM, on the SMs its last wave of tiles leaves idle: the
+ * side stream waits for an event recorded on `stream` after the dA launch, and `stream`
+ * waits for an event recorded on the side stream after the sums, so everything is
+ * complete, in order, when the work enqueued on `stream` is.  The sums go there only
+ * where it pays: bf16 tensors, dX's last wave keeping at most half of the CTA pairs busy,
+ * and at most 2.6e-4 bytes of sums per dX flop (the fwd+bwd bench workload qualifies);
+ * elsewhere, and with nothing registered, they run in line on `stream`.  Either way the
+ * results are the same bit for bit.
+ *   The registration is per host thread and bound to the device current at this call;
+ *   the stream must belong to that device.  The library never creates, destroys or
+ *   synchronises these objects: the caller keeps them alive while registered (events
+ *   created with cudaEventDisableTiming suffice).  All three NULL clears it.
+ *   TPMLP_ERR_NULL if only some are NULL; TPMLP_ERR_CUDA if no device can be queried.
+ */
+tpmlp_status tpmlp_set_side_stream(void* side_stream, void* fork_event, void* join_event);
+
+/*
  * Tiling of the bf16 GEMMs, process wide.  0 = automatic (default): 256x256 tiles
  * on CTA pairs when there are enough of them to fill the GPU, else single-CTA
  * tiles (128x256, or 128x128 when 128x256 tiles would leave more than half of the
  * SMs idle); CTA-pair tiles store their outputs directly from registers, or, when
  * a tile's K loop is short (at most 40 blocks of 64), through shared memory with
- * TMA stores; long-K GEMMs run on clusters of two CTA pairs (as in 5) when those
- * fill their last wave at least 2 points better than single pairs.  1 = single-CTA tiles only; 2 = CTA-pair tiles only (epilogue chosen
+ * TMA stores.  1 = single-CTA tiles only; 2 = CTA-pair tiles only (epilogue chosen
  * as in 0); 3 = CTA-pair tiles, direct stores; 4 = CTA-pair tiles, TMA stores (the
  * SwiGLU epilogues, and the later launches of a split contraction that add to their
- * output, always store directly); 5 = clusters of two CTA pairs that
- * compute neighbouring 256-column tiles and share each A tile through TMA
- * multicast (direct stores; GEMMs with an odd number of 256-column blocks fall back
- * to 2).  Results agree within rounding in every mode; the control exists for
- * tuning and tests.  TPMLP_ERR_SHAPE for other values.
+ * output, always store directly).  Every TMA load lands in the shared memory of the
+ * CTA that issues it (no cluster multicast).  Results agree within rounding in every
+ * mode; the control exists for tuning and tests.  TPMLP_ERR_SHAPE for other values.
  */
 tpmlp_status tpmlp_set_gemm_mode(int mode);
 int tpmlp_get_gemm_mode(void);

@@ -92,7 +92,7 @@ bool make_out_map(CUtensorMap* map, void* ptr, int64_t ld, int64_t ss, uint64_t 
 // main loop takes ~512 cycles per 64-wide K block, a direct-store epilogue ~10-20 k cycles.
 constexpr int kStagedMaxKBlocks = 40;
 
-// 0 auto, 1 single-CTA, 2 pair, 3 pair + direct stores, 4 pair + TMA stores, 5 two pairs per cluster
+// 0 auto, 1 single-CTA, 2 pair, 3 pair + direct stores, 4 pair + TMA stores
 std::atomic<int> g_gemm_mode{0};
 std::atomic<int> g_group_m{16};  // M-blocks per raster group
 // K blocks per launch of a split fp32 contraction (see launch_tc_gemm)
@@ -165,25 +165,25 @@ tpmlp_status launch_single(const CUtensorMap& ma, const CUtensorMap& mb, const t
     return TPMLP_OK;
 }
 
-// Co-resident clusters (of CL / 2 CTA pairs) of the pair kernel on this device (0 if it cannot run).
-template <bool A_MN, bool B_MN, int EPI, bool STAGED, int CL = 2>
+// Co-resident CTA pairs (clusters of two) of the pair kernel on this device (0 if it cannot run).
+template <bool A_MN, bool B_MN, int EPI, bool STAGED>
 int pair_capacity(const DeviceInfo& dev) {
     static int cap[64];
     static bool done[64];
     static bool attr_done[64] = {};
     if (dev.device >= 64) return 0;
     if (done[dev.device]) return cap[dev.device];
-    auto kern = tc::gemm_pair_kernel<A_MN, B_MN, EPI, STAGED, CL>;
+    auto kern = tc::gemm_pair_kernel<A_MN, B_MN, EPI, STAGED>;
     constexpr int smem = tc::PairGeom<STAGED>::smem_bytes;
     int n = 0;
     if (set_smem_attr(kern, dev.device, smem, attr_done)) {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(CL * (dev.sm_count / CL));
+        cfg.gridDim = dim3(2 * (dev.sm_count / 2));
         cfg.blockDim = dim3(tc::PairGeom<STAGED>::threads);
         cfg.dynamicSmemBytes = smem;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = CL;
+        attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
@@ -196,18 +196,18 @@ int pair_capacity(const DeviceInfo& dev) {
     return n;
 }
 
-template <bool A_MN, bool B_MN, int EPI, bool STAGED, int CL = 2>
+template <bool A_MN, bool B_MN, int EPI, bool STAGED>
 tpmlp_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
                          const CUtensorMap& mo2, const tc::KArgs& k, int clusters, cudaStream_t st) {
-    auto kern = tc::gemm_pair_kernel<A_MN, B_MN, EPI, STAGED, CL>;
+    auto kern = tc::gemm_pair_kernel<A_MN, B_MN, EPI, STAGED>;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(CL * clusters);
+    cfg.gridDim = dim3(2 * clusters);
     cfg.blockDim = dim3(tc::PairGeom<STAGED>::threads);
     cfg.dynamicSmemBytes = tc::PairGeom<STAGED>::smem_bytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddep_wait
@@ -223,25 +223,6 @@ tpmlp_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
     return TPMLP_OK;
 }
 
-// Two CTA pairs per cluster sharing A (multicast): needs an even number of 256-wide N-blocks
-// and runs the direct-store epilogue.  Forced by mode 5; chosen automatically for long K
-// loops when its waves are fuller.  Under the power cap the four-CTA clusters clock higher but
-// leave 8 of 152 SMs idle, and measured per tile the two tilings cost the same, so only the
-// fill of the last wave decides (e.g. the row GEMM at 640 pair tiles: 8.42 waves of 76 pairs
-// against 8.89 waves of 36 clusters).
-template <bool A_MN, bool B_MN, int EPI>
-bool plan_two_pairs(int mode, bool use_pair, int n_blocks, int k_iters, int pair_tiles, int cap,
-                    const DeviceInfo& dev) {
-    if (!use_pair || n_blocks % 2 != 0 || !(mode == 5 || (mode == 0 && k_iters > kStagedMaxKBlocks))) return false;
-    const int cap4 = pair_capacity<A_MN, B_MN, EPI, false, 4>(dev);
-    if (cap4 <= 0) return false;
-    auto fill = [](int tiles, int slots) {
-        const int waves = (tiles + slots - 1) / slots;
-        return static_cast<double>(tiles) / (static_cast<double>(waves) * slots);
-    };
-    return mode == 5 || fill(pair_tiles / 2, cap4) >= fill(pair_tiles, cap) + 0.02;
-}
-
 // Picks the tiling and launches.  CTA-pair 256x256 tiles when there are at least as many
 // of them as co-resident pairs (or when forced); otherwise single-CTA 128x256 tiles, or
 // 128x128 tiles when the 128x256 ones would leave more than half of the SMs idle.
@@ -255,13 +236,12 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
     const bool use_pair = cap > 0 && (mode >= 2 || pair_tiles >= cap);
     constexpr bool kNarrowOk = EPI != EPI_SWIGLU && EPI != EPI_DSWIGLU;  // packed layouts span 256 columns
     const bool narrow = kNarrowOk && !use_pair && 2 * k.num_tiles <= dev.sm_count && g.N > 128;
-    const bool quad = plan_two_pairs<A_MN, B_MN, EPI>(mode, use_pair, k.n_blocks, k.k_iters, pair_tiles, cap, dev);
     CUtensorMap ma, mb;
     const uint32_t b_rows = (use_pair || narrow) ? tc::BN / 2 : tc::BN;
     // MN-major operands: one 4-D box per stage when the MN extent is a multiple of 64
-    k.a_chunked = (a.mn_major && g.M % 64 == 0 && !quad) ? 1 : 0;
+    k.a_chunked = (a.mn_major && g.M % 64 == 0) ? 1 : 0;
     k.b_chunked = (b.mn_major && g.N % 64 == 0) ? 1 : 0;
-    const uint32_t a_rows = quad ? tc::BM / 2 : tc::BM;  // K-major A box: half a slice per CTA when shared
+    const uint32_t a_rows = tc::BM;
     bool ok;
     if (k.a_chunked) ok = make_map_chunked(&ma, a, g.M, g.K, tc::BM / 64);
     else ok = a.mn_major ? make_map(&ma, a, g.M, g.K, 64, tc::BK) : make_map(&ma, a, g.K, g.M, tc::BK, a_rows);
@@ -281,13 +261,6 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
     }
     k.m_blocks = m_pairs;
     k.num_tiles = pair_tiles;
-    if (quad) {
-        k.n_blocks /= 2;  // the kernel decodes 256x512 blocks; pair q takes N-block 2 nb + q
-        k.num_tiles = m_pairs * k.n_blocks * k.batch;
-        const int cap4 = pair_capacity<A_MN, B_MN, EPI, false, 4>(dev);
-        return launch_pair<A_MN, B_MN, EPI, false, 4>(ma, mb, ma, ma, k, k.num_tiles < cap4 ? k.num_tiles : cap4,
-                                                      st);
-    }
     const int clusters = pair_tiles < cap ? pair_tiles : cap;
     // Short K loops (a tile's main loop shorter than a direct-store epilogue): staged epilogue.
     if constexpr (kNarrowOk) {
@@ -364,6 +337,7 @@ tpmlp_status launch_one(const Operand& a, const Operand& b, const GemmSpec& g, c
     if (g.epi == EPI_SWIGLU && !amn && bmn) return launch_variant<false, true, EPI_SWIGLU>(a, b, g, k, dev, st);
     if (g.epi == EPI_DSWIGLU && !amn && !bmn) return launch_variant<false, false, EPI_DSWIGLU>(a, b, g, k, dev, st);
     if (g.epi == EPI_STORE && amn && bmn) return launch_variant<true, true, EPI_STORE>(a, b, g, k, dev, st);
+    if (g.epi == EPI_STORE && !amn && bmn) return launch_variant<false, true, EPI_STORE>(a, b, g, k, dev, st);
     if (g.epi == EPI_STORE && !amn && !bmn) return launch_variant<false, false, EPI_STORE>(a, b, g, k, dev, st);
     set_error("internal: no tcgen05 GEMM variant for epi=%d a_mn=%d b_mn=%d", g.epi, (int)amn, (int)bmn);
     return TPMLP_ERR_CUDA;
@@ -399,16 +373,16 @@ tpmlp_status launch_tc_gemm(const Operand& a, const Operand& b, const GemmSpec& 
     return TPMLP_OK;
 }
 
-bool shard_sum_gemm_uses_two_pairs(int64_t M, int64_t N, int64_t K, int64_t shards, const DeviceInfo& dev) {
+double shard_sum_gemm_last_wave_fill(int64_t M, int64_t N, const DeviceInfo& dev) {
     const int mode = g_gemm_mode.load(std::memory_order_relaxed);
-    if (mode == 1 || M <= 0) return false;
+    if (mode == 1 || M <= 0) return 0.0;
     const int cap = pair_capacity<false, false, EPI_STORE, false>(dev);
     const int m_pairs = static_cast<int>((M + 2 * tc::BM - 1) / (2 * tc::BM));
     const int n_blocks = static_cast<int>((N + tc::BN - 1) / tc::BN);
     const int pair_tiles = m_pairs * n_blocks;
-    const bool use_pair = cap > 0 && (mode >= 2 || pair_tiles >= cap);
-    const int k_iters = static_cast<int>((K + tc::BK - 1) / tc::BK * shards);
-    return plan_two_pairs<false, false, EPI_STORE>(mode, use_pair, n_blocks, k_iters, pair_tiles, cap, dev);
+    if (cap <= 0 || !(mode >= 2 || pair_tiles >= cap)) return 0.0;
+    const int last = pair_tiles % cap;
+    return last == 0 ? 1.0 : static_cast<double>(last) / cap;
 }
 
 void set_k_chunk_blocks(int blocks) {

@@ -828,15 +828,9 @@ __device__ __forceinline__ void epilogue_tile_staged(const KArgs& p, const CUten
 //                   warps 4-11 (4-7): epilogue of its 128 rows; the accumulator
 //                            is released by 16 (8) arrivals on the leader's barrier
 //
-// CL = 4 (two pairs per cluster, direct-store epilogue only): pair q = r / 2
-// computes N-block 2 nbs + q of the cluster's 256x512 output block, so both
-// pairs need the same A rows.  CTA r loads half of its 128-row A slice (rows
-// or MN chunk q, 8 KiB) and multicasts it to itself and CTA r ^ 2; every copy
-// completes on its destination pair's leader barrier, and a stage is free once
-// both pairs' UMMAs have read it (empty barriers count both leaders' commits).
-// Each A tile leaves L2 once per cluster instead of once per pair (measured:
-// 11-13 % fewer L2 read sectors), at the cost of the 8 SMs that four-CTA
-// clusters leave unused.
+// Every TMA load lands in the issuing CTA's own shared memory (no multicast):
+// the library may run on every GPU of a multi-GPU job, and each operand byte is
+// already read once per pair.
 // ============================================================================
 constexpr int P_A_BYTES = BM * BK * 2;        // 16 KiB: this CTA's 128 rows of A
 constexpr int P_B_BYTES = (BN / 2) * BK * 2;  // 16 KiB: this CTA's 128 columns of B
@@ -862,13 +856,11 @@ struct PairGeom {
     static_assert(smem_bytes <= 227 * 1024, "pair kernel shared memory");
 };
 
-template <bool A_MN, bool B_MN, int EPI, bool STAGED, int CL>
+template <bool A_MN, bool B_MN, int EPI, bool STAGED>
 __global__ void __launch_bounds__(PairGeom<STAGED>::threads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2,
                      const KArgs p) {
-    static_assert(CL == 2 || (CL == 4 && !STAGED), "cluster of one or two CTA pairs");
-    constexpr bool QUAD = CL == 4;
     constexpr int P_STAGES = PairGeom<STAGED>::stages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -884,19 +876,17 @@ __global__ void __launch_bounds__(PairGeom<STAGED>::threads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
-    const uint32_t prank = rank & 1u;          // position in the CTA pair
-    const uint32_t pleader = rank & ~1u;       // the pair's leader (UMMA issuer)
-    const int pq = static_cast<int>(rank >> 1);  // pair index in the cluster
+    const uint32_t prank = cluster_ctarank();  // position in the CTA pair
+    const uint32_t pleader = 0;                // the pair's leader (UMMA issuer)
     const bool leader = prank == 0;
-    const uint16_t pair_mask = static_cast<uint16_t>(0x3u << pleader);
-    const int cluster_id = blockIdx.x / CL;
-    const int n_clusters = gridDim.x / CL;
+    const uint16_t pair_mask = 0x3;
+    const int cluster_id = blockIdx.x / 2;
+    const int n_clusters = gridDim.x / 2;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < P_STAGES; ++s) {
             mbar_init(full + s, 1);
-            mbar_init(empty + s, QUAD ? 2 : 1);
+            mbar_init(empty + s, 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull + a, 1);
@@ -943,7 +933,6 @@ __global__ void __launch_bounds__(PairGeom<STAGED>::threads, 1)
             for (int t = cluster_id; t < p.num_tiles && ok; t += n_clusters, ++lt) {
                 int mb, nb, shard;
                 decode_tile(p, t, mb, nb, shard);
-                if constexpr (QUAD) nb = 2 * nb + pq;
                 const int row0 = mb * (2 * BM) + static_cast<int>(prank) * BM;
                 const int col0 = nb * BN + static_cast<int>(prank) * (BN / 2);
                 // Odd waves walk K backwards: a tile of the next wave usually shares its
@@ -967,15 +956,7 @@ __global__ void __launch_bounds__(PairGeom<STAGED>::threads, 1)
                     const uint32_t bar = full_leader0 + stage * 8;
                     uint8_t* a_dst = sA + stage * P_A_BYTES;
                     uint8_t* b_dst = sB + stage * P_B_BYTES;
-                    if constexpr (QUAD) {
-                        // half of this CTA's A slice (64 rows, or MN chunk pq: 8 KiB at the same
-                        // offset either way), to this CTA and its counterpart in the other pair
-                        const uint16_t mc = static_cast<uint16_t>(0x5u << prank);
-                        if constexpr (!A_MN)
-                            tma_load_3d_pair_mc(a_dst + pq * (P_A_BYTES / 2), &tmA, bar, k0, row0 + pq * 64, sa, mc);
-                        else
-                            tma_load_3d_pair_mc(a_dst + pq * MN_CHUNK_BYTES, &tmA, bar, row0 + pq * 64, k0, sa, mc);
-                    } else if constexpr (!A_MN) {
+                    if constexpr (!A_MN) {
                         tma_load_3d_pair(a_dst, &tmA, bar, k0, row0, sa);
                     } else if (p.a_chunked) {
                         tma_load_4d_pair(a_dst, &tmA, bar, 0, k0, row0 / 64, sa);
@@ -1016,7 +997,7 @@ __global__ void __launch_bounds__(PairGeom<STAGED>::threads, 1)
             }
             if (ok) {
                 // The UMMA commits that release stages arrive on this CTA's empty barriers from
-                // one or both pair leaders, possibly on other SMs, and nothing else orders them
+                // the pair leader, possibly on the other SM, and nothing else orders them
                 // before the cluster's final barrier: wait for the release of every stage's last
                 // use, so that no arrival can reach this CTA's shared memory after it exits.
                 for (int i = 0; i < P_STAGES; ++i) {
@@ -1035,9 +1016,9 @@ __global__ void __launch_bounds__(PairGeom<STAGED>::threads, 1)
                             mbar_wait_bounded(full + s, (last_parity >> s) & 1u, p.status, p.timeout_ns, kWhereDrain,
                                               /*watch_status=*/false);
                 }
-                // let this CTA's last copies (and, in a cluster of two pairs, its multicasts
-                // into the other pair) land before any CTA of the cluster can exit
-                if (!leader || QUAD) spin_ns(200000);
+                // let this CTA's last copies (counted on the leader's barriers) land before
+                // either CTA of the pair can exit
+                if (!leader) spin_ns(200000);
             }
         }
     } else if (warp == 1) {
@@ -1076,8 +1057,8 @@ __global__ void __launch_bounds__(PairGeom<STAGED>::threads, 1)
                         for (int kk = 0; kk < BK / 16; ++kk)
                             umma_f16_pair(d_tmem, adesc + kk * a_kstep, bdesc + kk * b_kstep, idesc,
                                           (it | kk) != 0 ? 1u : 0u);
-                        // the stage is free for the producers of every CTA whose copies it holds
-                        umma_commit_pair_mc(empty + stage, QUAD ? 0xF : 0x3);
+                        // the stage is free for the producers of both CTAs
+                        umma_commit_pair_mc(empty + stage, pair_mask);
                         if (++stage == P_STAGES) {
                             stage = 0;
                             phase ^= 1u;
@@ -1091,7 +1072,7 @@ __global__ void __launch_bounds__(PairGeom<STAGED>::threads, 1)
                 for (int i = 0; ok && i < 2; ++i, ++lt)
                     ok = mbar_wait_bounded(tempty + (lt & 1), ((lt >> 1) & 1) ^ 1u, p.status, p.timeout_ns, kWhereDrain);
             }
-            // both CTAs: every UMMA (and its multicast arrivals) is done once `drain` flips
+            // both CTAs: every UMMA (and its commit arrivals) is done once `drain` flips
             mbar_wait_bounded(drain, 0, p.status, p.timeout_ns, kWhereDrain, /*watch_status=*/false);
         }
     } else if (warp >= FIRST_EPI_WARP) {
@@ -1112,7 +1093,6 @@ __global__ void __launch_bounds__(PairGeom<STAGED>::threads, 1)
             tc_fence_after();
             int mb, nb, shard;
             decode_tile(p, t, mb, nb, shard);
-            if constexpr (QUAD) nb = 2 * nb + pq;
             const int row0 = mb * (2 * BM) + static_cast<int>(prank) * BM + q * 32;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
             if constexpr (STAGED) {

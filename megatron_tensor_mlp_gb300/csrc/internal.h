@@ -65,6 +65,7 @@ tpmlp_status launch_simt_gemm(const Operand& a, const Operand& b, const GemmSpec
 // out[s][n] = sum_m in[s][m][n]; in bf16 or f32 (in_f32), out f32 or bf16 (out_f32)
 tpmlp_status launch_colsum(const void* in, bool in_f32, int64_t shards, int64_t M, int64_t N, void* out,
                            bool out_f32, cudaStream_t st);
+// bf16 column sums without clusters, bit-identical to launch_colsum's (any free SM can run them)
 tpmlp_status launch_colsum_any_sm(const void* in, int64_t shards, int64_t M, int64_t N, void* out, bool out_f32,
                                   cudaStream_t st);
 tpmlp_status launch_shard_columns(const void* src, void* dst, int64_t rows, int64_t cols, int p, int esize,
@@ -72,15 +73,18 @@ tpmlp_status launch_shard_columns(const void* src, void* dst, int64_t rows, int6
 tpmlp_status launch_qkv_interleave(const void* src, void* dst, int64_t rows, int64_t h, int64_t n_heads,
                                    int esize, bool inverse, cudaStream_t st);
 tpmlp_status launch_debug_wait(uint32_t timeout_us, uint32_t* status, cudaStream_t st);
+// out[r][c] = S[r][c] + bias[c] rounded to the output type (bf16, or fp32 when out_f32)
+tpmlp_status launch_sum_finish(const float* S, const void* bias, void* out, int64_t rows, int64_t cols, bool out_f32,
+                               int sm_count, cudaStream_t st);
 // SwiGLU packed layout: W_sh[i][r][256 b + j] = (j < 128 ? G : U)[r][i fs + 128 b + j % 128]
 tpmlp_status launch_swiglu_pack(void* G, void* U, void* W_sh, int64_t rows, int64_t ffn, int p, int esize,
                                 bool inverse, cudaStream_t st);
 
 // Process-wide GEMM tiling mode (see tpmlp_set_gemm_mode).
-// Whether a shard-summing GEMM with K-major operands and a store epilogue (dX = sum_s A_s B_s of
-// the backwards: per-shard K, `shards` shards) runs on clusters of two CTA pairs, whose launch
-// leaves SMs free (the same decision launch_tc_gemm takes).
-bool shard_sum_gemm_uses_two_pairs(int64_t M, int64_t N, int64_t K, int64_t shards, const DeviceInfo& dev);
+// Fraction of the CTA pairs that the last wave of a shard-summing GEMM with K-major operands and
+// a store epilogue (dX = sum_s A_s B_s of the backwards: per-shard K, `shards` shards) keeps busy:
+// 1 for whole waves, 0 when it does not run on CTA pairs (the same tiling decision as launch_tc_gemm).
+double shard_sum_gemm_last_wave_fill(int64_t M, int64_t N, const DeviceInfo& dev);
 void set_gemm_mode(int mode);
 int get_gemm_mode();
 void set_group_m(int g);

@@ -195,7 +195,7 @@ __global__ void __cluster_dims__(1, CS_CLUSTER, 1) __launch_bounds__(CS_WARPS * 
 // of the 8-CTA cluster above in the same order (accumulator set g holds what CTA g of the
 // cluster sums: warp w takes rows 16 g + w + 128 i in increasing order; then each set is added
 // over the 16 warps, and the sets over g), so the results are bit-identical to that kernel's,
-// and any free SM can run it, e.g. beside a GEMM whose clusters leave SMs idle.
+// and any free SM can run it, e.g. beside a GEMM whose last wave leaves SMs idle.
 template <bool OUT_F32>
 __global__ void __launch_bounds__(CS_WARPS * 32)
     colsum_bf16_strip_kernel(const __nv_bfloat16* __restrict__ in, long long M, long long N, void* out) {
@@ -296,6 +296,57 @@ __global__ void swiglu_pack_kernel(uint4* __restrict__ G, uint4* __restrict__ U,
         uint4* src = (j < 128 ? G : U) + (r * f + src_col) / u;
         if (!inverse) W[x] = *src;
         else *src = W[x];
+    }
+}
+
+// ------------------------------------------------------------------ sum finish
+// The step after an All-Reduce of fp32 partial sums: out = round(S + bias), bias added once.
+// Each thread takes 8 consecutive columns (bf16 out: two 16-byte loads of S, one 16-byte bias
+// load, one 16-byte store) or 4 (fp32 out), in a grid-stride loop; cols is a multiple of 8
+// (bf16) or 4 (fp32), so a group never crosses a row.
+template <bool OUT_F32>
+__global__ void __launch_bounds__(256) sum_finish_kernel(const float* __restrict__ S, const void* __restrict__ bias,
+                                                         void* __restrict__ out, long long rows, long long cols) {
+    constexpr int V = OUT_F32 ? 4 : 8;
+    const long long groups_per_row = cols / V;
+    const long long total = rows * groups_per_row;
+    for (long long u = blockIdx.x * (long long)blockDim.x + threadIdx.x; u < total;
+         u += (long long)gridDim.x * blockDim.x) {
+        const long long r = u / groups_per_row;
+        const long long c = (u - r * groups_per_row) * V;
+        const float* src = S + r * cols + c;
+        if constexpr (OUT_F32) {
+            float4 v = *reinterpret_cast<const float4*>(src);
+            if (bias != nullptr) {
+                const float4 bb = *reinterpret_cast<const float4*>(static_cast<const float*>(bias) + c);
+                v.x += bb.x;
+                v.y += bb.y;
+                v.z += bb.z;
+                v.w += bb.w;
+            }
+            *reinterpret_cast<float4*>(static_cast<float*>(out) + r * cols + c) = v;
+        } else {
+            const float4 lo = *reinterpret_cast<const float4*>(src);
+            const float4 hi = *reinterpret_cast<const float4*>(src + 4);
+            float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+            if (bias != nullptr) {
+                const uint4 bw = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(bias) + c);
+                const uint32_t w[4] = {bw.x, bw.y, bw.z, bw.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[2 * i] += __uint_as_float(w[i] << 16);
+                    v[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+                }
+            }
+            uint4 o;
+            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                __nv_bfloat162 pr = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                ow[i] = *reinterpret_cast<uint32_t*>(&pr);
+            }
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + r * cols + c) = o;
+        }
     }
 }
 
@@ -419,6 +470,18 @@ tpmlp_status launch_swiglu_pack(void* G, void* U, void* W_sh, int64_t rows, int6
                                                               static_cast<uint4*>(W_sh), rows, ffn, fs, p, u,
                                                               inverse ? 1 : 0);
     return check_launch("SwiGLU pack");
+}
+
+tpmlp_status launch_sum_finish(const float* S, const void* bias, void* out, int64_t rows, int64_t cols, bool out_f32,
+                               int sm_count, cudaStream_t st) {
+    const long long groups = rows * (cols / (out_f32 ? 4 : 8));
+    long long blocks = (groups + 255) / 256;
+    const long long cap = static_cast<long long>(sm_count > 0 ? sm_count : 1) * 8;  // 8 x 256 threads per SM
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (out_f32) sum_finish_kernel<true><<<(unsigned)blocks, 256, 0, st>>>(S, bias, out, rows, cols);
+    else sum_finish_kernel<false><<<(unsigned)blocks, 256, 0, st>>>(S, bias, out, rows, cols);
+    return check_launch("sum finish");
 }
 
 tpmlp_status launch_debug_wait(uint32_t timeout_us, uint32_t* status, cudaStream_t st) {

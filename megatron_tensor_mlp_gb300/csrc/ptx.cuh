@@ -212,18 +212,6 @@ __device__ __forceinline__ void tma_load_4d_pair(void* smem_dst, const CUtensorM
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar_cluster_addr)
         : "memory");
 }
-// Multicast form of tma_load_3d_pair: the box lands at the same shared-memory offset in
-// every CTA of `cta_mask`, and each destination's bytes are counted on the mbarrier at
-// `bar_cluster_addr`'s offset in the leader (even rank) of that destination's CTA pair
-// (the address must name an even-ranked CTA).
-__device__ __forceinline__ void tma_load_3d_pair_mc(void* smem_dst, const CUtensorMap* map, uint32_t bar_cluster_addr,
-                                                    int32_t x, int32_t y, int32_t z, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster_addr), "h"(cta_mask)
-        : "memory");
-}
 // TMEM allocation shared by the CTA pair (one warp of each CTA executes these).
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* smem_slot, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_slot)),

@@ -180,6 +180,21 @@ tpmlp_status do_row(const void* Y_sh, const void* B_sh, const void* b2, void* Z,
     return run_gemm(a, b, g, dt, dev, st);
 }
 
+// Row layer without the bias, its shard sum left in fp32: Z_part = sum_i Y_i B_i over the shards
+// given (a rank's partial of a block whose shards are spread over several GPUs).
+tpmlp_status do_row_partial(const void* Y_sh, const void* B_sh, float* Z_part, int64_t M, int64_t h, int64_t ffn,
+                            int p, tpmlp_dtype dt, const DeviceInfo& dev, cudaStream_t st) {
+    const int64_t fs = ffn / p;
+    Operand a{Y_sh, fs, M * fs, p, false};            // Y_i [M][fs], K-major
+    Operand b{B_sh, h, fs * h, p, true};              // B_i [fs][h]: [K][N], MN-major
+    GemmSpec g = spec_base();
+    g.M = M; g.N = h; g.K = fs; g.n_shards = p;
+    g.sum_shards = true;
+    g.epi = EPI_STORE; g.out_f32 = true;
+    g.out = Z_part; g.out_ld = h; g.out_ss = 0;
+    return run_gemm(a, b, g, dt, dev, st);
+}
+
 // Row layer backward: dY_i = dZ B_i^T (times GeLU'(H_i) when act is GeLU), dB_i = Y_i^T dZ, db2.
 tpmlp_status do_row_bwd(const void* Y_sh, const void* B_sh, const void* dZ, const void* H_sh, void* dY_sh,
                         void* dB_sh, void* db2, int64_t M, int64_t h, int64_t ffn, int p, tpmlp_dtype dt,
@@ -215,12 +230,20 @@ tpmlp_status do_row_bwd(const void* Y_sh, const void* B_sh, const void* dZ, cons
     return TPMLP_OK;
 }
 
+// Column sums run beside the dX GEMM on the caller's side stream (tpmlp_set_side_stream).
+struct SideSums {
+    const void* dZ; void* db2; const void* dH; void* db1; int64_t M, h, fs, p; bool f32;
+    cudaStream_t side; cudaEvent_t fork, join;
+};
+tpmlp_status side_fork(const SideSums& w, cudaStream_t st);
+
 // Column layer backward: dA_i = X^T dY_i, db1_i = 1^T dY_i, dX = sum_i dY_i A_i^T.
-struct SideWork;  // column sums run beside the dX GEMM (see tpmlp_mlp_bwd)
-tpmlp_status side_fork(SideWork* w, cudaStream_t st);
+// dX_f32: dX is stored in fp32 (a rank's partial sum for an All-Reduce), else in dt.
+// side: the block's column sums to fork onto the side stream between the dA and dX launches.
 tpmlp_status do_column_bwd(const void* X, const void* A_sh, const void* dY_sh, void* dX, void* dA_sh, void* db1_sh,
                            int64_t M, int64_t h, int64_t ffn, int p, tpmlp_dtype dt, bool grad_f32,
-                           const DeviceInfo& dev, cudaStream_t st, SideWork* side = nullptr) {
+                           const DeviceInfo& dev, cudaStream_t st, bool dX_f32 = false,
+                           const SideSums* side = nullptr) {
     const int64_t fs = ffn / p;
     if (db1_sh) TP_TRY(launch_colsum(dY_sh, dt == TPMLP_F32, p, M, fs, db1_sh, grad_f32, st));
     {
@@ -233,58 +256,39 @@ tpmlp_status do_column_bwd(const void* X, const void* A_sh, const void* dY_sh, v
         g.out = dA_sh; g.out_ld = fs; g.out_ss = h * fs;
         TP_TRY(run_gemm(a, bb, g, dt, dev, st));
     }
-    if (side) TP_TRY(side_fork(side, st));
+    if (side) TP_TRY(side_fork(*side, st));
     {
         Operand a{dY_sh, fs, M * fs, p, false};      // dY_i [M][fs], K-major
         Operand bb{A_sh, fs, h * fs, p, false};      // A_i [h][fs]: [N][K], K-major
         GemmSpec g = spec_base();
         g.M = M; g.N = h; g.K = fs; g.n_shards = p;
         g.sum_shards = true;
-        g.epi = EPI_STORE; g.out_f32 = (dt == TPMLP_F32);
+        g.epi = EPI_STORE; g.out_f32 = dX_f32 || dt == TPMLP_F32;
         g.out = dX; g.out_ld = h; g.out_ss = 0;
         TP_TRY(run_gemm(a, bb, g, dt, dev, st));
     }
     return TPMLP_OK;
 }
 
-// The bias-gradient column sums of the fused backwards (tpmlp_mlp_bwd, tpmlp_swiglu_mlp_bwd) can
-// run on a second stream, forked after the dA GEMM is enqueued and joined after dX: they become
-// ready together with the dX GEMM, whose two-pair clusters leave SMs idle that the cluster-free
-// column sums can use.  One stream and two events per host thread and device, kept.
-struct SideWork {
-    const void* dZ; void* db2; const void* dH; void* db1; int64_t M, h, fs, p; bool f32;
-    cudaStream_t side; cudaEvent_t fork, join;
+// A side stream and two events of the caller's (tpmlp_set_side_stream), per host thread.  The
+// library never creates, destroys or synchronises them.
+struct SideHandles {
+    int device = -1;
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
 };
-struct SideHandles { cudaStream_t s = nullptr; cudaEvent_t fork = nullptr, join = nullptr; };
-thread_local SideHandles t_side[64];
-tpmlp_status side_handles(int device, SideHandles** out) {
-    if (device < 0 || device >= 64) {
-        set_error("device index %d out of range", device);
-        return TPMLP_ERR_CUDA;
-    }
-    SideHandles& h = t_side[device];
-    if (!h.s) {
-        cudaError_t e = cudaStreamCreateWithFlags(&h.s, cudaStreamNonBlocking);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.fork, cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.join, cudaEventDisableTiming);
-        if (e != cudaSuccess) {
-            set_error("side stream: %s", cudaGetErrorString(e));
-            return TPMLP_ERR_CUDA;
-        }
-    }
-    *out = &h;
-    return TPMLP_OK;
-}
-tpmlp_status side_fork(SideWork* w, cudaStream_t st) {
-    cudaError_t e = cudaEventRecord(w->fork, st);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(w->side, w->fork, 0);
+thread_local SideHandles t_side;
+
+tpmlp_status side_fork(const SideSums& w, cudaStream_t st) {
+    cudaError_t e = cudaEventRecord(w.fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(w.side, w.fork, 0);
     if (e != cudaSuccess) {
         set_error("side stream fork: %s", cudaGetErrorString(e));
         return TPMLP_ERR_CUDA;
     }
-    if (w->db2) TP_TRY(launch_colsum_any_sm(w->dZ, 1, w->M, w->h, w->db2, w->f32, w->side));
-    if (w->db1) TP_TRY(launch_colsum_any_sm(w->dH, w->p, w->M, w->fs, w->db1, w->f32, w->side));
-    e = cudaEventRecord(w->join, w->side);
+    if (w.db2) TP_TRY(launch_colsum_any_sm(w.dZ, 1, w.M, w.h, w.db2, w.f32, w.side));
+    if (w.db1) TP_TRY(launch_colsum_any_sm(w.dH, w.p, w.M, w.fs, w.db1, w.f32, w.side));
+    e = cudaEventRecord(w.join, w.side);
     if (e != cudaSuccess) {
         set_error("side stream join: %s", cudaGetErrorString(e));
         return TPMLP_ERR_CUDA;
@@ -292,28 +296,29 @@ tpmlp_status side_fork(SideWork* w, cudaStream_t st) {
     return TPMLP_OK;
 }
 
-// The column layer backward of a block (do_column_bwd) with the block's bias-gradient column
-// sums, db1 of dY_sh and db2 of dZ (either may be NULL), on the side stream for bf16 inputs.
-tpmlp_status column_bwd_side_sums(const void* X, const void* A_sh, const void* dY_sh, void* dX, void* dA_sh,
-                                  void* db1_sh, const void* dZ, void* db2, int64_t M, int64_t h, int64_t ffn, int p,
-                                  tpmlp_dtype dt, bool grad_f32, const DeviceInfo& dev, cudaStream_t st) {
-    // Beside dX only where that pays: dX must run on two-pair clusters (which leave SMs free),
-    // and long enough for the sums to finish on those SMs.  Measured: 419 MB of sums beside a
-    // 1.72 TFLOP dX (2.4e-4 byte/flop) finish inside it; 168 MB beside 0.55 TFLOP (3.1e-4) do
-    // not, and the join then delays the step.
+// The column layer backward of a block (do_column_bwd) with the block's bias-gradient column sums,
+// db1 of dY_sh and db2 of dZ (either may be NULL).  They run in line on `st`, or, when the caller
+// has registered a side stream and it pays, on that stream beside the dX GEMM: forked after the
+// dA launch (an event recorded on `st`) and joined before anything that follows dX on `st`.  The
+// dX GEMM's CTAs are resident by then (programmatic launch), so the sums take the SMs that dX's
+// last wave leaves idle.  Measured at the fwd+bwd bench workload, where dX's last wave keeps 32
+// of 76 CTA pairs busy and the sums read 2.4e-4 bytes per dX flop.  Both ways give the same bits.
+tpmlp_status column_bwd_with_db2(const void* X, const void* A_sh, const void* dY_sh, void* dX, void* dA_sh,
+                                 void* db1_sh, const void* dZ, void* db2, int64_t M, int64_t h, int64_t ffn, int p,
+                                 tpmlp_dtype dt, bool grad_f32, const DeviceInfo& dev, cudaStream_t st,
+                                 bool dX_f32 = false) {
     const int64_t fs = ffn / p;
     const double sum_bytes = 2.0 * ((db1_sh ? p * M * fs : 0) + (db2 ? M * h : 0));
-    const bool beside = dt == TPMLP_BF16 && (db1_sh || db2) && sum_bytes <= 2.6e-4 * (2.0 * M * h * ffn) &&
-                        shard_sum_gemm_uses_two_pairs(M, h, fs, p, dev);
+    const bool beside = t_side.s != nullptr && t_side.device == dev.device && dt == TPMLP_BF16 &&
+                        (db1_sh || db2) && sum_bytes <= 2.6e-4 * (2.0 * M * h * ffn) &&
+                        shard_sum_gemm_last_wave_fill(M, h, dev) <= 0.5;
     if (!beside) {
         if (db2) TP_TRY(launch_colsum(dZ, dt == TPMLP_F32, 1, M, h, db2, grad_f32, st));
-        return do_column_bwd(X, A_sh, dY_sh, dX, dA_sh, db1_sh, M, h, ffn, p, dt, grad_f32, dev, st);
+        return do_column_bwd(X, A_sh, dY_sh, dX, dA_sh, db1_sh, M, h, ffn, p, dt, grad_f32, dev, st, dX_f32);
     }
-    SideHandles* sh = nullptr;
-    TP_TRY(side_handles(dev.device, &sh));
-    SideWork w{dZ, db2, dY_sh, db1_sh, M, h, fs, p, grad_f32, sh->s, sh->fork, sh->join};
-    TP_TRY(do_column_bwd(X, A_sh, dY_sh, dX, dA_sh, nullptr, M, h, ffn, p, dt, grad_f32, dev, st, &w));
-    const cudaError_t e = cudaStreamWaitEvent(st, sh->join, 0);
+    const SideSums w{dZ, db2, dY_sh, db1_sh, M, h, fs, p, grad_f32, t_side.s, t_side.fork, t_side.join};
+    TP_TRY(do_column_bwd(X, A_sh, dY_sh, dX, dA_sh, nullptr, M, h, ffn, p, dt, grad_f32, dev, st, dX_f32, &w));
+    const cudaError_t e = cudaStreamWaitEvent(st, t_side.join, 0);
     if (e != cudaSuccess) {
         set_error("side stream join: %s", cudaGetErrorString(e));
         return TPMLP_ERR_CUDA;
@@ -482,8 +487,86 @@ tpmlp_status tpmlp_mlp_bwd(const void* X, const void* A_sh, const void* B_sh, co
     // row layer backward with GeLU' fused: dH_i = (dZ B_i^T) * GeLU'(H_i); dB_i; db2
     TP_TRY(do_row_bwd(Y_sh, B_sh, dZ, H_sh, dH_ws, dB_sh, nullptr, M, h, ffn, p, dt, gf32, TPMLP_ACT_GELU_ERF,
                       *dev, st));
-    // column layer backward from dH: dA_i, dX = sum_i dH_i A_i^T; db1_i and db2 beside dX
-    return column_bwd_side_sums(X, A_sh, dH_ws, dX, dA_sh, db1_sh, dZ, db2, M, h, ffn, p, dt, gf32, *dev, st);
+    // column layer backward from dH: db2, db1_i, dA_i, dX = sum_i dH_i A_i^T
+    return column_bwd_with_db2(X, A_sh, dH_ws, dX, dA_sh, db1_sh, dZ, db2, M, h, ffn, p, dt, gf32, *dev, st);
+}
+
+tpmlp_status tpmlp_mlp_fwd_partial(const void* X, const void* A_sh, const void* b1_sh, const void* B_sh, float* Z_part,
+                                   void* Y_ws, void* H_sh, int64_t s, int64_t b, int64_t h, int64_t ffn, int p,
+                                   tpmlp_dtype dt, void* stream) {
+    if (!X || !A_sh || !B_sh || !Z_part || !Y_ws) {
+        set_error("X, A_sh, B_sh, Z_part and Y_ws must not be NULL");
+        return TPMLP_ERR_NULL;
+    }
+    TP_TRY(check_mlp_shape(s, b, h, ffn, p, true));
+    TP_TRY(check_dtype(dt));
+    const int64_t M = s * b, fs = ffn / p, es = esize(dt);
+    TP_TRY(check_aligned({X, A_sh, b1_sh, B_sh, Z_part, Y_ws, H_sh}));
+    TP_TRY(check_pitch(h, dt, "h"));
+    TP_TRY(check_pitch(fs, dt, "ffn/p"));
+    TP_TRY(check_alias({{Z_part, M * h * 4}, {Y_ws, M * ffn * es}, {H_sh, M * ffn * es}},
+                       {{X, M * h * es}, {A_sh, h * ffn * es}, {b1_sh, ffn * es}, {B_sh, ffn * h * es}}));
+    const DeviceInfo* dev;
+    TP_TRY(get_device(&dev));
+    if (M == 0) return TPMLP_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    TP_TRY(do_column(X, A_sh, b1_sh, Y_ws, H_sh, M, h, ffn, p, dt, TPMLP_ACT_GELU_ERF, *dev, st));
+    return do_row_partial(Y_ws, B_sh, Z_part, M, h, ffn, p, dt, *dev, st);
+}
+
+tpmlp_status tpmlp_mlp_bwd_partial(const void* X, const void* A_sh, const void* B_sh, const void* H_sh,
+                                   const void* Y_sh, const void* dZ, float* dX_part, void* dA_sh, void* dB_sh,
+                                   void* db1_sh, void* db2, void* dH_ws, int64_t s, int64_t b, int64_t h,
+                                   int64_t ffn, int p, tpmlp_dtype dt, tpmlp_dtype grad_dt, void* stream) {
+    if (!X || !A_sh || !B_sh || !H_sh || !Y_sh || !dZ || !dX_part || !dA_sh || !dB_sh || !dH_ws) {
+        set_error("only db1_sh and db2 may be NULL");
+        return TPMLP_ERR_NULL;
+    }
+    TP_TRY(check_mlp_shape(s, b, h, ffn, p, true));
+    TP_TRY(check_dtype(dt));
+    TP_TRY(check_dtype(grad_dt));
+    if (dt == TPMLP_F32 && grad_dt != TPMLP_F32) {
+        set_error("grad_dt must be TPMLP_F32 when dt is TPMLP_F32");
+        return TPMLP_ERR_DTYPE;
+    }
+    const int64_t M = s * b, fs = ffn / p, es = esize(dt), gs = esize(grad_dt);
+    TP_TRY(check_aligned({X, A_sh, B_sh, H_sh, Y_sh, dZ, dX_part, dA_sh, dB_sh, db1_sh, db2, dH_ws}));
+    TP_TRY(check_pitch(h, dt, "h"));
+    TP_TRY(check_pitch(fs, dt, "ffn/p"));
+    TP_TRY(check_alias({{dX_part, M * h * 4}, {dA_sh, h * ffn * gs}, {dB_sh, ffn * h * gs}, {db1_sh, ffn * gs},
+                        {db2, h * gs}, {dH_ws, M * ffn * es}},
+                       {{X, M * h * es}, {A_sh, h * ffn * es}, {B_sh, ffn * h * es}, {H_sh, M * ffn * es},
+                        {Y_sh, M * ffn * es}, {dZ, M * h * es}}));
+    const DeviceInfo* dev;
+    TP_TRY(get_device(&dev));
+    if (M == 0) return TPMLP_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool gf32 = grad_dt == TPMLP_F32;
+    TP_TRY(do_row_bwd(Y_sh, B_sh, dZ, H_sh, dH_ws, dB_sh, nullptr, M, h, ffn, p, dt, gf32, TPMLP_ACT_GELU_ERF,
+                      *dev, st));
+    return column_bwd_with_db2(X, A_sh, dH_ws, dX_part, dA_sh, db1_sh, dZ, db2, M, h, ffn, p, dt, gf32, *dev, st,
+                               /*dX_f32=*/true);
+}
+
+tpmlp_status tpmlp_sum_finish(const float* S, const void* bias, void* out, int64_t rows, int64_t cols, tpmlp_dtype dt,
+                              void* stream) {
+    if (!S || !out) {
+        set_error("S and out must not be NULL");
+        return TPMLP_ERR_NULL;
+    }
+    if (rows < 0 || cols < 1 || rows > kMaxDim || cols > kMaxDim || (rows > 0 && cols > ((int64_t(1) << 40) / 4) / rows)) {
+        set_error("bad shape rows=%lld cols=%lld", (long long)rows, (long long)cols);
+        return TPMLP_ERR_SHAPE;
+    }
+    TP_TRY(check_dtype(dt));
+    TP_TRY(check_aligned({S, bias, out}));
+    TP_TRY(check_pitch(cols, dt, "cols"));
+    TP_TRY(check_alias({{out, rows * cols * esize(dt)}}, {{S, rows * cols * 4}, {bias, cols * esize(dt)}}));
+    const DeviceInfo* dev;
+    TP_TRY(get_device(&dev));
+    if (rows == 0) return TPMLP_OK;
+    return launch_sum_finish(S, bias, out, rows, cols, dt == TPMLP_F32, dev->sm_count,
+                             static_cast<cudaStream_t>(stream));
 }
 
 tpmlp_status tpmlp_row_bwd(const void* Y_sh, const void* B_sh, const void* dZ, const void* H_sh, void* dY_sh,
@@ -626,9 +709,8 @@ tpmlp_status tpmlp_swiglu_mlp_bwd(const void* X, const void* W_sh, const void* B
         g.out = dB_sh; g.out_ld = h; g.out_ss = fs * h;
         TP_TRY(run_gemm(a, bb, g, dt, *dev, st));
     }
-    // the packed gate/up layer is a column layer of width 2 ffn: dW = X^T dH, dX = sum_i dH_i W_i^T;
-    // dbw and db2 beside dX
-    return column_bwd_side_sums(X, W_sh, dH_ws, dX, dW_sh, dbw_sh, dZ, db2, M, h, 2 * ffn, p, dt, gf32, *dev, st);
+    // the packed gate/up layer is a column layer of width 2 ffn: dW = X^T dH, dX = sum_i dH_i W_i^T
+    return column_bwd_with_db2(X, W_sh, dH_ws, dX, dW_sh, dbw_sh, dZ, db2, M, h, 2 * ffn, p, dt, gf32, *dev, st);
 }
 
 tpmlp_status tpmlp_swiglu_pack(void* G, void* U, void* W_sh, int64_t rows, int64_t ffn, int p, tpmlp_dtype dt,
@@ -794,10 +876,32 @@ const char* tpmlp_last_error(void) { return t_err; }
 
 int tpmlp_version(void) { return 200; }
 
+tpmlp_status tpmlp_set_side_stream(void* side_stream, void* fork_event, void* join_event) {
+    if (!side_stream && !fork_event && !join_event) {
+        t_side = SideHandles{};
+        return TPMLP_OK;
+    }
+    if (!side_stream || !fork_event || !join_event) {
+        set_error("side_stream, fork_event and join_event must all be given, or all be NULL");
+        return TPMLP_ERR_NULL;
+    }
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        set_error("cudaGetDevice: %s", cudaGetErrorString(e));
+        return TPMLP_ERR_CUDA;
+    }
+    t_side.device = dev;
+    t_side.s = static_cast<cudaStream_t>(side_stream);
+    t_side.fork = static_cast<cudaEvent_t>(fork_event);
+    t_side.join = static_cast<cudaEvent_t>(join_event);
+    return TPMLP_OK;
+}
+
 tpmlp_status tpmlp_set_gemm_mode(int mode) {
-    if (mode < 0 || mode > 5) {
+    if (mode < 0 || mode > 4) {
         set_error("gemm mode must be 0 (automatic), 1 (single-CTA tiles), 2 (CTA-pair tiles), 3 (CTA-pair tiles, "
-                  "direct stores), 4 (CTA-pair tiles, TMA stores) or 5 (two CTA pairs per cluster sharing A)");
+                  "direct stores) or 4 (CTA-pair tiles, TMA stores)");
         return TPMLP_ERR_SHAPE;
     }
     set_gemm_mode(mode);

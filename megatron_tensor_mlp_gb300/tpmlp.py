@@ -37,6 +37,9 @@ _SIGS = {
     "tpmlp_mlp_fwd": [_vp] * 8 + [_i64] * 4 + [_i32, _i32, _vp],
     "tpmlp_mlp_bwd": [_vp] * 12 + [_i64] * 4 + [_i32, _i32, _i32, _vp],
     "tpmlp_mlp_fwd_noalloc": [_vp] * 6 + [_i64] * 4 + [_i32, _i32, _vp],
+    "tpmlp_mlp_fwd_partial": [_vp] * 7 + [_i64] * 4 + [_i32, _i32, _vp],
+    "tpmlp_mlp_bwd_partial": [_vp] * 12 + [_i64] * 4 + [_i32, _i32, _i32, _vp],
+    "tpmlp_sum_finish": [_vp, _vp, _vp, _i64, _i64, _i32, _vp],
     "tpmlp_swiglu_mlp_fwd": [_vp] * 8 + [_i64] * 4 + [_i32, _i32, _vp],
     "tpmlp_swiglu_mlp_bwd": [_vp] * 12 + [_i64] * 4 + [_i32, _i32, _i32, _vp],
     "tpmlp_swiglu_pack": [_vp] * 3 + [_i64, _i64, _i32, _i32, _i32, _vp],
@@ -48,6 +51,7 @@ _SIGS = {
     "tpmlp_device_status": [_vp],
     "tpmlp_debug_wait_timeout": [_u32, _vp],
     "tpmlp_set_gemm_mode": [_i32],
+    "tpmlp_set_side_stream": [_vp, _vp, _vp],
     "tpmlp_set_gemm_raster": [_i32],
     "tpmlp_set_k_chunk": [_i32],
 
@@ -137,6 +141,28 @@ def tpmlp_mlp_bwd(X, A_sh, B_sh, H_sh, Y_sh, dZ, dX, dA_sh, dB_sh, db1_sh, db2, 
     return _done(st, check)
 
 
+def tpmlp_mlp_fwd_partial(X, A_sh, b1_sh, B_sh, Z_part, Y_ws, H_sh, s, b, h, ffn, p, dt=BF16, stream=None,
+                          check=True):
+    """One rank's part of a block whose shards are spread over GPUs: fp32 Z_part, no b2."""
+    st = lib.tpmlp_mlp_fwd_partial(_ptr(X), _ptr(A_sh), _ptr(b1_sh), _ptr(B_sh), _ptr(Z_part), _ptr(Y_ws),
+                                   _ptr(H_sh), s, b, h, ffn, p, dt, _stream(stream))
+    return _done(st, check)
+
+
+def tpmlp_mlp_bwd_partial(X, A_sh, B_sh, H_sh, Y_sh, dZ, dX_part, dA_sh, dB_sh, db1_sh, db2, dH_ws, s, b, h, ffn, p,
+                          dt=BF16, grad_dt=F32, stream=None, check=True):
+    """One rank's backward: local weight and bias gradients, fp32 dX_part for the All-Reduce."""
+    st = lib.tpmlp_mlp_bwd_partial(_ptr(X), _ptr(A_sh), _ptr(B_sh), _ptr(H_sh), _ptr(Y_sh), _ptr(dZ),
+                                   _ptr(dX_part), _ptr(dA_sh), _ptr(dB_sh), _ptr(db1_sh), _ptr(db2), _ptr(dH_ws),
+                                   s, b, h, ffn, p, dt, grad_dt, _stream(stream))
+    return _done(st, check)
+
+
+def tpmlp_sum_finish(S, bias, out, rows, cols, dt=BF16, stream=None, check=True):
+    """out = round(S + bias) after the All-Reduce of fp32 partials."""
+    return _done(lib.tpmlp_sum_finish(_ptr(S), _ptr(bias), _ptr(out), rows, cols, dt, _stream(stream)), check)
+
+
 def tpmlp_swiglu_mlp_fwd(X, W_sh, bw_sh, B_sh, b2, Z, Y_ws, H_ws, s, b, h, ffn, p, dt=BF16, stream=None,
                          check=True):
     st = lib.tpmlp_swiglu_mlp_fwd(_ptr(X), _ptr(W_sh), _ptr(bw_sh), _ptr(B_sh), _ptr(b2), _ptr(Z), _ptr(Y_ws),
@@ -207,7 +233,21 @@ def tpmlp_debug_wait_timeout(timeout_us, stream=None, check=True):
 
 
 # tpmlp_set_gemm_mode values
-GEMM_AUTO, GEMM_SINGLE, GEMM_PAIR, GEMM_PAIR_DIRECT, GEMM_PAIR_STAGED, GEMM_TWO_PAIRS = 0, 1, 2, 3, 4, 5
+GEMM_AUTO, GEMM_SINGLE, GEMM_PAIR, GEMM_PAIR_DIRECT, GEMM_PAIR_STAGED = 0, 1, 2, 3, 4
+
+
+def tpmlp_set_side_stream(side_stream, fork_event, join_event, check=True):
+    """Register (or, with three Nones, clear) a side stream and two events of the caller's for the
+    fused backwards' column sums.  Torch objects or raw handles; the caller keeps them alive."""
+    def handle(x):
+        if x is None or isinstance(x, int):
+            return x
+        if hasattr(x, "cuda_stream"):
+            return x.cuda_stream
+        if not x.cuda_event:  # torch creates an event's CUDA object at its first record
+            x.record(side_stream if hasattr(side_stream, "cuda_stream") else None)
+        return x.cuda_event
+    return _done(lib.tpmlp_set_side_stream(handle(side_stream), handle(fork_event), handle(join_event)), check)
 
 
 def tpmlp_set_gemm_mode(mode, check=True):

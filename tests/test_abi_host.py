@@ -86,9 +86,9 @@ def test_bwd_and_layout_validation():
 
 
 def test_gemm_mode_control():
-    assert T.tpmlp_set_gemm_mode(6, check=False) == T.ERR_SHAPE
+    assert T.tpmlp_set_gemm_mode(5, check=False) == T.ERR_SHAPE
     assert T.tpmlp_set_gemm_mode(-1, check=False) == T.ERR_SHAPE
-    for m in (1, 2, 3, 4, 5, 0):
+    for m in (1, 2, 3, 4, 0):
         assert T.tpmlp_set_gemm_mode(m) == T.OK
         assert T.tpmlp_get_gemm_mode() == m
 
@@ -122,3 +122,11 @@ def test_binding_fails_loudly_without_library(tmp_path):
     (pkg / "tpmlp.py").write_text(src)
     r = subprocess.run([sys.executable, "-c", "import fakepkg.tpmlp"], cwd=tmp_path, capture_output=True, text=True)
     assert r.returncode != 0 and "is not built" in r.stderr
+
+
+def test_side_stream_registration_rules():
+    """All three handles or none: a partial registration is refused before any CUDA call, and
+    clearing needs no device."""
+    assert T.tpmlp_set_side_stream(None, None, None) == T.OK
+    assert T.tpmlp_set_side_stream(0x1000, None, None, check=False) == T.ERR_NULL
+    assert T.tpmlp_set_side_stream(None, 0x1000, 0x2000, check=False) == T.ERR_NULL

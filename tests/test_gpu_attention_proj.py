@@ -27,10 +27,10 @@ def _bf16(rng_seed, stream, shape, sigma, synth):
     return synth.normal(rng_seed, stream, shape, sigma, "bf16")
 
 
-@pytest.fixture(params=[0, 5], ids=["auto", "two-pairs"])
+@pytest.fixture(params=[0, 2], ids=["auto", "cta-pair"])
 def gemm_mode(request, env):
-    """Automatic tiling, or clusters of two CTA pairs wherever a GEMM has an even number of
-    256-wide N-blocks (the h = 384 case: QKV shards and the output projection both 384 wide)."""
+    """Automatic tiling, or CTA-pair 256x256 tiles forced even where there are fewer tiles than
+    co-resident pairs (every shape here)."""
     T = env[2]
     T.tpmlp_set_gemm_mode(request.param)
     yield request.param

@@ -17,10 +17,9 @@ def env():
     return harness, synth, tpmlp
 
 
-@pytest.fixture(params=[1, 3, 4, 5], ids=["single-cta", "pair-direct", "pair-staged", "two-pairs"])
+@pytest.fixture(params=[1, 3, 4], ids=["single-cta", "pair-direct", "pair-staged"])
 def gemm_mode(request, env):
-    """Force 128x256 single-CTA tiles, 256x256 CTA-pair tiles (either epilogue), or clusters of
-    two CTA pairs sharing A by multicast (GEMMs with an even number of 256-wide N-blocks)."""
+    """Force 128x256 single-CTA tiles or 256x256 CTA-pair tiles (either epilogue)."""
     T = env[2]
     T.tpmlp_set_gemm_mode(request.param)
     yield request.param
@@ -215,14 +214,14 @@ def test_single_and_pair_tiles_agree(env, orc):
     wl = synth.custom(150, 4, 384, 1536, 3, dtype="bf16", seed=9)
     buf = harness.MLPBuffers(wl, backward=True)
     out = {}
-    for mode in (1, 2, 3, 4, 5):
+    for mode in (1, 2, 3, 4):
         T.tpmlp_set_gemm_mode(mode)
         buf.fwd()
         buf.bwd()
         T.tpmlp_device_status()
         out[mode] = [t.clone() for t in (buf.Z, buf.Y, buf.H, buf.dX, buf.dA_sh, buf.dB_sh, buf.dH)]
     T.tpmlp_set_gemm_mode(0)
-    for mode in (2, 3, 4, 5):
+    for mode in (2, 3, 4):
         for a, b_ in zip(out[1], out[mode]):
             assert torch.equal(a, b_), mode
 
@@ -252,18 +251,17 @@ def test_many_shards(env, orc, shape, gemm_mode):
 
 @pytest.mark.parametrize("shape", [(1, 1, 8, 8, 1), (32, 1, 8, 64, 8), (1, 2, 16, 32, 2), (3, 1, 64, 8, 1),
                                    (1, 1, 64, 512, 1)],
-                         ids=["one-token-h8", "h8-p8", "two-tokens", "fs8", "one-token-two-pairs"])
+                         ids=["one-token-h8", "h8-p8", "two-tokens", "fs8", "one-token-two-nblocks"])
 def test_degenerate_shapes(env, orc, shape, gemm_mode):
     """The smallest legal problems: one token, h = 8 (one 16-byte row of X) with h / p = 1 and
     f / p = 8, every operand smaller than a single TMA box and a single tile in every GEMM (the
-    last shape a single token over two 256-wide N-blocks, so mode 5 runs it on a two-pair
-    cluster).  The h = 8, p = 8 case runs 32 tokens: with one token its Z has 8 elements, too few
+    last shape a single token over two 256-wide N-blocks).  The h = 8, p = 8 case runs 32 tokens: with one token its Z has 8 elements, too few
     for the relative Frobenius error to be more than a sample of the bf16 roundings (a CPU
     emulation of the kernels' rounding points, bf16 Y between the GEMMs and a bf16 Z store,
     gives 3.003e-3 there, exactly what the kernels produce).  One token also makes dA and dB
     outer products of bf16-rounded vectors, whose worst element carries one rounding unaveraged:
     at h = f = 512 the emulation exceeds the max-abs bound exactly as the kernels do, so the
-    two-pair case is 64 wide.  The emulation passes every shape here."""
+    two-N-block case is 64 wide.  The emulation passes every shape here."""
     _, synth, _ = env
     wl = synth.custom(*shape, dtype="bf16", sigma_w=0.1, sigma_bias=0.05, seed=sum(shape) + 11)
     _run_and_check(env, orc, wl)
@@ -278,7 +276,7 @@ def test_mixed_wave_shape(env, orc):
     _run_and_check(env, orc, wl)
 
 
-@pytest.mark.parametrize("mode", [3, 4, 5], ids=["pair-direct", "pair-staged", "two-pairs"])
+@pytest.mark.parametrize("mode", [3, 4], ids=["pair-direct", "pair-staged"])
 def test_every_gemm_two_waves(env, orc, mode):
     """All six GEMMs with more pair tiles than co-resident pairs (80 to 100 tiles), so
     every GEMM has second-wave tiles that walk K backwards: the batched column, dH,
@@ -293,22 +291,7 @@ def test_every_gemm_two_waves(env, orc, mode):
         T.tpmlp_set_gemm_mode(0)
 
 
-def test_two_pair_clusters_every_gemm(env, orc):
-    """Clusters of two CTA pairs in all six GEMMs: every GEMM has an even number of 256-wide
-    N-blocks with a ragged last one (h = 1800: 8 blocks, f/p = 1480: 6 blocks), ragged M and K
-    (M = 2400, K = 1800, 1480 per shard, 2400), and 40-60 256x512 cluster tiles, more than the
-    36 co-resident clusters, so second-wave tiles walk K (and the shard sums) backwards while
-    both pairs of a cluster share every A tile."""
-    _, synth, T = env
-    T.tpmlp_set_gemm_mode(5)
-    try:
-        wl = synth.custom(600, 4, 1800, 2960, 2, dtype="bf16", sigma_w=0.02, sigma_bias=0.05, seed=79)
-        _run_and_check(env, orc, wl)
-    finally:
-        T.tpmlp_set_gemm_mode(0)
-
-
-@pytest.mark.parametrize("mode", [1, 3, 5], ids=["single-cta", "pair-direct", "two-pairs"])
+@pytest.mark.parametrize("mode", [1, 3], ids=["single-cta", "pair-direct"])
 def test_split_contraction(env, orc, mode):
     """Weight gradients split into K chunks of 64 and 128 tokens (M = 200: four and two
     launches, the last one ragged), each later launch adding its partial product to the fp32

@@ -96,7 +96,7 @@ def _check_bf16(got, emu, name, floor_frac=2.0 ** -10):
     return _flip_fraction(got, emu, name)
 
 
-@pytest.mark.parametrize("mode", [1, 3, 5], ids=["single-cta", "pair-direct", "two-pairs"])
+@pytest.mark.parametrize("mode", [1, 3, 4], ids=["single-cta", "pair-direct", "pair-staged"])
 def test_rounding_points_match_emulation(env, mode):
     harness, synth, T = env
     T.tpmlp_set_gemm_mode(mode)
@@ -156,7 +156,7 @@ def _emulate_swiglu(X, G, Uw, bg, bu, B, b2, dZ, bf16_saves=False):
             "db2": dZ.sum(0)}
 
 
-@pytest.mark.parametrize("mode", [1, 2, 5], ids=["single-cta", "cta-pair", "two-pairs"])
+@pytest.mark.parametrize("mode", [1, 2], ids=["single-cta", "cta-pair"])
 def test_swiglu_rounding_points_match_emulation(env, orc, mode):
     import torch
     harness, synth, T = env
@@ -212,8 +212,7 @@ def test_swiglu_rounding_points_match_emulation(env, orc, mode):
 def test_full_workload_rounding_points_sampled(env, wi):
     """The bench's fwd+bwd workload (s=2048 b=4 h=5120 f=20480 p=4), and the forward at the
     pages' sizing (s=4096 b=1 h=8192 f=32768 p=8, K = 8192 and 32768), in their own launch
-    configuration (multi-wave pair tiles walking K backwards, the row and dX GEMMs on two-pair
-    clusters), on 16 sampled token rows: H, Y, Z, dH and dX are row-local, so the emulation of
+    configuration (multi-wave pair tiles walking K backwards), on 16 sampled token rows: H, Y, Z, dH and dX are row-local, so the emulation of
     reading r7 needs only those rows and the full weights.  With K = 5120 and 20480 the fp32
     accumulation error (measured ~1.9e-8 per 16-deep MMA step, growing linearly) reaches ~1e-5
     of the partial sums, so units are measured at max(|value|, RMS / 16), where it stays below
@@ -260,7 +259,7 @@ def test_full_workload_rounding_points_sampled(env, wi):
 
 
 # ---------------------------------------------------------------------- attention projections
-@pytest.mark.parametrize("mode", [1, 3, 5], ids=["single-cta", "pair-direct", "two-pairs"])
+@pytest.mark.parametrize("mode", [1, 3, 4], ids=["single-cta", "pair-direct", "pair-staged"])
 def test_attention_projection_rounding_points(env, orc, mode):
     """QKV = bf16(X W + b) over the per-head interleave, Z = bf16(ctx W_o + b_o) summed over the
     ranks' head blocks, dctx = bf16(dZ W_oᵀ), dX = bf16(dQKV Wᵀ) summed over ranks: each a single
