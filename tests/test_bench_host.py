@@ -44,3 +44,38 @@ def test_default_and_profiling_flags(monkeypatch):
     monkeypatch.setattr(sys, "argv", ["bench.py", "--next-rows-only", "--steps", "8", "--warmup", "2"])
     a = bench.parse()
     assert a.next_rows_only and a.steps == 8 and a.warmup == 2
+
+
+PEAKS = {"bf16_tflops": 1895.4, "bf16_tflops_sustained": 1707.2}
+
+
+def test_peak_regime_short_region_is_burst():
+    """A tenth of a second of load runs at the burst clock: the burst peak applies, whatever
+    the sampled clock."""
+    regime, peak, _ = bench.peak_regime({"sm_mhz": 1500.0, "sm_max_mhz": 2070.0}, 0.12, PEAKS)
+    assert regime == "burst" and peak == 1895.4
+
+
+def test_peak_regime_near_max_clock_is_burst():
+    regime, peak, _ = bench.peak_regime({"sm_mhz": 2055.0, "sm_max_mhz": 2070.0}, 3.0, PEAKS)
+    assert regime == "burst" and peak == 1895.4
+
+
+def test_peak_regime_settled_long_region_is_sustained():
+    regime, peak, why = bench.peak_regime({"sm_mhz": 1470.0, "sm_max_mhz": 2070.0}, 1.3, PEAKS)
+    assert regime == "sustained" and peak == 1707.2
+    assert "1470" in why and "2070" in why
+
+
+def test_clock_summary_uses_samples_inside_the_window():
+    """Samples stamped inside a marked window are summarised; a window with fewer than three
+    samples falls back to every sample and says so."""
+    s = bench.ClockSampler.__new__(bench.ClockSampler)
+    s.source, s.windows = "test", {"timed": [10.0, 10.1], "tiny": [20.0, 20.001]}
+    s.rows = [(9.9, 1400.0, 2070.0, 1300.0, 0x4)] + \
+        [(10.0 + 0.01 * i, 2000.0 + i, 2070.0, 900.0, 0x0) for i in range(1, 10)]
+    c = s.summary("timed")
+    assert c["window"] == "timed region" and c["samples"] == 9
+    assert c["sm_mhz"] == 2005.0 and c["reasons"] == []
+    t = s.summary("tiny")
+    assert t["window"] == "whole run" and t["samples"] == 10 and t["reasons"] == ["sw_power_cap"]
