@@ -226,9 +226,11 @@ tpmlp_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
 // Picks the tiling and launches.  CTA-pair 256x256 tiles when there are at least as many
 // of them as co-resident pairs (or when forced); otherwise single-CTA 128x256 tiles, or
 // 128x128 tiles when the 128x256 ones would leave more than half of the SMs idle.
+// sms_out != nullptr: only report how many SMs the launch would occupy (its persistent grid), and
+// launch nothing.
 template <bool A_MN, bool B_MN, int EPI>
 tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& g, tc::KArgs k, const DeviceInfo& dev,
-                            cudaStream_t st) {
+                            cudaStream_t st, int* sms_out = nullptr) {
     const int mode = g_gemm_mode.load(std::memory_order_relaxed);
     const int m_pairs = static_cast<int>((g.M + 2 * tc::BM - 1) / (2 * tc::BM));
     const int pair_tiles = m_pairs * k.n_blocks * k.batch;
@@ -236,6 +238,15 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
     const bool use_pair = cap > 0 && (mode >= 2 || pair_tiles >= cap);
     constexpr bool kNarrowOk = EPI != EPI_SWIGLU && EPI != EPI_DSWIGLU;  // packed layouts span 256 columns
     const bool narrow = kNarrowOk && !use_pair && 2 * k.num_tiles <= dev.sm_count && g.N > 128;
+    if (sms_out) {
+        if (use_pair) {
+            *sms_out = 2 * (pair_tiles < cap ? pair_tiles : cap);
+        } else {
+            const int tiles = narrow ? k.m_blocks * static_cast<int>((g.N + 127) / 128) * k.batch : k.num_tiles;
+            *sms_out = tiles < dev.sm_count ? tiles : dev.sm_count;
+        }
+        return TPMLP_OK;
+    }
     CUtensorMap ma, mb;
     const uint32_t b_rows = (use_pair || narrow) ? tc::BN / 2 : tc::BN;
     // MN-major operands: one 4-D box per stage when the MN extent is a multiple of 64
@@ -279,7 +290,7 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
 }
 
 tpmlp_status launch_one(const Operand& a, const Operand& b, const GemmSpec& g, const DeviceInfo& dev,
-                        cudaStream_t st, bool accumulate) {
+                        cudaStream_t st, bool accumulate, int* sms_out = nullptr) {
     tc::KArgs k{};
     k.accumulate = accumulate ? 1 : 0;
     k.M = static_cast<int>(g.M);
@@ -329,16 +340,22 @@ tpmlp_status launch_one(const Operand& a, const Operand& b, const GemmSpec& g, c
                      ? 1
                      : 0;
     }
-    if (k.num_tiles == 0) return TPMLP_OK;
+    if (k.num_tiles == 0) {
+        if (sms_out) *sms_out = 0;
+        return TPMLP_OK;
+    }
 
     const bool amn = a.mn_major, bmn = b.mn_major;
-    if (g.epi == EPI_BIAS_ACT && !amn && bmn) return launch_variant<false, true, EPI_BIAS_ACT>(a, b, g, k, dev, st);
-    if (g.epi == EPI_DGELU && !amn && !bmn) return launch_variant<false, false, EPI_DGELU>(a, b, g, k, dev, st);
-    if (g.epi == EPI_SWIGLU && !amn && bmn) return launch_variant<false, true, EPI_SWIGLU>(a, b, g, k, dev, st);
-    if (g.epi == EPI_DSWIGLU && !amn && !bmn) return launch_variant<false, false, EPI_DSWIGLU>(a, b, g, k, dev, st);
-    if (g.epi == EPI_STORE && amn && bmn) return launch_variant<true, true, EPI_STORE>(a, b, g, k, dev, st);
-    if (g.epi == EPI_STORE && !amn && bmn) return launch_variant<false, true, EPI_STORE>(a, b, g, k, dev, st);
-    if (g.epi == EPI_STORE && !amn && !bmn) return launch_variant<false, false, EPI_STORE>(a, b, g, k, dev, st);
+    if (g.epi == EPI_BIAS_ACT && !amn && bmn)
+        return launch_variant<false, true, EPI_BIAS_ACT>(a, b, g, k, dev, st, sms_out);
+    if (g.epi == EPI_DGELU && !amn && !bmn) return launch_variant<false, false, EPI_DGELU>(a, b, g, k, dev, st, sms_out);
+    if (g.epi == EPI_SWIGLU && !amn && bmn) return launch_variant<false, true, EPI_SWIGLU>(a, b, g, k, dev, st, sms_out);
+    if (g.epi == EPI_DSWIGLU && !amn && !bmn)
+        return launch_variant<false, false, EPI_DSWIGLU>(a, b, g, k, dev, st, sms_out);
+    if (g.epi == EPI_STORE && amn && bmn) return launch_variant<true, true, EPI_STORE>(a, b, g, k, dev, st, sms_out);
+    if (g.epi == EPI_STORE && !amn && bmn) return launch_variant<false, true, EPI_STORE>(a, b, g, k, dev, st, sms_out);
+    if (g.epi == EPI_STORE && !amn && !bmn)
+        return launch_variant<false, false, EPI_STORE>(a, b, g, k, dev, st, sms_out);
     set_error("internal: no tcgen05 GEMM variant for epi=%d a_mn=%d b_mn=%d", g.epi, (int)amn, (int)bmn);
     return TPMLP_ERR_CUDA;
 }
@@ -373,16 +390,11 @@ tpmlp_status launch_tc_gemm(const Operand& a, const Operand& b, const GemmSpec& 
     return TPMLP_OK;
 }
 
-double shard_sum_gemm_last_wave_fill(int64_t M, int64_t N, const DeviceInfo& dev) {
-    const int mode = g_gemm_mode.load(std::memory_order_relaxed);
-    if (mode == 1 || M <= 0) return 0.0;
-    const int cap = pair_capacity<false, false, EPI_STORE, false>(dev);
-    const int m_pairs = static_cast<int>((M + 2 * tc::BM - 1) / (2 * tc::BM));
-    const int n_blocks = static_cast<int>((N + tc::BN - 1) / tc::BN);
-    const int pair_tiles = m_pairs * n_blocks;
-    if (cap <= 0 || !(mode >= 2 || pair_tiles >= cap)) return 0.0;
-    const int last = pair_tiles % cap;
-    return last == 0 ? 1.0 : static_cast<double>(last) / cap;
+int tc_gemm_sms(const Operand& a, const Operand& b, const GemmSpec& g, const DeviceInfo& dev) {
+    // the first launch of a split contraction is the widest (each later one covers the same tiles)
+    int sms = 0;
+    if (launch_one(a, b, g, dev, nullptr, false, &sms) != TPMLP_OK) return dev.sm_count;
+    return sms;
 }
 
 void set_k_chunk_blocks(int blocks) {

@@ -81,10 +81,9 @@ tpmlp_status launch_swiglu_pack(void* G, void* U, void* W_sh, int64_t rows, int6
                                 bool inverse, cudaStream_t st);
 
 // Process-wide GEMM tiling mode (see tpmlp_set_gemm_mode).
-// Fraction of the CTA pairs that the last wave of a shard-summing GEMM with K-major operands and
-// a store epilogue (dX = sum_s A_s B_s of the backwards: per-shard K, `shards` shards) keeps busy:
-// 1 for whole waves, 0 when it does not run on CTA pairs (the same tiling decision as launch_tc_gemm).
-double shard_sum_gemm_last_wave_fill(int64_t M, int64_t N, const DeviceInfo& dev);
+// SMs a bf16 GEMM launch of launch_tc_gemm occupies for its whole run (its persistent grid: CTA
+// pairs or single CTAs, one per SM), by the same tiling decision; nothing is launched.
+int tc_gemm_sms(const Operand& a, const Operand& b, const GemmSpec& g, const DeviceInfo& dev);
 void set_gemm_mode(int mode);
 int get_gemm_mode();
 void set_group_m(int g);

@@ -230,44 +230,61 @@ tpmlp_status do_row_bwd(const void* Y_sh, const void* B_sh, const void* dZ, cons
     return TPMLP_OK;
 }
 
-// Column sums run beside the dX GEMM on the caller's side stream (tpmlp_set_side_stream).
+// Column sums run beside a GEMM on the caller's side stream (tpmlp_set_side_stream).
 struct SideSums {
     const void* dZ; void* db2; const void* dH; void* db1; int64_t M, h, fs, p; bool f32;
     cudaStream_t side; cudaEvent_t fork, join;
 };
 tpmlp_status side_fork(const SideSums& w, cudaStream_t st);
 
+// The two GEMMs of the column layer backward.
+struct GemmCall {
+    Operand a, b;
+    GemmSpec g;
+};
+// dA_i = X^T dY_i (K = tokens)
+GemmCall dA_call(const void* X, const void* dY_sh, void* dA_sh, int64_t M, int64_t h, int64_t ffn, int p,
+                 bool grad_f32) {
+    const int64_t fs = ffn / p;
+    GemmCall c{{X, h, 0, 1, true},              // X [M][h]: [K][M_gemm], MN-major
+               {dY_sh, fs, M * fs, p, true},    // dY_i [M][fs]: [K][N], MN-major
+               spec_base()};
+    c.g.M = h; c.g.N = fs; c.g.K = M; c.g.n_shards = p;
+    c.g.a_batched = false; c.g.b_batched = true;
+    c.g.epi = EPI_STORE; c.g.out_f32 = grad_f32;
+    c.g.out = dA_sh; c.g.out_ld = fs; c.g.out_ss = h * fs;
+    return c;
+}
+// dX = sum_i dY_i A_i^T (the shard sum in the K loop); dX_f32: fp32 output
+GemmCall dX_call(const void* dY_sh, const void* A_sh, void* dX, int64_t M, int64_t h, int64_t ffn, int p, bool dX_f32) {
+    const int64_t fs = ffn / p;
+    GemmCall c{{dY_sh, fs, M * fs, p, false},   // dY_i [M][fs], K-major
+               {A_sh, fs, h * fs, p, false},    // A_i [h][fs]: [N][K], K-major
+               spec_base()};
+    c.g.M = M; c.g.N = h; c.g.K = fs; c.g.n_shards = p;
+    c.g.sum_shards = true;
+    c.g.epi = EPI_STORE; c.g.out_f32 = dX_f32;
+    c.g.out = dX; c.g.out_ld = h; c.g.out_ss = 0;
+    return c;
+}
+
+enum ForkAt { kForkNone = 0, kForkBeforeDA = 1, kForkBeforeDX = 2 };
+
 // Column layer backward: dA_i = X^T dY_i, db1_i = 1^T dY_i, dX = sum_i dY_i A_i^T.
 // dX_f32: dX is stored in fp32 (a rank's partial sum for an All-Reduce), else in dt.
-// side: the block's column sums to fork onto the side stream between the dA and dX launches.
+// side / fork_at: the block's column sums to fork onto the side stream before the dA or dX launch.
 tpmlp_status do_column_bwd(const void* X, const void* A_sh, const void* dY_sh, void* dX, void* dA_sh, void* db1_sh,
                            int64_t M, int64_t h, int64_t ffn, int p, tpmlp_dtype dt, bool grad_f32,
                            const DeviceInfo& dev, cudaStream_t st, bool dX_f32 = false,
-                           const SideSums* side = nullptr) {
+                           const SideSums* side = nullptr, ForkAt fork_at = kForkNone) {
     const int64_t fs = ffn / p;
     if (db1_sh) TP_TRY(launch_colsum(dY_sh, dt == TPMLP_F32, p, M, fs, db1_sh, grad_f32, st));
-    {
-        Operand a{X, h, 0, 1, true};                 // X [M][h]: [K][M_gemm], MN-major
-        Operand bb{dY_sh, fs, M * fs, p, true};      // dY_i [M][fs]: [K][N], MN-major
-        GemmSpec g = spec_base();
-        g.M = h; g.N = fs; g.K = M; g.n_shards = p;
-        g.a_batched = false; g.b_batched = true;
-        g.epi = EPI_STORE; g.out_f32 = grad_f32;
-        g.out = dA_sh; g.out_ld = fs; g.out_ss = h * fs;
-        TP_TRY(run_gemm(a, bb, g, dt, dev, st));
-    }
-    if (side) TP_TRY(side_fork(*side, st));
-    {
-        Operand a{dY_sh, fs, M * fs, p, false};      // dY_i [M][fs], K-major
-        Operand bb{A_sh, fs, h * fs, p, false};      // A_i [h][fs]: [N][K], K-major
-        GemmSpec g = spec_base();
-        g.M = M; g.N = h; g.K = fs; g.n_shards = p;
-        g.sum_shards = true;
-        g.epi = EPI_STORE; g.out_f32 = dX_f32 || dt == TPMLP_F32;
-        g.out = dX; g.out_ld = h; g.out_ss = 0;
-        TP_TRY(run_gemm(a, bb, g, dt, dev, st));
-    }
-    return TPMLP_OK;
+    if (side && fork_at == kForkBeforeDA) TP_TRY(side_fork(*side, st));
+    const GemmCall ca = dA_call(X, dY_sh, dA_sh, M, h, ffn, p, grad_f32);
+    TP_TRY(run_gemm(ca.a, ca.b, ca.g, dt, dev, st));
+    if (side && fork_at == kForkBeforeDX) TP_TRY(side_fork(*side, st));
+    const GemmCall cx = dX_call(dY_sh, A_sh, dX, M, h, ffn, p, dX_f32 || dt == TPMLP_F32);
+    return run_gemm(cx.a, cx.b, cx.g, dt, dev, st);
 }
 
 // A side stream and two events of the caller's (tpmlp_set_side_stream), per host thread.  The
@@ -298,26 +315,33 @@ tpmlp_status side_fork(const SideSums& w, cudaStream_t st) {
 
 // The column layer backward of a block (do_column_bwd) with the block's bias-gradient column sums,
 // db1 of dY_sh and db2 of dZ (either may be NULL).  They run in line on `st`, or, when the caller
-// has registered a side stream and it pays, on that stream beside the dX GEMM: forked after the
-// dA launch (an event recorded on `st`) and joined before anything that follows dX on `st`.  The
-// dX GEMM's CTAs are resident by then (programmatic launch), so the sums take the SMs that dX's
-// last wave leaves idle.  Measured at the fwd+bwd bench workload, where dX's last wave keeps 32
-// of 76 CTA pairs busy and the sums read 2.4e-4 bytes per dX flop.  Both ways give the same bits.
+// has registered a side stream, on that stream beside the first of the dA and dX GEMMs whose
+// persistent grid leaves enough SMs idle for all the sums' CTAs at once (one CTA per 256-column
+// strip and shard): forked just before that GEMM's launch (an event recorded on `st`) and joined
+// before anything that follows dX on `st`.  The GEMM's CTAs are resident by the time the fork
+// event completes (programmatic launch), so the sums run only on the SMs it leaves idle.  A GEMM
+// that fills every SM gets no sums beside it: they would take SMs its CTAs wait for (measured at
+// the fwd+bwd bench workload, whose dX fills all 76 CTA pairs: backward 3-5 % slower).  Both
+// ways give the same bits.
 tpmlp_status column_bwd_with_db2(const void* X, const void* A_sh, const void* dY_sh, void* dX, void* dA_sh,
                                  void* db1_sh, const void* dZ, void* db2, int64_t M, int64_t h, int64_t ffn, int p,
                                  tpmlp_dtype dt, bool grad_f32, const DeviceInfo& dev, cudaStream_t st,
                                  bool dX_f32 = false) {
     const int64_t fs = ffn / p;
-    const double sum_bytes = 2.0 * ((db1_sh ? p * M * fs : 0) + (db2 ? M * h : 0));
-    const bool beside = t_side.s != nullptr && t_side.device == dev.device && dt == TPMLP_BF16 &&
-                        (db1_sh || db2) && sum_bytes <= 2.6e-4 * (2.0 * M * h * ffn) &&
-                        shard_sum_gemm_last_wave_fill(M, h, dev) <= 0.5;
-    if (!beside) {
+    ForkAt at = kForkNone;
+    if (t_side.s != nullptr && t_side.device == dev.device && dt == TPMLP_BF16 && (db1_sh || db2)) {
+        const int64_t strips = (db1_sh ? p * ((fs + 255) / 256) : 0) + (db2 ? (h + 255) / 256 : 0);
+        const GemmCall ca = dA_call(X, dY_sh, dA_sh, M, h, ffn, p, grad_f32);
+        const GemmCall cx = dX_call(dY_sh, A_sh, dX, M, h, ffn, p, dX_f32);
+        if (dev.sm_count - tc_gemm_sms(ca.a, ca.b, ca.g, dev) >= strips) at = kForkBeforeDA;
+        else if (dev.sm_count - tc_gemm_sms(cx.a, cx.b, cx.g, dev) >= strips) at = kForkBeforeDX;
+    }
+    if (at == kForkNone) {
         if (db2) TP_TRY(launch_colsum(dZ, dt == TPMLP_F32, 1, M, h, db2, grad_f32, st));
         return do_column_bwd(X, A_sh, dY_sh, dX, dA_sh, db1_sh, M, h, ffn, p, dt, grad_f32, dev, st, dX_f32);
     }
     const SideSums w{dZ, db2, dY_sh, db1_sh, M, h, fs, p, grad_f32, t_side.s, t_side.fork, t_side.join};
-    TP_TRY(do_column_bwd(X, A_sh, dY_sh, dX, dA_sh, nullptr, M, h, ffn, p, dt, grad_f32, dev, st, dX_f32, &w));
+    TP_TRY(do_column_bwd(X, A_sh, dY_sh, dX, dA_sh, nullptr, M, h, ffn, p, dt, grad_f32, dev, st, dX_f32, &w, at));
     const cudaError_t e = cudaStreamWaitEvent(st, t_side.join, 0);
     if (e != cudaSuccess) {
         set_error("side stream join: %s", cudaGetErrorString(e));

@@ -1,10 +1,11 @@
 """Column sums of the fused backward on a side stream of the caller's (GPU).
 
 With a stream and two events registered (tpmlp_set_side_stream), tpmlp_mlp_bwd runs db1 and db2
-beside the dX GEMM where its last wave leaves CTA pairs idle; with nothing registered they run in
-line.  Both give the same bits, and every other output is unchanged.  The shape (2048 tokens,
-h = 5120, ffn = 20480, p = 4) gives dX 160 CTA-pair tiles, a last wave of 8 of 76 pairs, and
-2.4e-4 bytes of sums per dX flop, so the side stream is taken.
+on that stream beside the first of the dA and dX GEMMs whose grid leaves enough SMs idle for all
+the sums' CTAs; with nothing registered they run in line.  Both give the same bits, and every
+other output is unchanged.  The shape is the s=512 b=4 h=1024 ffn=4096 p=4 workload: its dA GEMM
+runs 128 single-CTA tiles on the 152 SMs, and the sums need 20 CTAs (16 strips of db1, 4 of db2),
+so they go beside dA.
 """
 import numpy as np
 import pytest
@@ -19,7 +20,7 @@ def test_side_stream_sums_are_bit_identical():
     from megatron_tensor_mlp_gb300 import harness, synth
     from megatron_tensor_mlp_gb300 import tpmlp as T
 
-    wl = synth.custom(512, 4, 5120, 20480, 4, dtype="bf16", sigma_w=0.02, sigma_bias=0.0, seed=66)
+    wl = synth.custom(512, 4, 1024, 4096, 4, dtype="bf16", sigma_w=0.02, sigma_bias=0.01, seed=66)
     buf = harness.MLPBuffers(wl, backward=True)
     buf.fwd()
     buf.bwd()
