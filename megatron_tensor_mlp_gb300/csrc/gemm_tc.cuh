@@ -326,6 +326,53 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* f,
         if (g * 8 < nvalid) unpack_bf16x8(*reinterpret_cast<const uint4*>(src + g * 8), f + g * 8);
 }
 
+// GeLU' epilogue: 32 bf16 values of H (this thread's row, columns gn0..gn0+31) as 16 packed
+// pairs, loaded ahead of the chunk that uses them (the loads of a warp touch 32 rows, so each
+// costs a full memory latency; issued one chunk early they overlap the previous chunk's work,
+// and the first chunk's overlap the wait for the accumulator).  Words past the row's end are
+// not loaded (their values are never stored).
+__device__ __forceinline__ void load_h_raw(const KArgs& p, int gm, int gn0, int shard, uint32_t (&w)[16]) {
+    if (gm >= p.M) return;
+    const int nvalid = p.N - gn0;
+    if (nvalid <= 0) return;
+    const __nv_bfloat16* hp = static_cast<const __nv_bfloat16*>(p.aux) + shard * p.aux_ss + (long long)gm * p.aux_ld + gn0;
+    if (p.st32) {
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            if ((g + 1) * 16 <= nvalid) {
+                uint32_t t[8];
+                ld_v8(hp + g * 16, t);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w[g * 8 + i] = t[i];
+            } else if (g * 16 < nvalid) {
+                const uint4 u = *reinterpret_cast<const uint4*>(hp + g * 16);
+                w[g * 8 + 0] = u.x; w[g * 8 + 1] = u.y; w[g * 8 + 2] = u.z; w[g * 8 + 3] = u.w;
+            }
+        }
+        return;
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        if (g * 8 < nvalid) {
+            const uint4 u = *reinterpret_cast<const uint4*>(hp + g * 8);
+            w[g * 4 + 0] = u.x; w[g * 4 + 1] = u.y; w[g * 4 + 2] = u.z; w[g * 4 + 3] = u.w;
+        }
+    }
+}
+
+// v[j] <- v[j] * GeLU'(H[j]) for the first nvalid (a multiple of 8) of 32 values, H as loaded
+// by load_h_raw.
+__device__ __forceinline__ void dgelu_apply32(float* v, const uint32_t (&w)[16], int nvalid) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        if (g * 8 < nvalid) {
+            float hv[8];
+            unpack_bf16x8(make_uint4(w[g * 4 + 0], w[g * 4 + 1], w[g * 4 + 2], w[g * 4 + 3]), hv);
+            dgelu_mul8(v + g * 8, hv);
+        }
+    }
+}
+
 template <int EPI>
 __device__ __forceinline__ void epilogue_chunk(const KArgs& p, const uint32_t (&r)[32], int gm, int gn0, int shard) {
     if (gm >= p.M) return;
@@ -479,6 +526,39 @@ __device__ __forceinline__ void epilogue_tile(const KArgs& p, uint32_t t_row, in
             static_assert(EPI != EPI_DSWIGLU || NCH == 4, "the packed SwiGLU layout needs 256-wide tiles");
             if constexpr (EPI == EPI_DSWIGLU) dswiglu_chunk(p, r, gm, nb * BN + col, shard);
             else epilogue_chunk<EPI>(p, r, gm, nb * (NCH * 64) + col, shard);
+        }
+    }
+}
+
+// GeLU' epilogue of L consecutive 32-column chunks of a tile TW columns wide, starting at chunk
+// jbase, for this thread's row gm; h0 holds the first chunk's H on entry.  Two chunks per loop
+// trip so that the H buffers are named at compile time.
+template <int L, int TW>
+__device__ __forceinline__ void dgelu_chunks(const KArgs& p, uint32_t t_row, int gm, int nb, int jbase, int shard,
+                                             uint32_t (&h0)[16], uint32_t (&h1)[16]) {
+    static_assert(L % 2 == 0, "chunks come in pairs");
+#pragma unroll 1
+    for (int i = 0; i < L; i += 2) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            uint32_t(&cur)[16] = k == 0 ? h0 : h1;
+            uint32_t(&nxt)[16] = k == 0 ? h1 : h0;
+            const int col = (jbase + i + k) * 32;
+            const int gn0 = nb * TW + col;
+            if (i + k + 1 < L) load_h_raw(p, gm, gn0 + 32, shard, nxt);
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(t_row + col, r);
+            tmem_ld_wait();
+            const int nvalid = p.N - gn0;
+            if (gm < p.M && nvalid > 0) {
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                dgelu_apply32(v, cur, nvalid);
+                __nv_bfloat16* d =
+                    static_cast<__nv_bfloat16*>(p.out) + shard * p.out_ss + (long long)gm * p.out_ld + gn0;
+                store_bf16x32(d, v, nvalid, p.st32);
+            }
         }
     }
 }
@@ -666,6 +746,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++lt) {
             const int acc = lt & 1;
             const uint32_t acc_phase = (lt >> 1) & 1;
+            if constexpr (EPI == EPI_DGELU) {
+                // the tile's first H chunk loads while the accumulator is being computed
+                int mb, nb, shard;
+                decode_tile(p, t, mb, nb, shard);
+                const int gm = mb * BM + q * 32 + lane;
+                uint32_t h0[16], h1[16];
+                load_h_raw(p, gm, nb * SBN + half * (SBN / 2), shard, h0);
+                int okw = 0;
+                if (lane == 0) okw = mbar_wait_bounded(tfull + acc, acc_phase, p.status, p.timeout_ns, kWhereEpilogue);
+                okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+                if (!okw) break;
+                tc_fence_after();
+                const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * SBN;
+                dgelu_chunks<SBN / 64, SBN>(p, t_row, gm, nb, half * (SBN / 64), shard, h0, h1);
+            } else {
             int okw = 0;
             if (lane == 0) okw = mbar_wait_bounded(tfull + acc, acc_phase, p.status, p.timeout_ns, kWhereEpilogue);
             okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
@@ -676,6 +771,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int gm = mb * BM + q * 32 + lane;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * SBN;
             epilogue_tile<EPI, SBN / 64>(p, t_row, gm, nb, half, shard);
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty + acc);
@@ -805,6 +901,48 @@ __device__ __forceinline__ void epilogue_tile_staged(const KArgs& p, const CUten
             tma_store_3d(tm_out, box, gn0, row0, shard);
             if (two) tma_store_3d(tm_out2, ebuf + 2048, gn0, row0, shard);
             bulk_commit_group();
+        }
+    }
+}
+
+// Staged GeLU' epilogue of one warp's 32 rows x 128 columns (column half `half`), with each
+// chunk's H loaded one chunk ahead (h0 holds the first chunk's on entry): the same values and
+// boxes as epilogue_tile_staged<EPI_DGELU>.
+__device__ __forceinline__ void epilogue_tile_staged_dgelu(const KArgs& p, const CUtensorMap* tm_out, uint32_t t_row,
+                                                           int row0, int lane, int nb, int half, int shard,
+                                                           uint8_t* ebuf, uint32_t& seq, uint32_t (&h0)[16],
+                                                           uint32_t (&h1)[16]) {
+    if (row0 >= p.M) return;
+    const int gm = row0 + lane;
+#pragma unroll 1
+    for (int c = 0; c < 4; c += 2) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            uint32_t(&cur)[16] = k == 0 ? h0 : h1;
+            uint32_t(&nxt)[16] = k == 0 ? h1 : h0;
+            const int col = half * 128 + (c + k) * 32;
+            const int gn0 = nb * BN + col;
+            if (gn0 >= p.N) return;
+            if (c + k + 1 < 4) load_h_raw(p, gm, gn0 + 32, shard, nxt);
+            const int nvalid = p.N - gn0;
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(t_row + col, r);
+            tmem_ld_wait();
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+            uint8_t* box = ebuf + (seq & 1u) * 2048;  // two 2 KiB boxes alternate (single bf16 output)
+            ++seq;
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+            if (gm < p.M) dgelu_apply32(v, cur, nvalid);
+            stage_bf16x32(box, lane, v);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_3d(tm_out, box, gn0, row0, shard);
+                bulk_commit_group();
+            }
         }
     }
 }
@@ -1086,6 +1224,28 @@ __global__ void __launch_bounds__(PairGeom<STAGED>::threads, 1)
         for (int t = cluster_id; t < p.num_tiles; t += n_clusters, ++lt) {
             const int acc = lt & 1;
             const uint32_t acc_phase = (lt >> 1) & 1;
+            if constexpr (EPI == EPI_DGELU) {
+                // the tile's first H chunk loads while the accumulator is being computed
+                int mb, nb, shard;
+                decode_tile(p, t, mb, nb, shard);
+                const int row0 = mb * (2 * BM) + static_cast<int>(prank) * BM + q * 32;
+                uint32_t h0[16], h1[16];
+                load_h_raw(p, row0 + lane, nb * BN + (STAGED ? half * 128 : 0), shard, h0);
+                int okw = 0;
+                if (lane == 0) okw = mbar_wait_bounded(tfull + acc, acc_phase, p.status, p.timeout_ns, kWhereEpilogue);
+                okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+                if (!okw) break;
+                tc_fence_after();
+                const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+                if constexpr (STAGED)
+                    epilogue_tile_staged_dgelu(p, &tmO, t_row, row0, lane, nb, half, shard, ebuf, seq, h0, h1);
+                else
+                    dgelu_chunks<8, BN>(p, t_row, row0 + lane, nb, 0, shard, h0, h1);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(tempty_leader0 + acc * 8);
+                continue;
+            }
             int okw = 0;
             if (lane == 0) okw = mbar_wait_bounded(tfull + acc, acc_phase, p.status, p.timeout_ns, kWhereEpilogue);
             okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
