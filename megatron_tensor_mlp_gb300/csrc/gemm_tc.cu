@@ -92,7 +92,7 @@ bool make_out_map(CUtensorMap* map, void* ptr, int64_t ld, int64_t ss, uint64_t 
 // main loop takes ~512 cycles per 64-wide K block, a direct-store epilogue ~10-20 k cycles.
 constexpr int kStagedMaxKBlocks = 40;
 
-// 0 auto, 1 single-CTA, 2 pair, 3 pair + direct stores, 4 pair + TMA stores
+// 0 auto, 1 single-CTA, 2 pair, 3 pair + direct stores, 4 pair + TMA stores, 5 auto with split-K forced
 std::atomic<int> g_gemm_mode{0};
 std::atomic<int> g_group_m{16};  // M-blocks per raster group
 // K blocks per launch of a split fp32 contraction (see launch_tc_gemm)
@@ -223,6 +223,62 @@ tpmlp_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
     return TPMLP_OK;
 }
 
+// Co-resident clusters of the split-K kernel (two CTA pairs each) on this device.
+template <bool A_MN, bool B_MN, int EPI>
+int splitk_capacity(const DeviceInfo& dev) {
+    static int cap[64];
+    static bool done[64];
+    static bool attr_done[64] = {};
+    if (dev.device >= 64) return 0;
+    if (done[dev.device]) return cap[dev.device];
+    auto kern = tc::gemm_splitk_kernel<A_MN, B_MN, EPI>;
+    int n = 0;
+    if (set_smem_attr(kern, dev.device, tc::SK_SMEM, attr_done)) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(4 * (dev.sm_count / 4));
+        cfg.blockDim = dim3(tc::SK_THREADS);
+        cfg.dynamicSmemBytes = tc::SK_SMEM;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 4;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+        cudaGetLastError();
+    }
+    cap[dev.device] = n;
+    done[dev.device] = true;
+    return n;
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+tpmlp_status launch_splitk(const CUtensorMap& ma, const CUtensorMap& mb, const tc::KArgs& k, cudaStream_t st) {
+    auto kern = tc::gemm_splitk_kernel<A_MN, B_MN, EPI>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(4 * k.num_tiles);  // one tile per cluster of four
+    cfg.blockDim = dim3(tc::SK_THREADS);
+    cfg.dynamicSmemBytes = tc::SK_SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 4;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see griddep_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, k);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("tcgen05 split-K GEMM launch: %s", cudaGetErrorString(e));
+        return TPMLP_ERR_CUDA;
+    }
+    return TPMLP_OK;
+}
+
 // Picks the tiling and launches.  CTA-pair 256x256 tiles when there are at least as many
 // of them as co-resident pairs (or when forced); otherwise single-CTA 128x256 tiles, or
 // 128x128 tiles when the 128x256 ones would leave more than half of the SMs idle.
@@ -235,11 +291,28 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
     const int m_pairs = static_cast<int>((g.M + 2 * tc::BM - 1) / (2 * tc::BM));
     const int pair_tiles = m_pairs * k.n_blocks * k.batch;
     int cap = (mode == 1) ? 0 : pair_capacity<A_MN, B_MN, EPI, false>(dev);
-    const bool use_pair = cap > 0 && (mode >= 2 || pair_tiles >= cap);
+    bool use_pair = cap > 0 && ((mode >= 2 && mode <= 4) || pair_tiles >= cap);
+    // Split-K CTA pairs for a shard-summing GEMM whose 256x256 tiles are fewer than the pairs the
+    // GPU holds (it would otherwise run on single-CTA tiles), with a K loop long enough to split.
+    constexpr bool kSplitOk = (EPI == EPI_BIAS_ACT && !A_MN && B_MN) || (EPI == EPI_STORE && !A_MN);
+    bool split = false;
+    if constexpr (kSplitOk) {
+        if (g.sum_shards && !k.accumulate && k.k_iters >= 2 && cap > 0 &&
+            (mode == 5 || (mode == 0 && pair_tiles < cap && k.k_iters >= 16)))
+            split = splitk_capacity<A_MN, B_MN, EPI>(dev) >= pair_tiles;
+    }
+    if (split) use_pair = true;  // pair-shaped operand boxes
     constexpr bool kNarrowOk = EPI != EPI_SWIGLU && EPI != EPI_DSWIGLU;  // packed layouts span 256 columns
+    // Fewer pair tiles than pairs: single-CTA 128x256 tiles would occupy no more SMs (a pair tile is
+    // two of them stacked) but move twice the B bytes per SM and store from registers, so the pairs
+    // stay, unless 128x128 single-CTA tiles would occupy up to twice as many SMs.
+    if (!use_pair && cap > 0 && (mode == 0 || mode == 5) && !(kNarrowOk && 2 * k.num_tiles <= dev.sm_count && g.N > 128))
+        use_pair = true;
     const bool narrow = kNarrowOk && !use_pair && 2 * k.num_tiles <= dev.sm_count && g.N > 128;
     if (sms_out) {
-        if (use_pair) {
+        if (split) {
+            *sms_out = 4 * pair_tiles;
+        } else if (use_pair) {
             *sms_out = 2 * (pair_tiles < cap ? pair_tiles : cap);
         } else {
             const int tiles = narrow ? k.m_blocks * static_cast<int>((g.N + 127) / 128) * k.batch : k.num_tiles;
@@ -272,6 +345,9 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
     }
     k.m_blocks = m_pairs;
     k.num_tiles = pair_tiles;
+    if constexpr (kSplitOk) {
+        if (split) return launch_splitk<A_MN, B_MN, EPI>(ma, mb, k, st);
+    }
     const int clusters = pair_tiles < cap ? pair_tiles : cap;
     // Short K loops (a tile's main loop shorter than a direct-store epilogue): staged epilogue.
     if constexpr (kNarrowOk) {

@@ -1282,5 +1282,284 @@ __global__ void __launch_bounds__(PairGeom<STAGED>::threads, 1)
     }
 }
 
+
+// ============================================================================
+// Split-K CTA pairs, for shard-summing GEMMs (the row layer's Z = sum_i Y_i B_i and the
+// backward's dX = sum_i dH_i A_i^T) whose 256x256 tiles are fewer than the CTA pairs the
+// GPU holds.  Such GEMMs otherwise run on 128x128 single-CTA tiles, whose main loop is
+// bound by each SM's operand bandwidth (32 KiB per 256 tensor cycles).
+//
+// A cluster of four CTAs -- two CTA pairs -- computes one 256x256 output tile; pair
+// q = rank / 2 accumulates K blocks [q kh, ...) of the tile's K loop (kh = k_iters / 2)
+// into its own tensor memory with the same producer / UMMA structure as gemm_pair_kernel
+// (32 KiB per 512 tensor cycles per SM).  The two fp32 partial sums meet in distributed
+// shared memory: CTA (q, r) finishes column half q of its 128 rows, so once the partner
+// CTA (1 - q, r) -- same rows, other K half -- reports that its own products are complete
+// (its operand ring is then free), it writes the other column half of its partial
+// (128 x 128 fp32) into the partner's ring, and receives the matching half in its own.
+// The thread that holds a row in one CTA reads it back in the other (same lane quarter and
+// lane), so the buffer is laid out by thread: 16-byte piece j of thread x's row at slot
+// j * 128 + x, and each warp store or load covers 512 contiguous bytes.
+// Each CTA adds the two partials and runs the usual epilogue on its half.  Every TMA load
+// lands in the CTA that issues it (no multicast); every wait is bounded.
+//
+// One tile per cluster: the host launches 4 * num_tiles CTAs.
+// ============================================================================
+constexpr int SK_THREADS = 256;     // warp 0 producer, warp 1 TMEM + UMMA issuer, warps 4-7 epilogue
+constexpr int SK_STAGES = 7;
+constexpr int SK_SMEM = 1024 + SK_STAGES * P_STAGE_BYTES + BAR_BYTES;
+static_assert(BM * 128 * 4 <= SK_STAGES * P_A_BYTES, "the received half fits in the A ring");
+static_assert(SK_SMEM <= 227 * 1024, "split-K kernel shared memory");
+
+template <bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(SK_THREADS, 1)
+    gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const KArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + SK_STAGES * P_A_BYTES;
+    uint4* recv = reinterpret_cast<uint4*>(smem);  // 32 x 128 16-byte slots, over the A ring once it is free
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + SK_STAGES * P_STAGE_BYTES);
+    uint64_t* empty = full + SK_STAGES;
+    uint64_t* tfull = empty + SK_STAGES;
+    uint64_t* drain = tfull + 1;
+    uint64_t* peer_free = drain + 1;   // the partner's products are complete (one arrival per epilogue warp)
+    uint64_t* data_ready = peer_free + 1;  // the partner's half has landed in recv (one per epilogue thread)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(data_ready + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t prank = rank & 1u;     // position in the CTA pair
+    const uint32_t pleader = rank & ~1u;  // the pair's leader (UMMA issuer)
+    const int q = static_cast<int>(rank >> 1);  // the K half this pair accumulates, and the column half it finishes
+    const bool leader = prank == 0;
+    const uint16_t pair_mask = static_cast<uint16_t>(0x3u << pleader);
+    const uint32_t partner = rank ^ 2u;   // same rows, other K half
+    const int t = static_cast<int>(blockIdx.x) / 4;
+    const int kh = p.k_iters / 2;
+    const int it0 = q ? kh : 0, it1 = q ? p.k_iters : kh;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SK_STAGES; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        mbar_init(tfull, 1);
+        mbar_init(drain, 1);
+        mbar_init(peer_free, 4);
+        mbar_init(data_ready, 128);
+        fence_mbarrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, BN);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // every barrier of the cluster is initialised from here on
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    griddep_wait();
+    if (threadIdx.x == 0) griddep_launch_dependents();
+
+    int mb, nb, shard;
+    decode_tile(p, t, mb, nb, shard);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------------ producer (all four CTAs)
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0, last_parity = 0;
+            bool ok = true;
+            const int k_end = p.kb_per_shard * BK;
+            const uint32_t full_leader0 = mapa_shared(smem_u32(full), pleader);
+            const int row0 = mb * (2 * BM) + static_cast<int>(prank) * BM;
+            const int col0 = nb * BN + static_cast<int>(prank) * (BN / 2);
+            int sa, sb, k0;
+            if (p.sum_shards) {
+                sa = sb = it0 / p.kb_per_shard;
+                k0 = (it0 - sa * p.kb_per_shard) * BK;
+            } else {
+                sa = p.a_batched ? shard : 0;
+                sb = p.b_batched ? shard : 0;
+                k0 = it0 * BK;
+            }
+            for (int it = it0; it < it1; ++it) {
+                if (!mbar_wait_bounded(empty + stage, phase ^ 1u, p.status, p.timeout_ns, kWhereProducer)) {
+                    ok = false;
+                    break;
+                }
+                if (leader) {
+                    mbar_arrive_expect_tx(full + stage, 2 * P_STAGE_BYTES);
+                    armed |= 1u << stage;
+                    last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                }
+                const uint32_t bar = full_leader0 + stage * 8;
+                uint8_t* a_dst = sA + stage * P_A_BYTES;
+                uint8_t* b_dst = sB + stage * P_B_BYTES;
+                if constexpr (!A_MN) {
+                    tma_load_3d_pair(a_dst, &tmA, bar, k0, row0, sa);
+                } else if (p.a_chunked) {
+                    tma_load_4d_pair(a_dst, &tmA, bar, 0, k0, row0 / 64, sa);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < BM / 64; ++c)
+                        tma_load_3d_pair(a_dst + c * MN_CHUNK_BYTES, &tmA, bar, row0 + c * 64, k0, sa);
+                }
+                if constexpr (!B_MN) {
+                    tma_load_3d_pair(b_dst, &tmB, bar, k0, col0, sb);
+                } else if (p.b_chunked) {
+                    tma_load_4d_pair(b_dst, &tmB, bar, 0, k0, col0 / 64, sb);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < (BN / 2) / 64; ++c)
+                        tma_load_3d_pair(b_dst + c * MN_CHUNK_BYTES, &tmB, bar, col0 + c * 64, k0, sb);
+                }
+                if (++stage == SK_STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                k0 += BK;
+                if (k0 == k_end) {  // next shard of the sum
+                    k0 = 0;
+                    ++sa;
+                    ++sb;
+                }
+            }
+            if (ok) {
+                // the leader's commits that release stages arrive on this CTA's empty barriers,
+                // possibly from the other SM of the pair: observe each stage's last release
+                for (int i = 0; i < SK_STAGES; ++i) {
+                    if (!mbar_wait_bounded(empty + stage, phase ^ 1u, p.status, p.timeout_ns, kWhereDrain)) break;
+                    if (++stage == SK_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            } else {
+                if (leader) {
+                    for (int s = 0; s < SK_STAGES; ++s)
+                        if (armed & (1u << s))
+                            mbar_wait_bounded(full + s, (last_parity >> s) & 1u, p.status, p.timeout_ns, kWhereDrain,
+                                              /*watch_status=*/false);
+                } else {
+                    spin_ns(200000);  // let this CTA's last copies (counted on the leader's barriers) land
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            if (leader) {
+                // -------------------------------------------------------- UMMA issuer (pair leaders)
+                constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN, A_MN, B_MN);
+                const uint64_t a_desc0 = A_MN ? sdesc_sw128(smem_u32(sA), TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES)
+                                              : sdesc_sw128(smem_u32(sA), 16, 1024);
+                const uint64_t b_desc0 = B_MN ? sdesc_sw128(smem_u32(sB), TPMLP_MN_LBO_BYTES, TPMLP_MN_SBO_BYTES)
+                                              : sdesc_sw128(smem_u32(sB), 16, 1024);
+                constexpr uint64_t a_kstep = A_MN ? (2048 >> 4) : (32 >> 4);
+                constexpr uint64_t b_kstep = B_MN ? (2048 >> 4) : (32 >> 4);
+                int stage = 0;
+                uint32_t phase = 0;
+                bool ok = true;
+                for (int i = 0; i < it1 - it0; ++i) {
+                    if (!mbar_wait_bounded(full + stage, phase, p.status, p.timeout_ns, kWhereMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t adesc = a_desc0 + static_cast<uint64_t>(stage * (P_A_BYTES >> 4));
+                    const uint64_t bdesc = b_desc0 + static_cast<uint64_t>(stage * (P_B_BYTES >> 4));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma_f16_pair(tmem_base, adesc + kk * a_kstep, bdesc + kk * b_kstep, idesc,
+                                      (i | kk) != 0 ? 1u : 0u);
+                    umma_commit_pair_mc(empty + stage, pair_mask);
+                    if (++stage == SK_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) umma_commit_pair_mc(tfull, pair_mask);
+                umma_commit_pair_mc(drain, pair_mask);
+            }
+            mbar_wait_bounded(drain, 0, p.status, p.timeout_ns, kWhereDrain, /*watch_status=*/false);
+        }
+    } else if (warp >= FIRST_EPI_WARP) {
+        // ---------------------------------------------------------------- exchange + epilogue
+        const int ql = warp & 3;             // TMEM lane quarter
+        const int row_l = ql * 32 + lane;    // this thread's row among the CTA's 128
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(ql * 32) << 16);
+        int okw = 0;
+        if (lane == 0) okw = mbar_wait_bounded(tfull, 0, p.status, p.timeout_ns, kWhereEpilogue);
+        okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+        if (okw) {
+            tc_fence_after();
+            // this CTA's products are complete: its A ring may take the partner's half
+            fence_proxy_async_all();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(peer_free), partner));
+            // every lane acquires the partner's release itself: its own writes follow
+            const bool okp = __all_sync(0xFFFFFFFFu,
+                                        mbar_wait_bounded_cluster(peer_free, 0, p.status, p.timeout_ns, kWhereExchange));
+            if (okp) {
+                // the other column half of this CTA's partial, into the partner's ring
+                const uint32_t dst = mapa_shared(smem_u32(recv + row_l), partner);
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_row + (1 - q) * 128 + c * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_cluster_v4(dst + ((c * 8 + j) * 128) * 16, r[4 * j], r[4 * j + 1], r[4 * j + 2],
+                                      r[4 * j + 3]);
+                }
+                mbar_arrive_cluster(mapa_shared(smem_u32(data_ready), partner));
+                // every lane acquires: each reads rows the partner's threads wrote
+                const bool okd = __all_sync(
+                    0xFFFFFFFFu, mbar_wait_bounded_cluster(data_ready, 0, p.status, p.timeout_ns, kWhereExchange));
+                if (okd) {
+                    // own half: this CTA's partial plus the partner's, then the usual epilogue
+                    const int gm = mb * (2 * BM) + static_cast<int>(prank) * BM + row_l;
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        const int col = q * 128 + c * 32;
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(t_row + col, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const uint4 u = recv[(c * 8 + j) * 128 + row_l];
+                            r[4 * j + 0] = __float_as_uint(__uint_as_float(r[4 * j + 0]) + __uint_as_float(u.x));
+                            r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + __uint_as_float(u.y));
+                            r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + __uint_as_float(u.z));
+                            r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + __uint_as_float(u.w));
+                        }
+                        epilogue_chunk<EPI>(p, r, gm, nb * BN + col, shard);
+                    }
+                }
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // no CTA leaves while another may still write its shared memory or barriers
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc_pair(tmem_base, BN);
+    }
+}
+
 }  // namespace tc
 }  // namespace tpmlp

@@ -13,7 +13,7 @@ enum : uint32_t {
     kStatusDevice = 0x20000u,
 };
 enum : uint32_t {
-    kWhereProducer = 1, kWhereMma = 2, kWhereEpilogue = 3, kWhereDrain = 4, kWhereDebug = 5,
+    kWhereProducer = 1, kWhereMma = 2, kWhereEpilogue = 3, kWhereDrain = 4, kWhereDebug = 5, kWhereExchange = 6,
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -212,6 +212,44 @@ __device__ __forceinline__ void tma_load_4d_pair(void* smem_dst, const CUtensorM
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar_cluster_addr)
         : "memory");
 }
+// 16-byte store into the shared memory of a CTA of the cluster (address from mapa_shared).
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+// try_wait with cluster-scope acquire: after it succeeds, writes that other CTAs of the cluster
+// made before their release-arrive on this barrier are visible to this thread.
+__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+// mbar_wait_bounded with cluster-scope acquire (for barriers that other CTAs arrive on).
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                                          uint64_t timeout_ns, uint32_t where) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t spin = 0;; ++spin) {
+        if (mbar_try_wait_acq_cluster(bar, parity, 1000000u)) return true;
+        if ((spin & 7u) == 7u) {
+            if (ld_volatile_u32(status) != 0u) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) {
+                atomicCAS(status, 0u, kStatusTimeout | where);
+                return false;
+            }
+        }
+    }
+}
+// Order this thread's generic-proxy accesses to shared memory after the async proxy's (TMA
+// writes, tensor-core reads) that it has observed complete, and vice versa.
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
 // TMEM allocation shared by the CTA pair (one warp of each CTA executes these).
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* smem_slot, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_slot)),

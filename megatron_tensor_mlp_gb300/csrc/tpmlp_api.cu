@@ -923,9 +923,9 @@ tpmlp_status tpmlp_set_side_stream(void* side_stream, void* fork_event, void* jo
 }
 
 tpmlp_status tpmlp_set_gemm_mode(int mode) {
-    if (mode < 0 || mode > 4) {
+    if (mode < 0 || mode > 5) {
         set_error("gemm mode must be 0 (automatic), 1 (single-CTA tiles), 2 (CTA-pair tiles), 3 (CTA-pair tiles, "
-                  "direct stores) or 4 (CTA-pair tiles, TMA stores)");
+                  "direct stores), 4 (CTA-pair tiles, TMA stores) or 5 (automatic, split-K forced)");
         return TPMLP_ERR_SHAPE;
     }
     set_gemm_mode(mode);

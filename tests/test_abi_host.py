@@ -86,9 +86,9 @@ def test_bwd_and_layout_validation():
 
 
 def test_gemm_mode_control():
-    assert T.tpmlp_set_gemm_mode(5, check=False) == T.ERR_SHAPE
+    assert T.tpmlp_set_gemm_mode(6, check=False) == T.ERR_SHAPE
     assert T.tpmlp_set_gemm_mode(-1, check=False) == T.ERR_SHAPE
-    for m in (1, 2, 3, 4, 0):
+    for m in (1, 2, 3, 4, 5, 0):
         assert T.tpmlp_set_gemm_mode(m) == T.OK
         assert T.tpmlp_get_gemm_mode() == m
 

@@ -27,10 +27,10 @@ def _bf16(rng_seed, stream, shape, sigma, synth):
     return synth.normal(rng_seed, stream, shape, sigma, "bf16")
 
 
-@pytest.fixture(params=[0, 2], ids=["auto", "cta-pair"])
+@pytest.fixture(params=[0, 2, 5], ids=["auto", "cta-pair", "split-k"])
 def gemm_mode(request, env):
-    """Automatic tiling, or CTA-pair 256x256 tiles forced even where there are fewer tiles than
-    co-resident pairs (every shape here)."""
+    """Automatic tiling, CTA-pair 256x256 tiles forced even where there are fewer tiles than
+    co-resident pairs (every shape here), or split-K CTA pairs on the shard-summing GEMMs."""
     T = env[2]
     T.tpmlp_set_gemm_mode(request.param)
     yield request.param

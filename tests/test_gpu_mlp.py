@@ -17,9 +17,10 @@ def env():
     return harness, synth, tpmlp
 
 
-@pytest.fixture(params=[1, 3, 4], ids=["single-cta", "pair-direct", "pair-staged"])
+@pytest.fixture(params=[1, 3, 4, 5], ids=["single-cta", "pair-direct", "pair-staged", "split-k"])
 def gemm_mode(request, env):
-    """Force 128x256 single-CTA tiles or 256x256 CTA-pair tiles (either epilogue)."""
+    """Force 128x256 single-CTA tiles, 256x256 CTA-pair tiles (either epilogue), or split-K CTA
+    pairs for every shard-summing GEMM (row, dX) that fits one wave of them."""
     T = env[2]
     T.tpmlp_set_gemm_mode(request.param)
     yield request.param
@@ -314,6 +315,30 @@ def test_split_contraction(env, orc, mode):
     finally:
         T.tpmlp_set_k_chunk(0)
         T.tpmlp_set_gemm_mode(0)
+
+
+@pytest.mark.parametrize("shape", [(60, 5, 264, 576, 3), (256, 4, 1024, 4096, 4), (130, 3, 520, 2080, 2)],
+                         ids=["odd-k-blocks", "s256-h1024", "ragged"])
+def test_split_k_tiles(env, orc, shape):
+    """Split-K CTA pairs (mode 5) on the row and dX GEMMs: two pairs of a cluster each sum half
+    of the K blocks and add their partials through distributed shared memory.  Shard counts and
+    widths make the split fall inside a shard (3 shards x 3 K blocks: the halves are 4 and 5
+    blocks), on a workload-sized K loop (64 blocks), and on ragged M, N and K.  Full parity with
+    the oracle, and within fp32 reassociation of the CTA-pair result."""
+    import torch
+    harness, synth, T = env
+    wl = synth.custom(*shape, dtype="bf16", sigma_w=0.03, sigma_bias=0.05, seed=sum(shape) + 5)
+    T.tpmlp_set_gemm_mode(3)
+    try:
+        ref = _run_and_check(env, orc, wl)
+        want = [t.clone() for t in (ref.Z, ref.dX)]
+        T.tpmlp_set_gemm_mode(5)
+        buf = _run_and_check(env, orc, wl)
+    finally:
+        T.tpmlp_set_gemm_mode(0)
+    for got, w in zip((buf.Z, buf.dX), want):
+        err = (got.double() - w.double()).norm() / w.double().norm()
+        assert float(err) < 2e-3, float(err)
 
 
 def _random_shapes(n, seed):

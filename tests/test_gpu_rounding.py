@@ -96,7 +96,7 @@ def _check_bf16(got, emu, name, floor_frac=2.0 ** -10):
     return _flip_fraction(got, emu, name)
 
 
-@pytest.mark.parametrize("mode", [1, 3, 4], ids=["single-cta", "pair-direct", "pair-staged"])
+@pytest.mark.parametrize("mode", [1, 3, 4, 5], ids=["single-cta", "pair-direct", "pair-staged", "split-k"])
 def test_rounding_points_match_emulation(env, mode):
     harness, synth, T = env
     T.tpmlp_set_gemm_mode(mode)

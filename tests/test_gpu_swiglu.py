@@ -23,7 +23,7 @@ def env():
     return harness, synth, tpmlp
 
 
-@pytest.fixture(params=[1, 2], ids=["single-cta", "cta-pair"])
+@pytest.fixture(params=[1, 2, 5], ids=["single-cta", "cta-pair", "split-k"])
 def gemm_mode(request, env):
     T = env[2]
     T.tpmlp_set_gemm_mode(request.param)
