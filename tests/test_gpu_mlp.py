@@ -268,6 +268,58 @@ def test_degenerate_shapes(env, orc, shape, gemm_mode):
     _run_and_check(env, orc, wl)
 
 
+@pytest.mark.parametrize("shape", [(1, 1, 512, 512, 1), (1, 1, 8, 8, 1), (1, 2, 64, 512, 2), (1, 1, 1024, 4096, 4)],
+                         ids=["one-token-h512", "one-token-h8", "two-tokens", "one-token-h1024"])
+def test_tiny_outputs_elementwise_bound(env, orc, shape, gemm_mode):
+    """The bound for outputs too small for the statistical ones (reading r8a): every element within
+    the a-priori error of the rounding protocol (reading r7) of the exact values.  A bf16 rounding
+    adds at most 2^-9 relative error; an fp32 sum of K terms at most K 2^-23 of the sum of
+    magnitudes (2^-22 is used for margin); GeLU and GeLU' are 1.2-Lipschitz.  With u = half the
+    bf16 spacing at the exact value, S = |dZ| |B|^T and s_X = |X| |A| (sums of magnitudes):
+        eY  = 2^-8 |Y*| + 1.2 h 2^-22 s_X                        (Y from the fp32 H)
+        eH  = 2^-9 |H*| + h 2^-22 s_X                            (the saved bf16 H)
+        e   = (2^-8 |GeLU'(H*)| + 1.2 eH + |GeLU'(H*)| h 2^-22) S  (dH)
+        |Z - Z*|   <= u(Z*) + eY |B| + f 2^-22 |Y*| |B|
+        |dX - dX*| <= u(dX*) + e |A|^T + f 2^-22 |dH*| |A|^T
+        |dA - dA*| <= |X|^T e + M 2^-22 |X|^T |dH*|,   |db1 - db1*| <= sum_m e + M 2^-22 sum_m |dH*|
+        |dB - dB*| <= eY^T |dZ| + M 2^-22 |Y*|^T |dZ|
+    The first shape is the one-token call whose weight gradients exceed the RMS-scaled max-abs
+    bound by their own roundings."""
+    from scipy.special import ndtr
+    harness, synth, T = env
+    wl = synth.custom(*shape, dtype="bf16", sigma_w=0.1, sigma_bias=0.05, seed=sum(shape) + 13)
+    buf = harness.MLPBuffers(wl, backward=True)
+    buf.fwd()
+    buf.bwd()
+    T.tpmlp_device_status()
+    x = U.host_inputs_f64(buf)
+    X, A, B, dZ = x["X"], x["A"], x["B"], x["dZ"]
+    M, h = X.shape
+    f = A.shape[1]
+    H, Y, Z = orc.mlp_fwd(X, A, x["b1"], B, x["b2"])
+    g = orc.mlp_bwd(X, A, B, H, Y, dZ)
+    gp = ndtr(H) + H * np.exp(-0.5 * H * H) / np.sqrt(2.0 * np.pi)
+    acc = 2.0 ** -22
+    sX = np.abs(X) @ np.abs(A) + (0.0 if x["b1"] is None else np.abs(x["b1"]))
+    S = np.abs(dZ) @ np.abs(B).T
+    eY = 2.0 ** -8 * np.abs(Y) + 1.2 * h * acc * sX
+    eH = 2.0 ** -9 * np.abs(H) + h * acc * sX
+    e = (2.0 ** -8 * np.abs(gp) + 1.2 * eH + np.abs(gp) * h * acc) * S
+    dHa = np.abs(gp) * S
+    bounds = {
+        "Z": (harness.to_host(buf.Z), Z,
+              U.bf16_half_spacing(Z) + eY @ np.abs(B) + f * acc * (np.abs(Y) @ np.abs(B))),
+        "dX": (harness.to_host(buf.dX), g["dX"],
+               U.bf16_half_spacing(g["dX"]) + e @ np.abs(A).T + f * acc * (dHa @ np.abs(A).T)),
+        "dA": (harness.to_host(buf.dA_full()), g["dA"], np.abs(X).T @ e + M * acc * (np.abs(X).T @ dHa)),
+        "dB": (harness.to_host(buf.dB_full()), g["dB"], eY.T @ np.abs(dZ) + M * acc * (np.abs(Y).T @ np.abs(dZ))),
+        "db1": (harness.to_host(buf.db1_sh).reshape(-1), g["db1"], e.sum(axis=0) + M * acc * dHa.sum(axis=0)),
+    }
+    for name, (got, ref, bound) in bounds.items():
+        excess = np.abs(got - ref) - (bound + 1e-7)
+        assert float(np.max(excess)) <= 0.0, f"{name}: {float(np.max(excess)):.3e} beyond the element bound"
+
+
 def test_mixed_wave_shape(env, orc):
     """A shape whose row and dX GEMMs have 80 pair tiles (76 pairs fit at once), so the
     last wave holds 4 tiles, which walk K (and the shard sum) backwards; the
