@@ -130,3 +130,20 @@ def test_side_stream_registration_rules():
     assert T.tpmlp_set_side_stream(None, None, None) == T.OK
     assert T.tpmlp_set_side_stream(0x1000, None, None, check=False) == T.ERR_NULL
     assert T.tpmlp_set_side_stream(None, 0x1000, 0x2000, check=False) == T.ERR_NULL
+
+
+def test_tp_entry_points_validate_on_the_host():
+    """The rank-local entry points and the finish step refuse bad arguments before any CUDA call."""
+    assert T.tpmlp_sum_finish(None, None, 0x1000, 4, 8, check=False) == T.ERR_NULL
+    assert T.tpmlp_sum_finish(0x1000, None, 0x2000, 4, 12, check=False) == T.ERR_ALIGNMENT  # 12 bf16 = 24 B
+    assert T.tpmlp_sum_finish(0x1000, None, 0x1008, 4, 8, check=False) == T.ERR_ALIGNMENT
+    assert T.tpmlp_sum_finish(0x1000, None, 0x1000, 4, 8, check=False) == T.ERR_ALIAS
+    assert T.tpmlp_sum_finish(0x1000, None, 0x2000, -1, 8, check=False) == T.ERR_SHAPE
+    p16 = 0x10000
+    assert T.tpmlp_mlp_fwd_partial(p16, p16, None, p16, None, p16, None, 8, 2, 64, 256, 2, check=False) == T.ERR_NULL
+    assert T.tpmlp_mlp_fwd_partial(p16, p16, None, p16, p16 * 2, p16 * 3, None, 8, 2, 64, 250, 2,
+                                   check=False) == T.ERR_ALIGNMENT
+    assert T.tpmlp_mlp_bwd_partial(p16, p16, p16, p16, p16, p16, None, p16, p16, None, None, p16, 8, 2, 64, 256, 3,
+                                   check=False) == T.ERR_NULL
+    assert T.tpmlp_mlp_bwd_partial(p16, p16, p16, p16, p16, p16, p16 * 2, p16 * 3, p16 * 4, None, None, p16 * 5,
+                                   8, 2, 64, 256, 3, check=False) == T.ERR_DIVISIBILITY

@@ -170,3 +170,53 @@ def test_two_gpus_nccl(env, orc):
     for rank, Zr, dXr in out:
         U.assert_close(Zr, Z, "bf16", f"Z rank {rank}")
         U.assert_close(dXr, g["dX"], "bf16", f"dX rank {rank}")
+
+
+@pytest.mark.parametrize("rows,cols,with_bias,dt", [(1, 8, True, 0), (37, 264, True, 0), (512, 1024, False, 0),
+                                                  (37, 260, True, 1), (0, 64, True, 0)],
+                         ids=["one-row", "ragged", "no-bias", "fp32", "empty"])
+def test_sum_finish_bit_exact(env, rows, cols, with_bias, dt):
+    """round(S + bias) once, after the All-Reduce: bit-exact against torch's own fp32 add and
+    round-to-nearest-even conversion (bf16), or the plain fp32 sum."""
+    import torch
+    _, _, _, T = env
+    g = torch.Generator(device="cuda").manual_seed(rows * 7 + cols)
+    n = max(rows, 1)  # an empty call still passes valid buffers (pointers are checked first)
+    S = torch.randn((n, cols), dtype=torch.float32, device="cuda", generator=g) * 3.0
+    odt = torch.bfloat16 if dt == T.BF16 else torch.float32
+    bias = (torch.randn((cols,), dtype=torch.float32, device="cuda", generator=g).to(odt)) if with_bias else None
+    out = torch.full((n, cols), float("nan"), dtype=odt, device="cuda")
+    T.tpmlp_sum_finish(S, bias, out, rows, cols, dt=dt)
+    T.tpmlp_device_status()
+    want = (S + (bias.float() if with_bias else 0.0)).to(odt)
+    iv = torch.int16 if dt == T.BF16 else torch.int32
+    assert torch.equal(out[:rows].view(iv), want[:rows].view(iv))
+    if rows == 0:
+        assert bool(torch.isnan(out.float()).all())  # nothing written
+
+
+def test_emulated_ranks_fp32(env, orc):
+    """The fp32 path of the rank-local entry points (FMA GEMMs, no TF32): two ranks emulated on
+    one GPU, relative Frobenius error <= 1e-5 against the oracle."""
+    import torch
+    harness, synth, tp, T = env
+    wl = synth.custom(8, 2, 64, 256, 2, dtype="f32", sigma_w=0.05, sigma_bias=0.05, seed=64)
+    buf = harness.MLPBuffers(wl, backward=True)
+    s, b, h, f, _ = buf.dims()
+    M = s * b
+    Z_sum = torch.zeros((M, h), dtype=torch.float32, device="cuda")
+    dX_sum = torch.zeros((M, h), dtype=torch.float32, device="cuda")
+    for r in range(2):
+        lo, hi = tp.feature_range(r, 2, f)
+        A_sh, b1, B_sh = _rank_weights(harness, T, buf, lo, hi, 1)
+        ops = tp.LibraryRankOps(s, b, h, hi - lo, 1, dt=T.F32)
+        Zp, Y, H = ops.fwd_partial(buf.X, A_sh, b1, B_sh)
+        Z_sum += Zp
+        dX_sum += ops.bwd_partial(buf.X, A_sh, B_sh, H, Y, buf.dZ)["dX_part"]
+    Z, dX = ops.finish(Z_sum, buf.b2), ops.finish(dX_sum, None)
+    T.tpmlp_device_status()
+    x = U.host_inputs_f64(buf)
+    Hr, Yr, Zr = orc.mlp_fwd(x["X"], x["A"], x["b1"], x["B"], x["b2"])
+    gr = orc.mlp_bwd(x["X"], x["A"], x["B"], Hr, Yr, x["dZ"])
+    U.assert_close(harness.to_host(Z), Zr, "f32", "Z")
+    U.assert_close(harness.to_host(dX), gr["dX"], "f32", "dX")
