@@ -257,7 +257,7 @@ template <bool A_MN, bool B_MN, int EPI>
 tpmlp_status launch_splitk(const CUtensorMap& ma, const CUtensorMap& mb, const tc::KArgs& k, cudaStream_t st) {
     auto kern = tc::gemm_splitk_kernel<A_MN, B_MN, EPI>;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(4 * k.num_tiles);  // one tile per cluster of four
+    cfg.gridDim = dim3(4 * (k.num_tiles - k.tile_begin));  // one tile per cluster of four
     cfg.blockDim = dim3(tc::SK_THREADS);
     cfg.dynamicSmemBytes = tc::SK_SMEM;
     cfg.stream = st;
@@ -294,12 +294,22 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
     bool use_pair = cap > 0 && ((mode >= 2 && mode <= 4) || pair_tiles >= cap);
     // Split-K CTA pairs for a shard-summing GEMM whose 256x256 tiles are fewer than the pairs the
     // GPU holds (it would otherwise run on single-CTA tiles), with a K loop long enough to split.
-    constexpr bool kSplitOk = (EPI == EPI_BIAS_ACT && !A_MN && B_MN) || (EPI == EPI_STORE && !A_MN);
+    constexpr bool kSplitOk = (EPI == EPI_BIAS_ACT && !A_MN && B_MN) || (EPI == EPI_STORE && !A_MN) ||
+                              (EPI == EPI_STORE && A_MN && B_MN);
     bool split = false;
+    int tail = 0;  // > 0: the last partial wave's tiles, run as split-K after the full waves
     if constexpr (kSplitOk) {
         if (g.sum_shards && !k.accumulate && k.k_iters >= 2 && cap > 0 &&
             (mode == 5 || (mode == 0 && pair_tiles < cap && k.k_iters >= 16)))
             split = splitk_capacity<A_MN, B_MN, EPI>(dev) >= pair_tiles;
+        // A multi-wave GEMM whose last wave is at most half full: that wave's tiles on two CTA
+        // pairs each with half the K loop (the pair kernel takes the full waves), so the wave
+        // costs about half a tile time.
+        const int rem = cap > 0 ? pair_tiles % cap : 0;
+        // (long K loops only: their full waves keep the direct-store epilogue they would get anyway)
+        if (!split && (mode == 0 || mode == 5) && !k.accumulate && pair_tiles > cap && rem > 0 && 2 * rem <= cap &&
+            k.k_iters > kStagedMaxKBlocks && splitk_capacity<A_MN, B_MN, EPI>(dev) >= rem)
+            tail = rem;
     }
     if (split) use_pair = true;  // pair-shaped operand boxes
     constexpr bool kNarrowOk = EPI != EPI_SWIGLU && EPI != EPI_DSWIGLU;  // packed layouts span 256 columns
@@ -347,6 +357,14 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
     k.num_tiles = pair_tiles;
     if constexpr (kSplitOk) {
         if (split) return launch_splitk<A_MN, B_MN, EPI>(ma, mb, k, st);
+        if (tail > 0) {
+            tc::KArgs kf = k;  // the full waves on CTA pairs, direct-store epilogue (long K loops)
+            kf.num_tiles = pair_tiles - tail;
+            const tpmlp_status r = launch_pair<A_MN, B_MN, EPI, false>(ma, mb, ma, ma, kf, cap, st);
+            if (r != TPMLP_OK) return r;
+            k.tile_begin = pair_tiles - tail;
+            return launch_splitk<A_MN, B_MN, EPI>(ma, mb, k, st);
+        }
     }
     const int clusters = pair_tiles < cap ? pair_tiles : cap;
     // Short K loops (a tile's main loop shorter than a direct-store epilogue): staged epilogue.

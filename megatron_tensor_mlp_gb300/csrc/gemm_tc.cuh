@@ -69,6 +69,7 @@ struct KArgs {
     int a_chunked, b_chunked;  // MN-major operand loaded with one 4-D box per stage (MN extent % 64 == 0)
     int st32;                  // out, out2 and aux rows are 32-byte aligned: 32-byte global accesses
     int accumulate;            // EPI_STORE, fp32 out: out += acc (a later K chunk of a split contraction)
+    int tile_begin;            // pair and split-K kernels: this launch covers tiles [tile_begin, num_tiles)
     void* out; long long out_ld, out_ss;
     void* out2; long long out2_ld, out2_ss;
     const void* bias; long long bias_ss;
@@ -1068,7 +1069,7 @@ __global__ void __launch_bounds__(PairGeom<STAGED>::threads, 1)
             const int k_end = p.kb_per_shard * BK;
             const uint32_t full_leader0 = mapa_shared(smem_u32(full), pleader);  // the pair leader's barriers
             int lt = 0;
-            for (int t = cluster_id; t < p.num_tiles && ok; t += n_clusters, ++lt) {
+            for (int t = p.tile_begin + cluster_id; t < p.num_tiles && ok; t += n_clusters, ++lt) {
                 int mb, nb, shard;
                 decode_tile(p, t, mb, nb, shard);
                 const int row0 = mb * (2 * BM) + static_cast<int>(prank) * BM;
@@ -1174,7 +1175,7 @@ __global__ void __launch_bounds__(PairGeom<STAGED>::threads, 1)
                 uint32_t phase = 0;
                 int lt = 0;
                 bool ok = true;
-                for (int t = cluster_id; t < p.num_tiles && ok; t += n_clusters, ++lt) {
+                for (int t = p.tile_begin + cluster_id; t < p.num_tiles && ok; t += n_clusters, ++lt) {
                     const int acc = lt & 1;
                     const uint32_t acc_phase = (lt >> 1) & 1;
                     if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, p.status, p.timeout_ns, kWhereMma)) {
@@ -1221,7 +1222,7 @@ __global__ void __launch_bounds__(PairGeom<STAGED>::threads, 1)
         [[maybe_unused]] uint8_t* ebuf = sE + (warp - FIRST_EPI_WARP) * EPI_WARP_BYTES;  // STAGED only
         uint32_t seq = 0;
         int lt = 0;
-        for (int t = cluster_id; t < p.num_tiles; t += n_clusters, ++lt) {
+        for (int t = p.tile_begin + cluster_id; t < p.num_tiles; t += n_clusters, ++lt) {
             const int acc = lt & 1;
             const uint32_t acc_phase = (lt >> 1) & 1;
             if constexpr (EPI == EPI_DGELU) {
@@ -1303,7 +1304,8 @@ __global__ void __launch_bounds__(PairGeom<STAGED>::threads, 1)
 // Each CTA adds the two partials and runs the usual epilogue on its half.  Every TMA load
 // lands in the CTA that issues it (no multicast); every wait is bounded.
 //
-// One tile per cluster: the host launches 4 * num_tiles CTAs.
+// One tile per cluster: the host launches 4 * (num_tiles - tile_begin) CTAs.  Also used for the
+// last partial wave of a multi-wave GEMM, whose full waves run on gemm_pair_kernel.
 // ============================================================================
 constexpr int SK_THREADS = 256;     // warp 0 producer, warp 1 TMEM + UMMA issuer, warps 4-7 epilogue
 constexpr int SK_STAGES = 7;
@@ -1337,7 +1339,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1)
     const bool leader = prank == 0;
     const uint16_t pair_mask = static_cast<uint16_t>(0x3u << pleader);
     const uint32_t partner = rank ^ 2u;   // same rows, other K half
-    const int t = static_cast<int>(blockIdx.x) / 4;
+    const int t = p.tile_begin + static_cast<int>(blockIdx.x) / 4;
     const int kh = p.k_iters / 2;
     const int it0 = q ? kh : 0, it1 = q ? p.k_iters : kh;
 

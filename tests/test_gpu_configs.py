@@ -142,3 +142,49 @@ def test_two_million_token_weight_gradients_sampled(env, orc):
     U.assert_close(harness.to_host(buf.dB_full()[cidx]), dBr, "bf16", "dB rows")
     U.assert_close(harness.to_host(buf.db1_sh.reshape(-1)[cidx]), db1c, "bf16", "db1")
     U.assert_close(harness.to_host(buf.db2), orc.bwd_db2(dZ), "bf16", "db2")
+
+
+def test_last_wave_on_split_k_pairs(env, orc):
+    """A shape whose six GEMMs all have more 256x256 tiles than CTA pairs, a last wave at most
+    half full and K loops longer than 40 blocks (s=896 b=4 h=2568 ffn=5136 p=2: 308, 154 and 242
+    tiles, remainders 4, 2 and 14 on 76 pairs), so in automatic mode every GEMM runs its full
+    waves on CTA pairs and its last wave on split-K pairs of pairs.  Sampled rows and columns
+    against the oracle (the last token rows lie in the last wave's tiles), and every element
+    within fp32 reassociation of the same step on CTA pairs only (mode 3)."""
+    import torch
+    harness, synth, T = env
+    wl = synth.custom(896, 4, 2568, 5136, 2, dtype="bf16", sigma_w=0.02, sigma_bias=0.05, seed=91)
+    T.tpmlp_set_gemm_mode(3)
+    try:
+        ref = harness.MLPBuffers(wl, backward=True)
+        ref.fwd()
+        ref.bwd()
+        T.tpmlp_set_gemm_mode(0)
+        buf = harness.MLPBuffers(wl, backward=True, host=ref.host)
+        buf.fwd()
+        buf.bwd()
+        T.tpmlp_device_status()
+    finally:
+        T.tpmlp_set_gemm_mode(0)
+    for name, a, b in (("Z", buf.Z, ref.Z), ("dX", buf.dX, ref.dX), ("Y", buf.Y, ref.Y), ("dH", buf.dH, ref.dH)):
+        err = float((a.double() - b.double()).norm() / b.double().norm())
+        assert err < 2e-3, (name, err)
+    for name, a, b in (("dA", buf.dA_sh, ref.dA_sh), ("dB", buf.dB_sh, ref.dB_sh)):
+        err = float((a.double() - b.double()).norm() / b.double().norm())
+        assert err < 1e-5, (name, err)
+    M, h, f, p = wl.M, wl.h, wl.ffn, wl.p
+    widen = synth.widen
+    X, A, B, dZ = (widen(buf.host[k]) for k in ("X", "A", "B", "dZ"))
+    b1, b2 = widen(buf.host["b1"]), widen(buf.host["b2"])
+    rows = _rows(M, 6, 91)
+    Hr, Yr, Zr = orc.mlp_fwd(X[rows], A, b1, B, b2)
+    ridx = torch.from_numpy(rows).cuda()
+    U.assert_close(harness.to_host(buf.Z[ridx]), Zr, "bf16", "Z rows")
+    cols = _cols(f, p, 4, 91)
+    dAc, dBr, db1c = orc.bwd_ffn_cols(X, A, b1, B, dZ, cols)
+    cidx = torch.from_numpy(cols).cuda()
+    U.assert_close(harness.to_host(buf.dA_full()[:, cidx]), dAc, "bf16", "dA cols")
+    U.assert_close(harness.to_host(buf.dB_full()[cidx]), dBr, "bf16", "dB rows")
+    xr = np.array([0, M // 2, M - 2, M - 1], dtype=np.int64)
+    dXr = orc.bwd_dX_rows(X, A, b1, B, dZ, xr)
+    U.assert_close(harness.to_host(buf.dX[torch.from_numpy(xr).cuda()]), dXr, "bf16", "dX rows")
