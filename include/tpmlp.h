@@ -396,6 +396,13 @@ const char* tpmlp_last_error(void);
 /* Library version: major * 10000 + minor * 100 + patch. */
 int tpmlp_version(void);
 
+/* Number of kernels this library has launched in this process, on any thread, stream
+ * or device, since it was loaded: one per launch the runtime accepted, counted on the
+ * host when the launch is enqueued (not when it runs).  A call rejected by argument
+ * validation launches and counts nothing.  The difference of two readings around a
+ * region is how many of this library's kernels the region enqueued. */
+uint64_t tpmlp_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -162,6 +162,7 @@ tpmlp_status launch_single(const CUtensorMap& ma, const CUtensorMap& mb, const t
         set_error("tcgen05 GEMM launch: %s", cudaGetErrorString(e));
         return TPMLP_ERR_CUDA;
     }
+    count_launch();
     return TPMLP_OK;
 }
 
@@ -220,6 +221,7 @@ tpmlp_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
         set_error("tcgen05 CTA-pair GEMM launch: %s", cudaGetErrorString(e));
         return TPMLP_ERR_CUDA;
     }
+    count_launch();
     return TPMLP_OK;
 }
 
@@ -276,6 +278,7 @@ tpmlp_status launch_splitk(const CUtensorMap& ma, const CUtensorMap& mb, const t
         set_error("tcgen05 split-K GEMM launch: %s", cudaGetErrorString(e));
         return TPMLP_ERR_CUDA;
     }
+    count_launch();
     return TPMLP_OK;
 }
 

@@ -57,6 +57,10 @@ const DeviceInfo* device_info();
 
 void set_error(const char* fmt, ...);
 
+// Adds one to the process-wide count of kernels this library has launched
+// (tpmlp_launch_count); every launcher calls it once per accepted launch.
+void count_launch();
+
 // Kernel launchers (all return TPMLP_OK or TPMLP_ERR_CUDA with the message set).
 tpmlp_status launch_tc_gemm(const Operand& a, const Operand& b, const GemmSpec& g, const DeviceInfo& dev,
                             cudaStream_t st);

@@ -377,6 +377,7 @@ tpmlp_status check_launch(const char* what) {
         set_error("%s launch: %s", what, cudaGetErrorString(e));
         return TPMLP_ERR_CUDA;
     }
+    count_launch();
     return TPMLP_OK;
 }
 

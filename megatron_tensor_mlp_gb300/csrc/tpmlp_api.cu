@@ -2,6 +2,7 @@
 // per-device state, and the mapping of each entry point onto GEMM launches.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -17,6 +18,7 @@ __device__ uint32_t g_status_word;
 
 namespace {
 thread_local char t_err[512] = "";
+std::atomic<uint64_t> g_launches{0};
 
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
@@ -371,6 +373,8 @@ void set_error(const char* fmt, ...) {
     std::vsnprintf(t_err, sizeof(t_err), fmt, ap);
     va_end(ap);
 }
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 const DeviceInfo* device_info() {
     int dev = 0;
@@ -899,6 +903,8 @@ const char* tpmlp_status_string(tpmlp_status st) {
 const char* tpmlp_last_error(void) { return t_err; }
 
 int tpmlp_version(void) { return 200; }
+
+uint64_t tpmlp_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 tpmlp_status tpmlp_set_side_stream(void* side_stream, void* fork_event, void* join_event) {
     if (!side_stream && !fork_event && !join_event) {

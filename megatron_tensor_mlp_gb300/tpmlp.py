@@ -74,6 +74,8 @@ lib.tpmlp_get_gemm_mode.argtypes = []
 lib.tpmlp_get_gemm_mode.restype = ctypes.c_int
 lib.tpmlp_version.argtypes = []
 lib.tpmlp_version.restype = ctypes.c_int
+lib.tpmlp_launch_count.argtypes = []
+lib.tpmlp_launch_count.restype = ctypes.c_uint64
 
 
 class TpmlpError(RuntimeError):
@@ -284,3 +286,8 @@ def tpmlp_last_error() -> str:
 
 def tpmlp_version() -> int:
     return int(lib.tpmlp_version())
+
+
+def tpmlp_launch_count() -> int:
+    """Kernels this library has enqueued in this process so far (host-side count)."""
+    return int(lib.tpmlp_launch_count())

@@ -147,3 +147,11 @@ def test_tp_entry_points_validate_on_the_host():
                                    check=False) == T.ERR_NULL
     assert T.tpmlp_mlp_bwd_partial(p16, p16, p16, p16, p16, p16, p16 * 2, p16 * 3, p16 * 4, None, None, p16 * 5,
                                    8, 2, 64, 256, 3, check=False) == T.ERR_DIVISIBILITY
+
+
+def test_rejected_calls_launch_nothing():
+    n0 = T.tpmlp_launch_count()
+    assert _fwd(X=None) == T.ERR_NULL
+    assert _fwd(ffn=250, p=4) == T.ERR_DIVISIBILITY
+    assert T.tpmlp_sum_finish(None, None, 0x1000, 4, 8, check=False) == T.ERR_NULL
+    assert T.tpmlp_launch_count() == n0
