@@ -332,16 +332,22 @@ tpmlp_status tpmlp_debug_wait_timeout(uint32_t timeout_us, void* stream);
 
 /*
  * Optional side stream for the fused backwards (tpmlp_mlp_bwd, tpmlp_mlp_bwd_partial,
- * tpmlp_swiglu_mlp_bwd).  Their bias-gradient column sums (db1 = 1^T dH, db2 = 1^T dZ) need
- * no tensor cores; with a stream and two events of the caller's registered here, they run
- * on that stream beside the dX GEMM, on the SMs its last wave of tiles leaves idle: the
- * side stream waits for an event recorded on `stream` after the dA launch, and `stream`
- * waits for an event recorded on the side stream after the sums, so everything is
- * complete, in order, when the work enqueued on `stream` is.  The sums go there only
- * where it pays: bf16 tensors, dX's last wave keeping at most half of the CTA pairs busy,
- * and at most 2.6e-4 bytes of sums per dX flop (the fwd+bwd bench workload qualifies);
- * elsewhere, and with nothing registered, they run in line on `stream`.  Either way the
- * results are the same bit for bit.
+ * tpmlp_swiglu_mlp_bwd), for bf16 tensors.  With a stream and two events of the caller's
+ * registered here:
+ *   - tpmlp_mlp_bwd and tpmlp_mlp_bwd_partial run their two pairs of independent GEMMs side
+ *     by side, each GEMM on a share of the SMs, where that is clearly faster than one after
+ *     the other (GEMMs of one or two waves of tiles, e.g. s=512 b=4 h=1024 ffn=4096 p=4):
+ *     dH_i on `stream` beside dB_i (then db2) on the side stream, then dA_i (after db1) on
+ *     `stream` beside dX on the side stream;
+ *   - otherwise the bias-gradient column sums (db1 = 1^T dH, db2 = 1^T dZ), which need no
+ *     tensor cores, run on the side stream beside the first of the dA and dX GEMMs whose grid
+ *     leaves enough SMs idle for all of them; where no GEMM does, they run in line.
+ * The side stream waits for an event recorded on `stream` before its first kernel (and, for
+ * dX, after dH), and `stream` waits for an event recorded on the side stream after its last,
+ * so everything is complete, in order, when the work enqueued on `stream` is.  With nothing
+ * registered everything runs in line on `stream`.  dH, dB, dA, db1 and db2 have the same bits
+ * either way; dX, where it runs side by side, may differ in the last place of a few values
+ * (its fp32 partial sums added in another order).
  *   The registration is per host thread and bound to the device current at this call;
  *   the stream must belong to that device.  The library never creates, destroys or
  *   synchronises these objects: the caller keeps them alive while registered (events

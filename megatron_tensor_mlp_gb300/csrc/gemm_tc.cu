@@ -140,12 +140,13 @@ bool make_map_chunked(CUtensorMap* map, const Operand& op, uint64_t mn, uint64_t
 
 template <bool A_MN, bool B_MN, int EPI, int SBN>
 tpmlp_status launch_single(const CUtensorMap& ma, const CUtensorMap& mb, const tc::KArgs& k, const DeviceInfo& dev,
-                           cudaStream_t st) {
+                           int max_grid, cudaStream_t st) {
     auto kern = tc::gemm_kernel<A_MN, B_MN, EPI, SBN>;
     constexpr int smem = tc::SingleGeom<SBN>::smem_bytes;
     static bool attr_done[64] = {};
     if (!set_smem_attr(kern, dev.device, smem, attr_done)) return TPMLP_ERR_CUDA;
-    const int grid = k.num_tiles < dev.sm_count ? k.num_tiles : dev.sm_count;
+    int grid = k.num_tiles < dev.sm_count ? k.num_tiles : dev.sm_count;
+    if (max_grid > 0 && grid > max_grid) grid = max_grid;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(tc::NUM_THREADS);
@@ -285,15 +286,17 @@ tpmlp_status launch_splitk(const CUtensorMap& ma, const CUtensorMap& mb, const t
 // Picks the tiling and launches.  CTA-pair 256x256 tiles when there are at least as many
 // of them as co-resident pairs (or when forced); otherwise single-CTA 128x256 tiles, or
 // 128x128 tiles when the 128x256 ones would leave more than half of the SMs idle.
-// sms_out != nullptr: only report how many SMs the launch would occupy (its persistent grid), and
-// launch nothing.
+// g.max_sms > 0 caps the grid at that many SMs (a GEMM run beside another on the rest).
+// plan_out != nullptr: only report how the launch would run (GemmPlan), and launch nothing.
 template <bool A_MN, bool B_MN, int EPI>
 tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& g, tc::KArgs k, const DeviceInfo& dev,
-                            cudaStream_t st, int* sms_out = nullptr) {
+                            cudaStream_t st, GemmPlan* plan_out = nullptr) {
     const int mode = g_gemm_mode.load(std::memory_order_relaxed);
     const int m_pairs = static_cast<int>((g.M + 2 * tc::BM - 1) / (2 * tc::BM));
     const int pair_tiles = m_pairs * k.n_blocks * k.batch;
     int cap = (mode == 1) ? 0 : pair_capacity<A_MN, B_MN, EPI, false>(dev);
+    if (g.max_sms > 0 && cap > g.max_sms / 2) cap = g.max_sms / 2;
+    const int sm_cap = g.max_sms > 0 && g.max_sms < dev.sm_count ? g.max_sms : dev.sm_count;
     bool use_pair = cap > 0 && ((mode >= 2 && mode <= 4) || pair_tiles >= cap);
     // Split-K CTA pairs for a shard-summing GEMM whose 256x256 tiles are fewer than the pairs the
     // GPU holds (it would otherwise run on single-CTA tiles), with a K loop long enough to split.
@@ -304,14 +307,14 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
     if constexpr (kSplitOk) {
         if (g.sum_shards && !k.accumulate && k.k_iters >= 2 && cap > 0 &&
             (mode == 5 || (mode == 0 && pair_tiles < cap && k.k_iters >= 16)))
-            split = splitk_capacity<A_MN, B_MN, EPI>(dev) >= pair_tiles;
+            split = splitk_capacity<A_MN, B_MN, EPI>(dev) >= pair_tiles && 4 * pair_tiles <= sm_cap;
         // A multi-wave GEMM whose last wave is at most half full: that wave's tiles on two CTA
         // pairs each with half the K loop (the pair kernel takes the full waves), so the wave
         // costs about half a tile time.
         const int rem = cap > 0 ? pair_tiles % cap : 0;
         // (long K loops only: their full waves keep the direct-store epilogue they would get anyway)
-        if (!split && (mode == 0 || mode == 5) && !k.accumulate && pair_tiles > cap && rem > 0 && 2 * rem <= cap &&
-            k.k_iters > kStagedMaxKBlocks && splitk_capacity<A_MN, B_MN, EPI>(dev) >= rem)
+        if (!split && (mode == 0 || mode == 5) && !k.accumulate && g.max_sms == 0 && pair_tiles > cap && rem > 0 &&
+            2 * rem <= cap && k.k_iters > kStagedMaxKBlocks && splitk_capacity<A_MN, B_MN, EPI>(dev) >= rem)
             tail = rem;
     }
     if (split) use_pair = true;  // pair-shaped operand boxes
@@ -322,14 +325,16 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
     if (!use_pair && cap > 0 && (mode == 0 || mode == 5) && !(kNarrowOk && 2 * k.num_tiles <= dev.sm_count && g.N > 128))
         use_pair = true;
     const bool narrow = kNarrowOk && !use_pair && 2 * k.num_tiles <= dev.sm_count && g.N > 128;
-    if (sms_out) {
+    if (plan_out) {
         if (split) {
-            *sms_out = 4 * pair_tiles;
+            *plan_out = GemmPlan{4 * pair_tiles, pair_tiles, pair_tiles, (k.k_iters + 1) / 2, 1};
         } else if (use_pair) {
-            *sms_out = 2 * (pair_tiles < cap ? pair_tiles : cap);
+            const int clusters = pair_tiles < cap ? pair_tiles : cap;
+            *plan_out = GemmPlan{2 * clusters, pair_tiles, clusters, k.k_iters, 0};
         } else {
             const int tiles = narrow ? k.m_blocks * static_cast<int>((g.N + 127) / 128) * k.batch : k.num_tiles;
-            *sms_out = tiles < dev.sm_count ? tiles : dev.sm_count;
+            const int grid = tiles < sm_cap ? tiles : sm_cap;
+            *plan_out = GemmPlan{grid, tiles, grid, k.k_iters, 0};
         }
         return TPMLP_OK;
     }
@@ -351,13 +356,17 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
             if (narrow) {
                 k.n_blocks = static_cast<int>((g.N + 127) / 128);
                 k.num_tiles = k.m_blocks * k.n_blocks * k.batch;
-                return launch_single<A_MN, B_MN, EPI, 128>(ma, mb, k, dev, st);
+                return launch_single<A_MN, B_MN, EPI, 128>(ma, mb, k, dev, sm_cap, st);
             }
         }
-        return launch_single<A_MN, B_MN, EPI, 256>(ma, mb, k, dev, st);
+        return launch_single<A_MN, B_MN, EPI, 256>(ma, mb, k, dev, sm_cap, st);
     }
     k.m_blocks = m_pairs;
     k.num_tiles = pair_tiles;
+    {
+        const int full = pair_capacity<A_MN, B_MN, EPI, false>(dev);  // the uncapped grid's clusters
+        k.rev_period = full > 0 ? full : 1;
+    }
     if constexpr (kSplitOk) {
         if (split) return launch_splitk<A_MN, B_MN, EPI>(ma, mb, k, st);
         if (tail > 0) {
@@ -387,7 +396,7 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
 }
 
 tpmlp_status launch_one(const Operand& a, const Operand& b, const GemmSpec& g, const DeviceInfo& dev,
-                        cudaStream_t st, bool accumulate, int* sms_out = nullptr) {
+                        cudaStream_t st, bool accumulate, GemmPlan* plan_out = nullptr) {
     tc::KArgs k{};
     k.accumulate = accumulate ? 1 : 0;
     k.M = static_cast<int>(g.M);
@@ -438,21 +447,21 @@ tpmlp_status launch_one(const Operand& a, const Operand& b, const GemmSpec& g, c
                      : 0;
     }
     if (k.num_tiles == 0) {
-        if (sms_out) *sms_out = 0;
+        if (plan_out) *plan_out = GemmPlan{0, 0, 0, 0, 0};
         return TPMLP_OK;
     }
 
     const bool amn = a.mn_major, bmn = b.mn_major;
     if (g.epi == EPI_BIAS_ACT && !amn && bmn)
-        return launch_variant<false, true, EPI_BIAS_ACT>(a, b, g, k, dev, st, sms_out);
-    if (g.epi == EPI_DGELU && !amn && !bmn) return launch_variant<false, false, EPI_DGELU>(a, b, g, k, dev, st, sms_out);
-    if (g.epi == EPI_SWIGLU && !amn && bmn) return launch_variant<false, true, EPI_SWIGLU>(a, b, g, k, dev, st, sms_out);
+        return launch_variant<false, true, EPI_BIAS_ACT>(a, b, g, k, dev, st, plan_out);
+    if (g.epi == EPI_DGELU && !amn && !bmn) return launch_variant<false, false, EPI_DGELU>(a, b, g, k, dev, st, plan_out);
+    if (g.epi == EPI_SWIGLU && !amn && bmn) return launch_variant<false, true, EPI_SWIGLU>(a, b, g, k, dev, st, plan_out);
     if (g.epi == EPI_DSWIGLU && !amn && !bmn)
-        return launch_variant<false, false, EPI_DSWIGLU>(a, b, g, k, dev, st, sms_out);
-    if (g.epi == EPI_STORE && amn && bmn) return launch_variant<true, true, EPI_STORE>(a, b, g, k, dev, st, sms_out);
-    if (g.epi == EPI_STORE && !amn && bmn) return launch_variant<false, true, EPI_STORE>(a, b, g, k, dev, st, sms_out);
+        return launch_variant<false, false, EPI_DSWIGLU>(a, b, g, k, dev, st, plan_out);
+    if (g.epi == EPI_STORE && amn && bmn) return launch_variant<true, true, EPI_STORE>(a, b, g, k, dev, st, plan_out);
+    if (g.epi == EPI_STORE && !amn && bmn) return launch_variant<false, true, EPI_STORE>(a, b, g, k, dev, st, plan_out);
     if (g.epi == EPI_STORE && !amn && !bmn)
-        return launch_variant<false, false, EPI_STORE>(a, b, g, k, dev, st, sms_out);
+        return launch_variant<false, false, EPI_STORE>(a, b, g, k, dev, st, plan_out);
     set_error("internal: no tcgen05 GEMM variant for epi=%d a_mn=%d b_mn=%d", g.epi, (int)amn, (int)bmn);
     return TPMLP_ERR_CUDA;
 }
@@ -487,11 +496,18 @@ tpmlp_status launch_tc_gemm(const Operand& a, const Operand& b, const GemmSpec& 
     return TPMLP_OK;
 }
 
-int tc_gemm_sms(const Operand& a, const Operand& b, const GemmSpec& g, const DeviceInfo& dev) {
+bool tc_gemm_plan(const Operand& a, const Operand& b, const GemmSpec& g, const DeviceInfo& dev, GemmPlan* plan) {
     // the first launch of a split contraction is the widest (each later one covers the same tiles)
-    int sms = 0;
-    if (launch_one(a, b, g, dev, nullptr, false, &sms) != TPMLP_OK) return dev.sm_count;
-    return sms;
+    const int64_t chunk = static_cast<int64_t>(g_k_chunk_blocks.load(std::memory_order_relaxed)) * tc::BK;
+    GemmSpec gc = g;
+    if (g.epi == EPI_STORE && g.out_f32 && !g.sum_shards && g.K > chunk) gc.K = chunk;
+    return launch_one(a, b, gc, dev, nullptr, false, plan) == TPMLP_OK;
+}
+
+int tc_gemm_sms(const Operand& a, const Operand& b, const GemmSpec& g, const DeviceInfo& dev) {
+    GemmPlan pl{};
+    if (!tc_gemm_plan(a, b, g, dev, &pl)) return dev.sm_count;
+    return pl.sms;
 }
 
 void set_k_chunk_blocks(int blocks) {

@@ -70,6 +70,7 @@ struct KArgs {
     int st32;                  // out, out2 and aux rows are 32-byte aligned: 32-byte global accesses
     int accumulate;            // EPI_STORE, fp32 out: out += acc (a later K chunk of a split contraction)
     int tile_begin;            // pair and split-K kernels: this launch covers tiles [tile_begin, num_tiles)
+    int rev_period;            // pair kernel: tile t walks K backwards when (t / rev_period) is odd
     void* out; long long out_ld, out_ss;
     void* out2; long long out2_ld, out2_ss;
     const void* bias; long long bias_ss;
@@ -1068,17 +1069,17 @@ __global__ void __launch_bounds__(PairGeom<STAGED>::threads, 1)
             bool ok = true;
             const int k_end = p.kb_per_shard * BK;
             const uint32_t full_leader0 = mapa_shared(smem_u32(full), pleader);  // the pair leader's barriers
-            int lt = 0;
-            for (int t = p.tile_begin + cluster_id; t < p.num_tiles && ok; t += n_clusters, ++lt) {
+            for (int t = p.tile_begin + cluster_id; t < p.num_tiles && ok; t += n_clusters) {
                 int mb, nb, shard;
                 decode_tile(p, t, mb, nb, shard);
                 const int row0 = mb * (2 * BM) + static_cast<int>(prank) * BM;
                 const int col0 = nb * BN + static_cast<int>(prank) * (BN / 2);
                 // Odd waves walk K backwards: a tile of the next wave usually shares its
                 // A (or B) panel with a tile of this one, and starts on the K range that
-                // this wave read last and the L2 still holds.  (Each tile's accumulation
-                // order is fixed by its index, so results stay deterministic.)
-                const bool rev = (lt & 1) != 0;
+                // this wave read last and the L2 still holds.  Waves are counted as those
+                // of the full grid (rev_period tiles each), so a tile's accumulation order,
+                // and its bits, do not depend on the grid it runs on.
+                const bool rev = ((t / p.rev_period) & 1) != 0;
                 int sa = p.sum_shards ? (rev ? p.n_shards - 1 : 0) : (p.a_batched ? shard : 0);
                 int sb = p.sum_shards ? (rev ? p.n_shards - 1 : 0) : (p.b_batched ? shard : 0);
                 int k0 = rev ? k_end - BK : 0;

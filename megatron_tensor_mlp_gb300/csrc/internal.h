@@ -43,6 +43,18 @@ struct GemmSpec {
     void* out2; int64_t out2_ld, out2_ss;         // pre-activation save (EPI_BIAS_ACT), may be null
     const void* bias; int64_t bias_ss;            // [shard][N] of the input dtype, may be null
     const void* aux; int64_t aux_ld, aux_ss;      // EPI_DGELU: H
+    int max_sms;         // > 0: the launch occupies at most this many SMs (a GEMM run beside another)
+};
+
+// How a tcgen05 GEMM would run (tc_gemm_plan): the SMs its grid occupies, its work tiles, how
+// many of them are in flight at once, the K blocks (of 64) each CTA pair or CTA accumulates
+// per tile, and whether two CTA pairs split each tile's K loop.
+struct GemmPlan {
+    int sms;
+    int tiles;
+    int slots;
+    int k_blocks;
+    int split_k;
 };
 
 struct DeviceInfo {
@@ -84,10 +96,14 @@ tpmlp_status launch_sum_finish(const float* S, const void* bias, void* out, int6
 tpmlp_status launch_swiglu_pack(void* G, void* U, void* W_sh, int64_t rows, int64_t ffn, int p, int esize,
                                 bool inverse, cudaStream_t st);
 
-// Process-wide GEMM tiling mode (see tpmlp_set_gemm_mode).
-// SMs a bf16 GEMM launch of launch_tc_gemm occupies for its whole run (its persistent grid: CTA
-// pairs or single CTAs, one per SM), by the same tiling decision; nothing is launched.
+// How a bf16 GEMM launch of launch_tc_gemm would run, by the same tiling decision (false when
+// no tcgen05 variant takes it); nothing is launched.  A K-chunked fp32 contraction reports its
+// first launch.
+bool tc_gemm_plan(const Operand& a, const Operand& b, const GemmSpec& g, const DeviceInfo& dev, GemmPlan* plan);
+// SMs such a launch occupies for its whole run (its persistent grid: CTA pairs or single CTAs,
+// one per SM).
 int tc_gemm_sms(const Operand& a, const Operand& b, const GemmSpec& g, const DeviceInfo& dev);
+// Process-wide GEMM tiling mode (see tpmlp_set_gemm_mode).
 void set_gemm_mode(int mode);
 int get_gemm_mode();
 void set_group_m(int g);

@@ -2,6 +2,7 @@
 // per-device state, and the mapping of each entry point onto GEMM launches.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -197,39 +198,57 @@ tpmlp_status do_row_partial(const void* Y_sh, const void* B_sh, float* Z_part, i
     return run_gemm(a, b, g, dt, dev, st);
 }
 
+// One GEMM launch: its operands and everything else.
+struct GemmCall {
+    Operand a, b;
+    GemmSpec g;
+};
+tpmlp_status run_call(const GemmCall& c, tpmlp_dtype dt, const DeviceInfo& dev, cudaStream_t st, int max_sms = 0) {
+    GemmSpec g = c.g;
+    g.max_sms = max_sms;
+    return run_gemm(c.a, c.b, g, dt, dev, st);
+}
+
+// dY_i = dZ B_i^T, times GeLU'(H_i) when act is GeLU (K = h)
+GemmCall dY_call(const void* B_sh, const void* dZ, const void* H_sh, void* dY_sh, int64_t M, int64_t h, int64_t ffn,
+                 int p, tpmlp_dtype dt, int act) {
+    const int64_t fs = ffn / p;
+    GemmCall c{{dZ, h, 0, 1, false},            // dZ [M][h]: [M][K]
+               {B_sh, h, fs * h, p, false},     // B_i [fs][h]: [N][K], K-major
+               spec_base()};
+    c.g.M = M; c.g.N = fs; c.g.K = h; c.g.n_shards = p;
+    c.g.a_batched = false; c.g.b_batched = true;
+    if (act == TPMLP_ACT_GELU_ERF) {
+        c.g.epi = EPI_DGELU;
+        c.g.aux = H_sh; c.g.aux_ld = fs; c.g.aux_ss = M * fs;
+    } else {
+        c.g.epi = EPI_STORE;
+        c.g.out_f32 = (dt == TPMLP_F32);
+    }
+    c.g.out = dY_sh; c.g.out_ld = fs; c.g.out_ss = M * fs;
+    return c;
+}
+// dB_i = Y_i^T dZ (K = tokens)
+GemmCall dB_call(const void* Y_sh, const void* dZ, void* dB_sh, int64_t M, int64_t h, int64_t ffn, int p,
+                 bool grad_f32) {
+    const int64_t fs = ffn / p;
+    GemmCall c{{Y_sh, fs, M * fs, p, true},     // Y_i [M][fs]: [K][M_gemm], MN-major
+               {dZ, h, 0, 1, true},             // dZ [M][h]: [K][N], MN-major
+               spec_base()};
+    c.g.M = fs; c.g.N = h; c.g.K = M; c.g.n_shards = p;
+    c.g.a_batched = true; c.g.b_batched = false;
+    c.g.epi = EPI_STORE; c.g.out_f32 = grad_f32;
+    c.g.out = dB_sh; c.g.out_ld = h; c.g.out_ss = fs * h;
+    return c;
+}
+
 // Row layer backward: dY_i = dZ B_i^T (times GeLU'(H_i) when act is GeLU), dB_i = Y_i^T dZ, db2.
 tpmlp_status do_row_bwd(const void* Y_sh, const void* B_sh, const void* dZ, const void* H_sh, void* dY_sh,
                         void* dB_sh, void* db2, int64_t M, int64_t h, int64_t ffn, int p, tpmlp_dtype dt,
                         bool grad_f32, int act, const DeviceInfo& dev, cudaStream_t st) {
-    const int64_t fs = ffn / p;
-    {
-        Operand a{dZ, h, 0, 1, false};               // dZ [M][h]: [M][K]
-        Operand bb{B_sh, h, fs * h, p, false};       // B_i [fs][h]: [N][K], K-major
-        GemmSpec g = spec_base();
-        g.M = M; g.N = fs; g.K = h; g.n_shards = p;
-        g.a_batched = false; g.b_batched = true;
-        if (act == TPMLP_ACT_GELU_ERF) {
-            g.epi = EPI_DGELU;
-            g.aux = H_sh; g.aux_ld = fs; g.aux_ss = M * fs;
-        } else {
-            g.epi = EPI_STORE;
-            g.out_f32 = (dt == TPMLP_F32);
-        }
-        g.out = dY_sh; g.out_ld = fs; g.out_ss = M * fs;
-        TP_TRY(run_gemm(a, bb, g, dt, dev, st));
-    }
+    TP_TRY(run_call(dY_call(B_sh, dZ, H_sh, dY_sh, M, h, ffn, p, dt, act), dt, dev, st));
     if (db2) TP_TRY(launch_colsum(dZ, dt == TPMLP_F32, 1, M, h, db2, grad_f32, st));
-    {
-        Operand a{Y_sh, fs, M * fs, p, true};        // Y_i [M][fs]: [K][M_gemm], MN-major
-        Operand bb{dZ, h, 0, 1, true};               // dZ [M][h]: [K][N], MN-major
-        GemmSpec g = spec_base();
-        g.M = fs; g.N = h; g.K = M; g.n_shards = p;
-        g.a_batched = true; g.b_batched = false;
-        g.epi = EPI_STORE; g.out_f32 = grad_f32;
-        g.out = dB_sh; g.out_ld = h; g.out_ss = fs * h;
-        TP_TRY(run_gemm(a, bb, g, dt, dev, st));
-    }
-    return TPMLP_OK;
+    return run_call(dB_call(Y_sh, dZ, dB_sh, M, h, ffn, p, grad_f32), dt, dev, st);
 }
 
 // Column sums run beside a GEMM on the caller's side stream (tpmlp_set_side_stream).
@@ -239,11 +258,6 @@ struct SideSums {
 };
 tpmlp_status side_fork(const SideSums& w, cudaStream_t st);
 
-// The two GEMMs of the column layer backward.
-struct GemmCall {
-    Operand a, b;
-    GemmSpec g;
-};
 // dA_i = X^T dY_i (K = tokens)
 GemmCall dA_call(const void* X, const void* dY_sh, void* dA_sh, int64_t M, int64_t h, int64_t ffn, int p,
                  bool grad_f32) {
@@ -350,6 +364,150 @@ tpmlp_status column_bwd_with_db2(const void* X, const void* A_sh, const void* dY
         return TPMLP_ERR_CUDA;
     }
     return TPMLP_OK;
+}
+
+// ---------------------------------------------------------------- two GEMMs side by side
+// A GEMM of one or two waves of tiles spends much of its launch filling its pipeline and
+// draining its last tile's epilogue, with SMs idle behind its last partial wave.  Two
+// independent ones -- dH_i and dB_i of the row layer's backward, dA_i and dX of the column
+// layer's -- then finish sooner side by side, each on its share of the SMs, than one after the
+// other.  Costs are in K-block times (one 64-deep K step of a CTA pair's 256x256 tile, about
+// 0.27 us at the boost clock): a GEMM's waves of tiles, each the longer of its K loop and a
+// short-K tile's epilogue, plus the last tile's epilogue, which nothing overlaps, plus the
+// exchange of a split-K GEMM's partial sums.
+constexpr double kEpilogueBlocks = 18.0;  // a short-K tile's epilogue (measured 4.5-5.7 us)
+constexpr double kExchangeBlocks = 8.0;   // split-K partial sums through distributed shared memory (~2 us)
+constexpr double kLaunchBlocks = 10.0;    // the gap between two dependent launches (~2.5-3 us)
+
+double gemm_cost(const GemmCall& c, const DeviceInfo& dev, int sms) {
+    GemmSpec g = c.g;
+    g.max_sms = sms;
+    GemmPlan pl{};
+    if (!tc_gemm_plan(c.a, c.b, g, dev, &pl)) return 1e30;
+    if (pl.tiles == 0) return 0.0;
+    if (pl.slots <= 0) return 1e30;
+    const int waves = (pl.tiles + pl.slots - 1) / pl.slots;
+    const double per_tile = pl.k_blocks > kEpilogueBlocks ? pl.k_blocks : kEpilogueBlocks;
+    return waves * per_tile + kEpilogueBlocks + (pl.split_k ? kExchangeBlocks : 0.0);
+}
+
+// SMs for `a` when `a` and `b` should run side by side (`b` takes the rest; even counts, as CTA
+// pairs take two), or 0 when one after the other is about as fast.
+int side_by_side_sms(const GemmCall& a, const GemmCall& b, const DeviceInfo& dev) {
+    const int S = dev.sm_count;
+    const double apart = gemm_cost(a, dev, S) + gemm_cost(b, dev, S) + kLaunchBlocks;
+    double best = apart;
+    int best_x = 0;
+    for (int x = 2; x + 2 <= S; x += 2) {
+        const double c = std::max(gemm_cost(a, dev, x), gemm_cost(b, dev, S - x));
+        if (c < best) {
+            best = c;
+            best_x = x;
+        }
+    }
+    return best < 0.9 * apart ? best_x : 0;  // the fork and join cost a little too
+}
+
+// The two splits of a backward (dH | dB, dA | dX), remembered per shape for this thread.
+struct SplitKey {
+    int64_t M, h, ffn;
+    int p, device, mode, group_m, gf32, dx32;
+    bool operator==(const SplitKey& o) const {
+        return M == o.M && h == o.h && ffn == o.ffn && p == o.p && device == o.device && mode == o.mode &&
+               group_m == o.group_m && gf32 == o.gf32 && dx32 == o.dx32;
+    }
+};
+struct SplitMemo {
+    SplitKey key[4];
+    int x1[4], x2[4];
+    int n = 0, next = 0;
+};
+thread_local SplitMemo t_split;
+
+void backward_splits(const GemmCall& dy, const GemmCall& db, const GemmCall& da, const GemmCall& dx, const SplitKey& key,
+                     const DeviceInfo& dev, int* x1, int* x2) {
+    for (int i = 0; i < t_split.n; ++i) {
+        if (t_split.key[i] == key) {
+            *x1 = t_split.x1[i];
+            *x2 = t_split.x2[i];
+            return;
+        }
+    }
+    *x1 = side_by_side_sms(dy, db, dev);
+    *x2 = side_by_side_sms(da, dx, dev);
+    const int i = t_split.next;
+    t_split.key[i] = key;
+    t_split.x1[i] = *x1;
+    t_split.x2[i] = *x2;
+    t_split.next = (i + 1) % 4;
+    if (t_split.n < 4) ++t_split.n;
+}
+
+tpmlp_status record_and_wait(cudaEvent_t ev, cudaStream_t from, cudaStream_t to, const char* what) {
+    cudaError_t e = cudaEventRecord(ev, from);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(to, ev, 0);
+    if (e != cudaSuccess) {
+        set_error("%s: %s", what, cudaGetErrorString(e));
+        return TPMLP_ERR_CUDA;
+    }
+    return TPMLP_OK;
+}
+
+// The block backward (GeLU' fused) from dZ.  With a side stream of the caller's registered
+// (tpmlp_set_side_stream) and a split that pays (side_by_side_sms), the two pairs of independent
+// GEMMs run side by side:
+//   st:   dH_i (x1 SMs)            | db1, dA_i = X^T dH_i (x2 SMs)
+//   side: dB_i (the rest), db2     | dX = sum_i dH_i A_i^T (the rest)
+// The side stream starts after everything before it on `st`, starts dX only after dH, and `st`
+// waits for it before returning; a phase whose split does not pay runs both its GEMMs on `st`.
+// Every tile keeps its accumulation order on a smaller grid, so dH, dB, dA and the column sums
+// have the same bits either way; dX may run on CTA pairs rather than split-K pairs in a
+// narrower share, which adds its fp32 partial sums in another order.  Otherwise: do_row_bwd
+// and column_bwd_with_db2.  dX_f32: dX is a rank's fp32 partial sum.
+tpmlp_status block_bwd(const void* X, const void* A_sh, const void* B_sh, const void* H_sh, const void* Y_sh,
+                       const void* dZ, void* dX, void* dA_sh, void* dB_sh, void* db1_sh, void* db2, void* dH_ws,
+                       int64_t M, int64_t h, int64_t ffn, int p, tpmlp_dtype dt, bool gf32, bool dX_f32,
+                       const DeviceInfo& dev, cudaStream_t st) {
+    int x1 = 0, x2 = 0;
+    const bool side = t_side.s != nullptr && t_side.device == dev.device && dt == TPMLP_BF16;
+    const GemmCall dy = dY_call(B_sh, dZ, H_sh, dH_ws, M, h, ffn, p, dt, TPMLP_ACT_GELU_ERF);
+    const GemmCall db = dB_call(Y_sh, dZ, dB_sh, M, h, ffn, p, gf32);
+    const GemmCall da = dA_call(X, dH_ws, dA_sh, M, h, ffn, p, gf32);
+    const GemmCall dx = dX_call(dH_ws, A_sh, dX, M, h, ffn, p, dX_f32 || dt == TPMLP_F32);
+    if (side) {
+        const SplitKey key{M, h, ffn, p, dev.device, get_gemm_mode(), get_group_m(), gf32 ? 1 : 0, dX_f32 ? 1 : 0};
+        backward_splits(dy, db, da, dx, key, dev, &x1, &x2);
+    }
+    if (x1 == 0 && x2 == 0) {
+        TP_TRY(do_row_bwd(Y_sh, B_sh, dZ, H_sh, dH_ws, dB_sh, nullptr, M, h, ffn, p, dt, gf32, TPMLP_ACT_GELU_ERF,
+                          dev, st));
+        return column_bwd_with_db2(X, A_sh, dH_ws, dX, dA_sh, db1_sh, dZ, db2, M, h, ffn, p, dt, gf32, dev, st,
+                                   dX_f32);
+    }
+    const int S = dev.sm_count;
+    const int64_t fs = ffn / p;
+    cudaStream_t ss = t_side.s;
+    TP_TRY(record_and_wait(t_side.fork, st, ss, "side stream fork"));
+    if (x1 > 0) {
+        TP_TRY(run_call(db, dt, dev, ss, S - x1));
+        if (db2) TP_TRY(launch_colsum(dZ, false, 1, M, h, db2, gf32, ss));
+        TP_TRY(run_call(dy, dt, dev, st, x1));
+    } else {
+        TP_TRY(run_call(dy, dt, dev, st));
+        if (db2) TP_TRY(launch_colsum(dZ, false, 1, M, h, db2, gf32, st));
+        TP_TRY(run_call(db, dt, dev, st));
+    }
+    if (x2 > 0) {
+        TP_TRY(record_and_wait(t_side.fork, st, ss, "side stream fork"));  // dH is complete
+        TP_TRY(run_call(dx, dt, dev, ss, S - x2));
+        if (db1_sh) TP_TRY(launch_colsum(dH_ws, false, p, M, fs, db1_sh, gf32, st));
+        TP_TRY(run_call(da, dt, dev, st, x2));
+    } else {
+        if (db1_sh) TP_TRY(launch_colsum(dH_ws, false, p, M, fs, db1_sh, gf32, st));
+        TP_TRY(run_call(da, dt, dev, st));
+        TP_TRY(run_call(dx, dt, dev, st));
+    }
+    return record_and_wait(t_side.join, ss, st, "side stream join");
 }
 
 // SwiGLU shape rules: ffn/p a multiple of 128 (gate/up blocks of 128 features), bf16 only.
@@ -511,12 +669,10 @@ tpmlp_status tpmlp_mlp_bwd(const void* X, const void* A_sh, const void* B_sh, co
     TP_TRY(get_device(&dev));
     if (M == 0) return TPMLP_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const bool gf32 = grad_dt == TPMLP_F32;
-    // row layer backward with GeLU' fused: dH_i = (dZ B_i^T) * GeLU'(H_i); dB_i; db2
-    TP_TRY(do_row_bwd(Y_sh, B_sh, dZ, H_sh, dH_ws, dB_sh, nullptr, M, h, ffn, p, dt, gf32, TPMLP_ACT_GELU_ERF,
-                      *dev, st));
-    // column layer backward from dH: db2, db1_i, dA_i, dX = sum_i dH_i A_i^T
-    return column_bwd_with_db2(X, A_sh, dH_ws, dX, dA_sh, db1_sh, dZ, db2, M, h, ffn, p, dt, gf32, *dev, st);
+    // row layer backward with GeLU' fused: dH_i = (dZ B_i^T) * GeLU'(H_i); dB_i; db2; then the
+    // column layer backward from dH: db1_i, dA_i, dX = sum_i dH_i A_i^T
+    return block_bwd(X, A_sh, B_sh, H_sh, Y_sh, dZ, dX, dA_sh, dB_sh, db1_sh, db2, dH_ws, M, h, ffn, p, dt,
+                     grad_dt == TPMLP_F32, false, *dev, st);
 }
 
 tpmlp_status tpmlp_mlp_fwd_partial(const void* X, const void* A_sh, const void* b1_sh, const void* B_sh, float* Z_part,
@@ -569,11 +725,8 @@ tpmlp_status tpmlp_mlp_bwd_partial(const void* X, const void* A_sh, const void* 
     TP_TRY(get_device(&dev));
     if (M == 0) return TPMLP_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const bool gf32 = grad_dt == TPMLP_F32;
-    TP_TRY(do_row_bwd(Y_sh, B_sh, dZ, H_sh, dH_ws, dB_sh, nullptr, M, h, ffn, p, dt, gf32, TPMLP_ACT_GELU_ERF,
-                      *dev, st));
-    return column_bwd_with_db2(X, A_sh, dH_ws, dX_part, dA_sh, db1_sh, dZ, db2, M, h, ffn, p, dt, gf32, *dev, st,
-                               /*dX_f32=*/true);
+    return block_bwd(X, A_sh, B_sh, H_sh, Y_sh, dZ, dX_part, dA_sh, dB_sh, db1_sh, db2, dH_ws, M, h, ffn, p, dt,
+                     grad_dt == TPMLP_F32, /*dX_f32=*/true, *dev, st);
 }
 
 tpmlp_status tpmlp_sum_finish(const float* S, const void* bias, void* out, int64_t rows, int64_t cols, tpmlp_dtype dt,
