@@ -151,53 +151,6 @@ GemmSpec spec_base() {
     return g;
 }
 
-// Column layer (validated arguments).  One launch over all p shards.
-tpmlp_status do_column(const void* X, const void* A_sh, const void* b1_sh, void* Y_sh, void* H_sh, int64_t M,
-                       int64_t h, int64_t ffn, int p, tpmlp_dtype dt, int act, const DeviceInfo& dev,
-                       cudaStream_t st) {
-    const int64_t fs = ffn / p;
-    Operand a{X, h, 0, 1, false};                     // X [M][h], K-major
-    Operand b{A_sh, fs, h * fs, p, true};             // A_i [h][fs]: [K][N], MN-major
-    GemmSpec g = spec_base();
-    g.M = M; g.N = fs; g.K = h; g.n_shards = p;
-    g.sum_shards = false; g.a_batched = false; g.b_batched = true;
-    g.epi = EPI_BIAS_ACT; g.act = act;
-    g.out = Y_sh; g.out_ld = fs; g.out_ss = M * fs;
-    g.out2 = H_sh; g.out2_ld = fs; g.out2_ss = M * fs;
-    g.bias = b1_sh; g.bias_ss = fs;
-    return run_gemm(a, b, g, dt, dev, st);
-}
-
-// Row layer with the shard sum in the K loop.
-tpmlp_status do_row(const void* Y_sh, const void* B_sh, const void* b2, void* Z, int64_t M, int64_t h, int64_t ffn,
-                    int p, tpmlp_dtype dt, const DeviceInfo& dev, cudaStream_t st) {
-    const int64_t fs = ffn / p;
-    Operand a{Y_sh, fs, M * fs, p, false};            // Y_i [M][fs], K-major
-    Operand b{B_sh, h, fs * h, p, true};              // B_i [fs][h]: [K][N], MN-major
-    GemmSpec g = spec_base();
-    g.M = M; g.N = h; g.K = fs; g.n_shards = p;
-    g.sum_shards = true;
-    g.epi = EPI_BIAS_ACT; g.act = TPMLP_ACT_NONE;
-    g.out = Z; g.out_ld = h; g.out_ss = 0;
-    g.bias = b2; g.bias_ss = 0;
-    return run_gemm(a, b, g, dt, dev, st);
-}
-
-// Row layer without the bias, its shard sum left in fp32: Z_part = sum_i Y_i B_i over the shards
-// given (a rank's partial of a block whose shards are spread over several GPUs).
-tpmlp_status do_row_partial(const void* Y_sh, const void* B_sh, float* Z_part, int64_t M, int64_t h, int64_t ffn,
-                            int p, tpmlp_dtype dt, const DeviceInfo& dev, cudaStream_t st) {
-    const int64_t fs = ffn / p;
-    Operand a{Y_sh, fs, M * fs, p, false};            // Y_i [M][fs], K-major
-    Operand b{B_sh, h, fs * h, p, true};              // B_i [fs][h]: [K][N], MN-major
-    GemmSpec g = spec_base();
-    g.M = M; g.N = h; g.K = fs; g.n_shards = p;
-    g.sum_shards = true;
-    g.epi = EPI_STORE; g.out_f32 = true;
-    g.out = Z_part; g.out_ld = h; g.out_ss = 0;
-    return run_gemm(a, b, g, dt, dev, st);
-}
-
 // One GEMM launch: its operands and everything else.
 struct GemmCall {
     Operand a, b;
@@ -207,6 +160,62 @@ tpmlp_status run_call(const GemmCall& c, tpmlp_dtype dt, const DeviceInfo& dev, 
     GemmSpec g = c.g;
     g.max_sms = max_sms;
     return run_gemm(c.a, c.b, g, dt, dev, st);
+}
+
+// Column layer: H_i = X A_i + b1_i, Y_i = act(H_i).  One launch over all p shards.
+GemmCall column_call(const void* X, const void* A_sh, const void* b1_sh, void* Y_sh, void* H_sh, int64_t M,
+                     int64_t h, int64_t ffn, int p, int act) {
+    const int64_t fs = ffn / p;
+    GemmCall c{{X, h, 0, 1, false},             // X [M][h], K-major
+               {A_sh, fs, h * fs, p, true},     // A_i [h][fs]: [K][N], MN-major
+               spec_base()};
+    c.g.M = M; c.g.N = fs; c.g.K = h; c.g.n_shards = p;
+    c.g.sum_shards = false; c.g.a_batched = false; c.g.b_batched = true;
+    c.g.epi = EPI_BIAS_ACT; c.g.act = act;
+    c.g.out = Y_sh; c.g.out_ld = fs; c.g.out_ss = M * fs;
+    c.g.out2 = H_sh; c.g.out2_ld = fs; c.g.out2_ss = M * fs;
+    c.g.bias = b1_sh; c.g.bias_ss = fs;
+    return c;
+}
+tpmlp_status do_column(const void* X, const void* A_sh, const void* b1_sh, void* Y_sh, void* H_sh, int64_t M,
+                       int64_t h, int64_t ffn, int p, tpmlp_dtype dt, int act, const DeviceInfo& dev,
+                       cudaStream_t st) {
+    return run_call(column_call(X, A_sh, b1_sh, Y_sh, H_sh, M, h, ffn, p, act), dt, dev, st);
+}
+
+// Row layer with the shard sum in the K loop: Z = sum_i Y_i B_i + b2.
+GemmCall row_call(const void* Y_sh, const void* B_sh, const void* b2, void* Z, int64_t M, int64_t h, int64_t ffn,
+                  int p) {
+    const int64_t fs = ffn / p;
+    GemmCall c{{Y_sh, fs, M * fs, p, false},    // Y_i [M][fs], K-major
+               {B_sh, h, fs * h, p, true},      // B_i [fs][h]: [K][N], MN-major
+               spec_base()};
+    c.g.M = M; c.g.N = h; c.g.K = fs; c.g.n_shards = p;
+    c.g.sum_shards = true;
+    c.g.epi = EPI_BIAS_ACT; c.g.act = TPMLP_ACT_NONE;
+    c.g.out = Z; c.g.out_ld = h; c.g.out_ss = 0;
+    c.g.bias = b2; c.g.bias_ss = 0;
+    return c;
+}
+tpmlp_status do_row(const void* Y_sh, const void* B_sh, const void* b2, void* Z, int64_t M, int64_t h, int64_t ffn,
+                    int p, tpmlp_dtype dt, const DeviceInfo& dev, cudaStream_t st) {
+    return run_call(row_call(Y_sh, B_sh, b2, Z, M, h, ffn, p), dt, dev, st);
+}
+
+// Row layer without the bias, its shard sum left in fp32: Z_part = sum_i Y_i B_i over the shards
+// given (a rank's partial of a block whose shards are spread over several GPUs).
+GemmCall row_partial_call(const void* Y_sh, const void* B_sh, float* Z_part, int64_t M, int64_t h, int64_t ffn,
+                          int p) {
+    GemmCall c = row_call(Y_sh, B_sh, nullptr, Z_part, M, h, ffn, p);
+    c.g.epi = EPI_STORE; c.g.act = 0; c.g.out_f32 = true;
+    return c;
+}
+
+// The block forward: the column GEMM, then the row GEMM.
+tpmlp_status block_fwd(const GemmCall& col, const GemmCall& row, tpmlp_dtype dt, const DeviceInfo& dev,
+                       cudaStream_t st) {
+    TP_TRY(run_call(col, dt, dev, st));
+    return run_call(row, dt, dev, st);
 }
 
 // dY_i = dZ B_i^T, times GeLU'(H_i) when act is GeLU (K = h)
@@ -379,11 +388,14 @@ constexpr double kEpilogueBlocks = 18.0;  // a short-K tile's epilogue (measured
 constexpr double kExchangeBlocks = 8.0;   // split-K partial sums through distributed shared memory (~2 us)
 constexpr double kLaunchBlocks = 10.0;    // the gap between two dependent launches (~2.5-3 us)
 
-double gemm_cost(const GemmCall& c, const DeviceInfo& dev, int sms) {
+// Cost of a GEMM on at most `sms` SMs (above), and in *used the SMs its grid occupies.
+double gemm_cost(const GemmCall& c, const DeviceInfo& dev, int sms, int* used = nullptr) {
     GemmSpec g = c.g;
     g.max_sms = sms;
     GemmPlan pl{};
+    if (used) *used = 0;
     if (!tc_gemm_plan(c.a, c.b, g, dev, &pl)) return 1e30;
+    if (used) *used = pl.sms;
     if (pl.tiles == 0) return 0.0;
     if (pl.slots <= 0) return 1e30;
     const int waves = (pl.tiles + pl.slots - 1) / pl.slots;
@@ -391,19 +403,30 @@ double gemm_cost(const GemmCall& c, const DeviceInfo& dev, int sms) {
     return waves * per_tile + kEpilogueBlocks + (pl.split_k ? kExchangeBlocks : 0.0);
 }
 
-// SMs for `a` when `a` and `b` should run side by side (`b` takes the rest; even counts, as CTA
-// pairs take two), or 0 when one after the other is about as fast.
+// SMs for `a` when `a` and `b` should run side by side, or 0 when one after the other is about
+// as fast.  Each candidate caps one GEMM's grid (even counts: CTA pairs take two) and gives the
+// other every SM the first does not occupy; among equally fast splits the one leaving fewest
+// SMs idle wins.
 int side_by_side_sms(const GemmCall& a, const GemmCall& b, const DeviceInfo& dev) {
     const int S = dev.sm_count;
     const double apart = gemm_cost(a, dev, S) + gemm_cost(b, dev, S) + kLaunchBlocks;
     double best = apart;
-    int best_x = 0;
-    for (int x = 2; x + 2 <= S; x += 2) {
-        const double c = std::max(gemm_cost(a, dev, x), gemm_cost(b, dev, S - x));
-        if (c < best) {
-            best = c;
-            best_x = x;
+    int best_x = 0, best_idle = S;
+    auto consider = [&](double cost, int a_sms, int idle) {
+        if (cost < best || (cost == best && best_x > 0 && idle < best_idle)) {
+            best = cost;
+            best_x = a_sms;
+            best_idle = idle;
         }
+    };
+    for (int x = 2; x + 2 <= S; x += 2) {
+        int ua = 0, ub = 0;
+        const double ca = gemm_cost(a, dev, x, &ua);  // a capped at x, b on the rest
+        const double cb = gemm_cost(b, dev, S - ua, &ub);
+        if (ua > 0 && ub > 0) consider(std::max(ca, cb), ua, S - ua - ub);
+        const double cb2 = gemm_cost(b, dev, x, &ub);  // b capped at x, a on the rest
+        const double ca2 = gemm_cost(a, dev, S - ub, &ua);
+        if (ua > 0 && ub > 0) consider(std::max(ca2, cb2), S - ub, S - ua - ub);
     }
     return best < 0.9 * apart ? best_x : 0;  // the fork and join cost a little too
 }
@@ -638,8 +661,8 @@ tpmlp_status tpmlp_mlp_fwd(const void* X, const void* A_sh, const void* b1_sh, c
     TP_TRY(get_device(&dev));
     if (M == 0) return TPMLP_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    TP_TRY(do_column(X, A_sh, b1_sh, Y_ws, H_sh, M, h, ffn, p, dt, TPMLP_ACT_GELU_ERF, *dev, st));
-    return do_row(Y_ws, B_sh, b2, Z, M, h, ffn, p, dt, *dev, st);
+    return block_fwd(column_call(X, A_sh, b1_sh, Y_ws, H_sh, M, h, ffn, p, TPMLP_ACT_GELU_ERF),
+                     row_call(Y_ws, B_sh, b2, Z, M, h, ffn, p), dt, *dev, st);
 }
 
 tpmlp_status tpmlp_mlp_bwd(const void* X, const void* A_sh, const void* B_sh, const void* H_sh, const void* Y_sh,
@@ -694,8 +717,8 @@ tpmlp_status tpmlp_mlp_fwd_partial(const void* X, const void* A_sh, const void* 
     TP_TRY(get_device(&dev));
     if (M == 0) return TPMLP_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    TP_TRY(do_column(X, A_sh, b1_sh, Y_ws, H_sh, M, h, ffn, p, dt, TPMLP_ACT_GELU_ERF, *dev, st));
-    return do_row_partial(Y_ws, B_sh, Z_part, M, h, ffn, p, dt, *dev, st);
+    return block_fwd(column_call(X, A_sh, b1_sh, Y_ws, H_sh, M, h, ffn, p, TPMLP_ACT_GELU_ERF),
+                     row_partial_call(Y_ws, B_sh, Z_part, M, h, ffn, p), dt, *dev, st);
 }
 
 tpmlp_status tpmlp_mlp_bwd_partial(const void* X, const void* A_sh, const void* B_sh, const void* H_sh,
