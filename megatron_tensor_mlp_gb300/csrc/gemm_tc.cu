@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <climits>
 #include <mutex>
 
 #include "gemm_tc.cuh"
@@ -364,8 +365,11 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
     k.m_blocks = m_pairs;
     k.num_tiles = pair_tiles;
     {
+        // K reversal pays only across many waves of tiles (L2 reuse from one wave to the next);
+        // a GEMM of at most two waves on the full grid walks K forwards on every grid, so its bits
+        // do not depend on the grid.
         const int full = pair_capacity<A_MN, B_MN, EPI, false>(dev);  // the uncapped grid's clusters
-        k.rev_period = full > 0 ? full : 1;
+        k.rev_period = (full > 0 && pair_tiles > 2 * full) ? full : INT_MAX;
     }
     if constexpr (kSplitOk) {
         if (split) return launch_splitk<A_MN, B_MN, EPI>(ma, mb, k, st);

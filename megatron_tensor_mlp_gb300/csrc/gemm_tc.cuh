@@ -70,7 +70,7 @@ struct KArgs {
     int st32;                  // out, out2 and aux rows are 32-byte aligned: 32-byte global accesses
     int accumulate;            // EPI_STORE, fp32 out: out += acc (a later K chunk of a split contraction)
     int tile_begin;            // pair and split-K kernels: this launch covers tiles [tile_begin, num_tiles)
-    int rev_period;            // pair kernel: tile t walks K backwards when (t / rev_period) is odd
+    int rev_period;            // pair kernel: tile t walks K backwards when (t / rev_period) is odd (INT_MAX: never)
     void* out; long long out_ld, out_ss;
     void* out2; long long out2_ld, out2_ss;
     const void* bias; long long bias_ss;

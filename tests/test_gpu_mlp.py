@@ -17,10 +17,11 @@ def env():
     return harness, synth, tpmlp
 
 
-@pytest.fixture(params=[1, 3, 4, 5], ids=["single-cta", "pair-direct", "pair-staged", "split-k"])
+@pytest.fixture(params=[0, 1, 3, 4, 5], ids=["auto", "single-cta", "pair-direct", "pair-staged", "split-k"])
 def gemm_mode(request, env):
-    """Force 128x256 single-CTA tiles, 256x256 CTA-pair tiles (either epilogue), or split-K CTA
-    pairs for every shard-summing GEMM (row, dX) that fits one wave of them."""
+    """The automatic tiling, or forced 128x256 single-CTA tiles, 256x256 CTA-pair tiles (either
+    epilogue), or split-K CTA pairs for every shard-summing GEMM (row, dX) that fits one wave of
+    them."""
     T = env[2]
     T.tpmlp_set_gemm_mode(request.param)
     yield request.param
