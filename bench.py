@@ -49,7 +49,9 @@ def parse():
     ap.add_argument("--no-next-rows", action="store_true", help="skip the SwiGLU / attention-projection timings")
     ap.add_argument("--next-rows-only", action="store_true",
                     help="time only the SwiGLU and attention-projection steps (for profiling their launches)")
-    ap.add_argument("--e2e-steps", type=int, default=60)
+    ap.add_argument("--e2e-steps", type=int, default=None,
+                    help="timed steps of the end-to-end leg (default: as many as the device-timed region, at "
+                         "most 60; 0 skips the leg)")
     ap.add_argument("--bwd", action="store_true",
                     help="run forward + backward on a forward-only workload (for profiling its backward GEMMs)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
@@ -693,8 +695,8 @@ def run_gpu(args):
     # step i-1's results copied out on a copy stream while step i computes (double-buffered
     # device inputs and outputs); every step's copies still happen inside the timed region.
     e2e = None
-    if args.e2e_steps > 0:
-        n_e2e = args.e2e_steps
+    n_e2e = args.e2e_steps if args.e2e_steps is not None else min(60, args.steps)
+    if n_e2e > 0:
         X_host = [buf.X.cpu().pin_memory() for _ in range(2)]
         dZ_host = [buf.dZ.cpu().pin_memory() for _ in range(2)] if wl.backward else None
         Z_host = [torch.empty(buf.Z.shape, dtype=buf.Z.dtype).pin_memory() for _ in range(2)]
@@ -762,14 +764,18 @@ def run_gpu(args):
                 break
         barrier()
         a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sampler.mark_start("e2e")
         a.record(stream)
         copy_stream.wait_event(a)  # no copy of the timed steps starts before the timed region
         run_pipeline(n_e2e)
         z.record(stream)
         torch.cuda.synchronize()
+        sampler.mark_end("e2e")
         e2e_ms = dist_max(a.elapsed_time(z) / n_e2e)
         e2e = {"value": round(job_throughput(flops_step, ws, e2e_ms) / 1e12, 2), "unit": "TFLOP/s",
-               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_ms, 4), "steps": n_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "clocks": {k: v for k, v in sampler.summary("e2e").items() if k in ("sm_mhz", "reasons", "samples",
+                                                                                      "window", "seconds")},
                "note": "every step copies X, dZ in from pinned host memory and reads Z, dX back, on a copy "
                        "stream overlapped with the neighbouring steps' compute; weights stay resident"}
     T.tpmlp_device_status()
