@@ -1,9 +1,9 @@
 """The fused backward with a side stream of the caller's (GPU).
 
 With a stream and two events registered (tpmlp_set_side_stream), tpmlp_mlp_bwd at the s=512 b=4
-h=1024 ffn=4096 p=4 workload (every GEMM one or two waves of tiles) runs its two pairs of
-independent GEMMs side by side, dH beside dB and dA beside dX, each on a share of the SMs; with
-nothing registered everything runs in line on one stream.  Each tile keeps its accumulation order
+h=1024 ffn=4096 p=4 workload (every GEMM one or two waves of tiles; also a ragged shape near it)
+runs its two pairs of independent GEMMs side by side, dH beside dB and dA beside dX, each on a
+share of the SMs; with nothing registered everything runs in line on one stream.  Each tile keeps its accumulation order
 on the smaller grids, so dH, dB, dA and the column sums db1, db2 have the same bits both ways.
 dX runs on CTA pairs over its whole K loop in its share, rather than on split-K pairs that add
 two fp32 halves, so a few of its bf16 values round the other way: it is checked against the
@@ -15,14 +15,15 @@ import pytest
 pytestmark = pytest.mark.gpu
 
 
-def test_side_stream_sums_are_bit_identical():
+@pytest.mark.parametrize("shape", [(512, 4, 1024, 4096, 4), (250, 4, 1032, 4128, 4)], ids=["s512-h1024", "ragged"])
+def test_side_stream_sums_are_bit_identical(shape):
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from megatron_tensor_mlp_gb300 import harness, synth
     from megatron_tensor_mlp_gb300 import tpmlp as T
 
-    wl = synth.custom(512, 4, 1024, 4096, 4, dtype="bf16", sigma_w=0.02, sigma_bias=0.01, seed=66)
+    wl = synth.custom(*shape, dtype="bf16", sigma_w=0.02, sigma_bias=0.01, seed=66)
     buf = harness.MLPBuffers(wl, backward=True)
     buf.fwd()
     buf.bwd()
