@@ -1,5 +1,7 @@
 """The five workloads at full size, in the launch configuration the benchmark
-times, against the oracle on sampled outputs computed one by one (GPU)."""
+times (a side stream registered for the fused backward, as the benchmark does; the
+s=512 workload with its backward too, which the benchmark also times), against the
+oracle on sampled outputs computed one by one (GPU)."""
 import numpy as np
 import pytest
 
@@ -35,13 +37,20 @@ def test_workload_sampled(env, orc, cfg):
     import torch
     harness, synth, T = env
     wl = synth.WORKLOADS[cfg]
-    buf = harness.MLPBuffers(wl)
+    backward = wl.backward or cfg == 2
+    buf = harness.MLPBuffers(wl, backward=backward)
     for t in (buf.Z, buf.Y, buf.H):
         if t is not None:
             t.fill_(float("nan"))
-    buf.fwd()
-    if wl.backward:
-        buf.bwd()
+    side = (torch.cuda.Stream(), torch.cuda.Event(), torch.cuda.Event())
+    T.tpmlp_set_side_stream(*side)
+    try:
+        buf.fwd()
+        if backward:
+            buf.bwd()
+        torch.cuda.synchronize()
+    finally:
+        T.tpmlp_set_side_stream(None, None, None)
     T.tpmlp_device_status()
     M, h, f, p = wl.M, wl.h, wl.ffn, wl.p
     rows = _rows(M, 10, cfg)
@@ -59,7 +68,7 @@ def test_workload_sampled(env, orc, cfg):
         U.assert_close(harness.to_host(buf.H_full()[ridx]), Hr, "bf16", f"H rows (cfg {cfg})")
     # a property at full size: every output finite
     assert bool(torch.isfinite(buf.Z).all())
-    if not wl.backward:
+    if not backward:
         return
     dZ = widen(buf.host["dZ"])
     cols = _cols(f, p, 6, cfg)
