@@ -488,7 +488,8 @@ def time_next_rows(stream, steps, peaks, explicit_warmup=None):
     """Forward+backward timings of the widened rows at the fwd+bwd workload's sizes
     (s=2048, b=4, h=5120, p=4): the SwiGLU block (ffn=20480 per branch) and the attention
     tensor-parallel projections (QKV column projection over the per-head interleave, 40 heads,
-    and the output row projection).  Inputs are seeded synthetic bf16."""
+    and the output row projection); then the bandwidth of the two layout kernels at the pages'
+    sizing.  Inputs are seeded synthetic bf16."""
     import torch
     from megatron_tensor_mlp_gb300 import synth
     from megatron_tensor_mlp_gb300 import tpmlp as T
@@ -556,6 +557,31 @@ def time_next_rows(stream, steps, peaks, explicit_warmup=None):
     out["attention_projections_fwd_bwd"] = {"shape": f"s{s} b{b} h{h} heads{heads} p{p}", "ms": round(ms, 4),
                                             "TFLOP/s": round(tf, 1),
                                             "pct_of_nominal_2250": round(100 * tf / NOMINAL_BF16_TFLOPS, 2)}
+    del Wq, Wq_sh, Wo, QKV, ctx, dQKV, dWq, dWo, dctx, X, dZ, B, Z, dX
+    torch.cuda.empty_cache()
+
+    # The layout kernels (set-up, bit-exact copies) at the pages' sizing (h=8192, ffn=32768, p=8,
+    # 64 heads): HBM bound, so the measure is the bytes they move (the tensor read once and
+    # written once) against the measured copy bandwidth.
+    hp, fp, pp, hd = 8192, 32768, 8, 64
+    hbm = peaks.get("hbm_gbs", 6800.0)
+
+    def layout_row(name, shape, fn, nbytes):
+        ms = timed(fn, n)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"shape": shape, "ms": round(ms, 4), "GB/s": round(gbs, 1),
+                     "frac_of_measured_hbm": round(gbs / hbm, 4)}
+
+    Wa = gen(16, (hp, fp), 0.02)
+    Wa_sh = torch.empty((pp, hp, fp // pp), dtype=bf, device="cuda")
+    layout_row("shard_columns", f"A [{hp}, {fp}] bf16 -> [{pp}][{hp}][{fp // pp}]",
+               lambda: T.tpmlp_shard_columns(Wa, Wa_sh, hp, fp, pp, stream=stream), 2 * Wa.numel() * 2)
+    del Wa, Wa_sh
+    torch.cuda.empty_cache()
+    Wq = gen(17, (hp, 3 * hp), 0.02)
+    Wq_out = torch.empty_like(Wq)
+    layout_row("qkv_interleave", f"W_qkv [{hp}, {3 * hp}] bf16, {hd} heads, p={pp}",
+               lambda: T.tpmlp_qkv_interleave(Wq, Wq_out, hp, hp, hd, pp, stream=stream), 2 * Wq.numel() * 2)
     return out
 
 

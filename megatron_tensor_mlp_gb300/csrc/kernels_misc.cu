@@ -4,6 +4,7 @@
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cstdint>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -241,41 +242,49 @@ __global__ void __launch_bounds__(CS_WARPS * 32)
 
 // ------------------------------------------------------------------ layouts
 // Column shard: dst[i][r][c] = src[r][i*cs + c] in 16-byte units (rows of cs*esize bytes).
+// Each CTA takes whole rows of the unsharded layout in turn: it reads a row front to back and
+// writes its p pieces, each a contiguous run of the sharded layout, with no division per unit;
+// four independent units per thread and step keep enough bytes in flight.
 __global__ void shard_columns_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long rows,
-                                     long long units_per_row /*cols*esize/16*/, long long units_per_shard_row,
-                                     int p, int inverse) {
-    const long long total = rows * units_per_row;
-    for (long long u = blockIdx.x * (long long)blockDim.x + threadIdx.x; u < total;
-         u += (long long)gridDim.x * blockDim.x) {
-        // u enumerates the sharded layout: (i, r, cu)
-        const long long per_shard = rows * units_per_shard_row;
-        const long long i = u / per_shard;
-        const long long rem = u - i * per_shard;
-        const long long r = rem / units_per_shard_row;
-        const long long cu = rem - r * units_per_shard_row;
-        const long long unsharded = r * units_per_row + i * units_per_shard_row + cu;
-        if (!inverse) dst[u] = src[unsharded];
-        else dst[unsharded] = src[u];
+                                     int units_per_row /*cols*esize/16*/, int units_per_shard_row, int p,
+                                     int inverse) {
+    for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
+        const long long row_base = r * units_per_row;
+        for (int i = 0; i < p; ++i) {
+            const long long a = row_base + static_cast<long long>(i) * units_per_shard_row;  // unsharded
+            const long long b = (static_cast<long long>(i) * rows + r) * units_per_shard_row;  // sharded
+            const uint4* from = inverse ? src + b : src + a;
+            uint4* to = inverse ? dst + a : dst + b;
+            int c = static_cast<int>(threadIdx.x);
+            for (; c + 3 * static_cast<int>(blockDim.x) < units_per_shard_row; c += 4 * static_cast<int>(blockDim.x)) {
+                const uint4 v0 = from[c], v1 = from[c + blockDim.x], v2 = from[c + 2 * blockDim.x],
+                            v3 = from[c + 3 * blockDim.x];
+                to[c] = v0;
+                to[c + blockDim.x] = v1;
+                to[c + 2 * blockDim.x] = v2;
+                to[c + 3 * blockDim.x] = v3;
+            }
+            for (; c < units_per_shard_row; c += blockDim.x) to[c] = from[c];
+        }
     }
-    (void)p;
 }
 
-__device__ __forceinline__ long long qkv_src_col_dev(long long dst_col, long long h, long long d) {
-    const long long blk = dst_col / d, e = dst_col - blk * d;
-    const long long g = blk / 3, t = blk - g * 3;
-    return t * h + g * d + e;
-}
-
+// QKV interleave in units of T (16 bytes when a head's width allows): each CTA takes whole
+// rows in turn; unit c of a row's head-major output is unit qkv_src_col(c) of the packed
+// [Q | K | V] input (or the reverse), with 32-bit index arithmetic.
 template <typename T>
-__global__ void qkv_kernel(const T* __restrict__ src, T* __restrict__ dst, long long rows, long long cols_units,
-                           long long h_units, long long d_units, int inverse) {
-    const long long total = rows * cols_units;
-    for (long long u = blockIdx.x * (long long)blockDim.x + threadIdx.x; u < total;
-         u += (long long)gridDim.x * blockDim.x) {
-        const long long r = u / cols_units, c = u - r * cols_units;
-        const long long sc = qkv_src_col_dev(c, h_units, d_units);
-        if (!inverse) dst[u] = src[r * cols_units + sc];
-        else dst[r * cols_units + sc] = src[u];
+__global__ void qkv_kernel(const T* __restrict__ src, T* __restrict__ dst, long long rows, int cols_units,
+                           int h_units, int d_units, int inverse) {
+    for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
+        const T* s = src + r * cols_units;
+        T* d = dst + r * cols_units;
+        for (int c = static_cast<int>(threadIdx.x); c < cols_units; c += static_cast<int>(blockDim.x)) {
+            const int blk = c / d_units, e = c - blk * d_units;
+            const int g = blk / 3, t = blk - g * 3;
+            const int sc = t * h_units + g * d_units + e;
+            if (!inverse) d[c] = s[sc];
+            else d[sc] = s[c];
+        }
     }
 }
 
@@ -437,9 +446,15 @@ tpmlp_status launch_colsum_any_sm(const void* in, int64_t shards, int64_t M, int
 tpmlp_status launch_shard_columns(const void* src, void* dst, int64_t rows, int64_t cols, int p, int esize,
                                   bool inverse, cudaStream_t st) {
     const long long upr = cols * esize / 16, upsr = upr / p;
-    const long long total = rows * upr;
-    shard_columns_kernel<<<grid_for(total, 256), 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
-                                                               rows, upr, upsr, p, inverse ? 1 : 0);
+    if (upr > INT32_MAX) {
+        set_error("column shard: a row of more than 2^31 16-byte units");
+        return TPMLP_ERR_SHAPE;
+    }
+    // one row per CTA at a time; enough CTAs for every SM several times over
+    const long long grid = rows < 152LL * 16 ? rows : 152LL * 16;
+    shard_columns_kernel<<<static_cast<unsigned>(grid > 0 ? grid : 1), 256, 0, st>>>(
+        static_cast<const uint4*>(src), static_cast<uint4*>(dst), rows, static_cast<int>(upr), static_cast<int>(upsr), p,
+        inverse ? 1 : 0);
     return check_launch("column shard");
 }
 
@@ -447,17 +462,24 @@ tpmlp_status launch_qkv_interleave(const void* src, void* dst, int64_t rows, int
                                    bool inverse, cudaStream_t st) {
     const long long d = h / n_heads;
     const long long cols = 3 * h;
+    if (cols > INT32_MAX) {
+        set_error("QKV interleave: rows of more than 2^31 elements");
+        return TPMLP_ERR_SHAPE;
+    }
+    const unsigned grid = static_cast<unsigned>(rows < 152LL * 16 ? (rows > 0 ? rows : 1) : 152LL * 16);  // rows per CTA in turn
     if ((d * esize) % 16 == 0) {
         const long long k = 16 / esize;  // elements per unit
-        const long long total = rows * (cols / k);
-        qkv_kernel<uint4><<<grid_for(total, 256), 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
-                                                               rows, cols / k, h / k, d / k, inverse ? 1 : 0);
+        qkv_kernel<uint4><<<grid, 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), rows,
+                                               static_cast<int>(cols / k), static_cast<int>(h / k),
+                                               static_cast<int>(d / k), inverse ? 1 : 0);
     } else if (esize == 2) {
-        qkv_kernel<uint16_t><<<grid_for(rows * cols, 256), 256, 0, st>>>(
-            static_cast<const uint16_t*>(src), static_cast<uint16_t*>(dst), rows, cols, h, d, inverse ? 1 : 0);
+        qkv_kernel<uint16_t><<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(src), static_cast<uint16_t*>(dst), rows,
+                                                  static_cast<int>(cols), static_cast<int>(h), static_cast<int>(d),
+                                                  inverse ? 1 : 0);
     } else {
-        qkv_kernel<uint32_t><<<grid_for(rows * cols, 256), 256, 0, st>>>(
-            static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst), rows, cols, h, d, inverse ? 1 : 0);
+        qkv_kernel<uint32_t><<<grid, 256, 0, st>>>(static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst), rows,
+                                                  static_cast<int>(cols), static_cast<int>(h), static_cast<int>(d),
+                                                  inverse ? 1 : 0);
     }
     return check_launch("QKV interleave");
 }
