@@ -258,6 +258,12 @@ class ClockSampler:
                 "power_w_median": med([r[3] for r in inside if r[3] is not None])}
 
 
+def e2e_step_count(args):
+    """Timed steps of the end-to-end leg: --e2e-steps when given (0 skips the leg), else as many as
+    the device-timed region, at most 60."""
+    return args.e2e_steps if args.e2e_steps is not None else min(60, args.steps)
+
+
 def peak_regime(clocks, seconds, peaks):
     """The measured bf16 peak that matches how a timed region ran.  The burst figure (cuBLAS
     best-of-10) applies to a region shorter than about a second or one whose median SM clock is
@@ -722,7 +728,7 @@ def run_gpu(args):
     # step i-1's results copied out on a copy stream while step i computes (double-buffered
     # device inputs and outputs); every step's copies still happen inside the timed region.
     e2e = None
-    n_e2e = args.e2e_steps if args.e2e_steps is not None else min(60, args.steps)
+    n_e2e = e2e_step_count(args)
     if n_e2e > 0:
         X_host = [buf.X.cpu().pin_memory() for _ in range(2)]
         dZ_host = [buf.dZ.cpu().pin_memory() for _ in range(2)] if wl.backward else None

@@ -79,3 +79,13 @@ def test_clock_summary_uses_samples_inside_the_window():
     assert c["sm_mhz"] == 2005.0 and c["reasons"] == []
     t = s.summary("tiny")
     assert t["window"] == "whole run" and t["samples"] == 10 and t["reasons"] == ["sw_power_cap"]
+
+
+def test_e2e_leg_times_as_many_steps_as_the_device_region(monkeypatch):
+    """The end-to-end leg runs under the device-timed region's conditions: as many steps (at most
+    60) unless --e2e-steps says otherwise, 0 skipping it."""
+    for argv, want in ((["bench.py"], 60), (["bench.py", "--steps", "20", "--warmup", "5"], 20),
+                       (["bench.py", "--steps", "20", "--e2e-steps", "7"], 7),
+                       (["bench.py", "--e2e-steps", "0"], 0)):
+        monkeypatch.setattr(sys, "argv", argv)
+        assert bench.e2e_step_count(bench.parse()) == want
