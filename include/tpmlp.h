@@ -128,8 +128,8 @@ tpmlp_status tpmlp_mlp_fwd(const void* X, const void* A_sh, const void* b1_sh, c
  *          db2 [h] (or NULL), all grad_dt (fp32 recommended for bf16 inputs).
  * Workspace: dH_ws [p][M][ffn/p] dt, holds dH on return.
  * Requires ffn % p == 0 and h % p == 0; grad_dt must be TPMLP_F32 when dt is TPMLP_F32.
- * Launch order on `stream`: dH, dB, db2, db1, dA, dX (db1 and db2 beside dX on a side stream
- * of the caller's where one is registered: tpmlp_set_side_stream).
+ * Launch order on `stream`: dH, dB, db2, db1, dA, dX (where a side stream of the caller's is
+ * registered, the GEMMs or the column sums may run beside one another: tpmlp_set_side_stream).
  */
 tpmlp_status tpmlp_mlp_bwd(const void* X, const void* A_sh, const void* B_sh, const void* H_sh, const void* Y_sh,
                            const void* dZ, void* dX, void* dA_sh, void* dB_sh, void* db1_sh, void* db2,
@@ -339,12 +339,19 @@ tpmlp_status tpmlp_debug_wait_timeout(uint32_t timeout_us, void* stream);
  *     the other (GEMMs of one or two waves of tiles, e.g. s=512 b=4 h=1024 ffn=4096 p=4):
  *     dH_i on `stream` beside dB_i (then db2) on the side stream, then dA_i (after db1) on
  *     `stream` beside dX on the side stream;
- *   - otherwise the bias-gradient column sums (db1 = 1^T dH, db2 = 1^T dZ), which need no
- *     tensor cores, run on the side stream beside the first of the dA and dX GEMMs whose grid
- *     leaves enough SMs idle for all of them; where no GEMM does, they run in line.
- * The side stream waits for an event recorded on `stream` before its first kernel (and, for
- * dX, after dH), and `stream` waits for an event recorded on the side stream after its last,
- * so everything is complete, in order, when the work enqueued on `stream` is.  With nothing
+ *   - otherwise, in those two, where dB_i or dA_i runs its last partial wave as a second
+ *     launch (split-K CTA pairs, four CTAs per tile) that leaves at least half the SMs idle
+ *     (e.g. s=2048 b=4 h=5120 ffn=20480 p=4: 4 tiles on 16 SMs), the bias-gradient column
+ *     sums (db1 = 1^T dH, db2 = 1^T dZ), which need no tensor cores, run on the side stream
+ *     beside that last wave: db2 beside dB_i's and db1 beside dA_i's, or both beside the one
+ *     there is; `stream` waits for them before its next GEMM;
+ *   - otherwise (and in tpmlp_swiglu_mlp_bwd) the column sums run on the side stream beside
+ *     the first of the dA and dX GEMMs whose grid leaves enough SMs idle for all of them;
+ *     where no GEMM does, they run in line.
+ * The side stream waits for an event recorded on `stream` before its first kernel (for dX,
+ * after dH; for sums beside a last wave, between that GEMM's two launches), and `stream`
+ * waits for an event recorded on the side stream after its last, so everything is
+ * complete, in order, when the work enqueued on `stream` is.  With nothing
  * registered everything runs in line on `stream`.  dH, dB, dA, db1 and db2 have the same bits
  * either way; dX, where it runs side by side, may differ in the last place of a few values
  * (its fp32 partial sums added in another order).

@@ -328,14 +328,14 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
     const bool narrow = kNarrowOk && !use_pair && 2 * k.num_tiles <= dev.sm_count && g.N > 128;
     if (plan_out) {
         if (split) {
-            *plan_out = GemmPlan{4 * pair_tiles, pair_tiles, pair_tiles, (k.k_iters + 1) / 2, 1};
+            *plan_out = GemmPlan{4 * pair_tiles, pair_tiles, pair_tiles, (k.k_iters + 1) / 2, 1, 0};
         } else if (use_pair) {
             const int clusters = pair_tiles < cap ? pair_tiles : cap;
-            *plan_out = GemmPlan{2 * clusters, pair_tiles, clusters, k.k_iters, 0};
+            *plan_out = GemmPlan{2 * clusters, pair_tiles, clusters, k.k_iters, 0, tail};
         } else {
             const int tiles = narrow ? k.m_blocks * static_cast<int>((g.N + 127) / 128) * k.batch : k.num_tiles;
             const int grid = tiles < sm_cap ? tiles : sm_cap;
-            *plan_out = GemmPlan{grid, tiles, grid, k.k_iters, 0};
+            *plan_out = GemmPlan{grid, tiles, grid, k.k_iters, 0, 0};
         }
         return TPMLP_OK;
     }
@@ -378,6 +378,13 @@ tpmlp_status launch_variant(const Operand& a, const Operand& b, const GemmSpec& 
             kf.num_tiles = pair_tiles - tail;
             const tpmlp_status r = launch_pair<A_MN, B_MN, EPI, false>(ma, mb, ma, ma, kf, cap, st);
             if (r != TPMLP_OK) return r;
+            if (g.tail_event != nullptr) {
+                const cudaError_t e = cudaEventRecord(g.tail_event, st);
+                if (e != cudaSuccess) {
+                    set_error("event between a GEMM's full waves and its last wave: %s", cudaGetErrorString(e));
+                    return TPMLP_ERR_CUDA;
+                }
+            }
             k.tile_begin = pair_tiles - tail;
             return launch_splitk<A_MN, B_MN, EPI>(ma, mb, k, st);
         }
@@ -451,7 +458,7 @@ tpmlp_status launch_one(const Operand& a, const Operand& b, const GemmSpec& g, c
                      : 0;
     }
     if (k.num_tiles == 0) {
-        if (plan_out) *plan_out = GemmPlan{0, 0, 0, 0, 0};
+        if (plan_out) *plan_out = GemmPlan{0, 0, 0, 0, 0, 0};
         return TPMLP_OK;
     }
 

@@ -44,17 +44,22 @@ struct GemmSpec {
     const void* bias; int64_t bias_ss;            // [shard][N] of the input dtype, may be null
     const void* aux; int64_t aux_ld, aux_ss;      // EPI_DGELU: H
     int max_sms;         // > 0: the launch occupies at most this many SMs (a GEMM run beside another)
+    cudaEvent_t tail_event;  // non-null: recorded on the stream between the full waves and the split-K
+                             // last wave, when the GEMM runs one (GemmPlan::tail > 0)
 };
 
 // How a tcgen05 GEMM would run (tc_gemm_plan): the SMs its grid occupies, its work tiles, how
 // many of them are in flight at once, the K blocks (of 64) each CTA pair or CTA accumulates
-// per tile, and whether two CTA pairs split each tile's K loop.
+// per tile, whether two CTA pairs split each tile's K loop, and how many tiles of a last
+// partial wave run after the full waves as a second launch on split-K CTA pairs (four CTAs
+// per tile).
 struct GemmPlan {
     int sms;
     int tiles;
     int slots;
     int k_blocks;
     int split_k;
+    int tail;
 };
 
 struct DeviceInfo {

@@ -476,6 +476,65 @@ tpmlp_status record_and_wait(cudaEvent_t ev, cudaStream_t from, cudaStream_t to,
     return TPMLP_OK;
 }
 
+// The block backward's column sums beside the last waves of its weight-gradient GEMMs.  A GEMM
+// of several waves whose last wave is at most half full runs that wave as a second, short
+// launch on four CTAs per tile (split-K CTA pairs), which leaves most SMs idle while it runs
+// (at s=2048 b=4 h=5120 ffn=20480 p=4: dB_i and dA_i, 4 tiles on 16 of 152 SMs for ~25 us).
+// When dB_i's or dA_i's last wave leaves at least half the SMs idle, the side stream waits for
+// an event recorded between that GEMM's two launches (GemmSpec::tail_event) and sums there --
+// db2 beside dB_i's last wave, db1 beside dA_i's (both beside the one there is) -- and `st`
+// waits for the sums before its next GEMM, whose persistent grid then finds every SM free: the
+// sums cost the time by which they outlast the last wave, instead of their whole time in line.
+// The same column-sum kernel runs either way, so the bits do not change.  *done = false when
+// neither GEMM has such a last wave (nothing launched: the caller runs the backward in line).
+struct SumsBesideTails {
+    const void* dZ; void* db2; const void* dH; void* db1; int64_t M, h, fs, p; bool f32;
+};
+tpmlp_status sums_beside_tails(const GemmCall& dy, const GemmCall& db, const GemmCall& da, const GemmCall& dx,
+                               const SumsBesideTails& w, tpmlp_dtype dt, const DeviceInfo& dev, cudaStream_t st,
+                               bool* done) {
+    *done = false;
+    auto roomy_tail = [&](const GemmCall& c) {
+        GemmPlan pl{};
+        return tc_gemm_plan(c.a, c.b, c.g, dev, &pl) && pl.tail > 0 && 2 * (4 * pl.tail) <= dev.sm_count;
+    };
+    const bool at_db = roomy_tail(db), at_da = roomy_tail(da);
+    if (!at_db && !at_da) return TPMLP_OK;
+    *done = true;
+    cudaStream_t ss = t_side.s;
+    auto db2_sum = [&](cudaStream_t on) { return launch_colsum(w.dZ, false, 1, w.M, w.h, w.db2, w.f32, on); };
+    auto db1_sum = [&](cudaStream_t on) { return launch_colsum(w.dH, false, w.p, w.M, w.fs, w.db1, w.f32, on); };
+    // GEMM c on st with the sums marked `mine` beside its last wave.  The fork event is recorded
+    // once before the GEMM and again between its two launches; should the launch run no separate
+    // last wave after all, the sums still start after everything before the GEMM (correct, only
+    // not beside the last wave).
+    auto gemm_with_sums = [&](const GemmCall& c, bool mine2, bool mine1) -> tpmlp_status {
+        const bool fork = (mine2 && w.db2) || (mine1 && w.db1);
+        if (!fork) return run_call(c, dt, dev, st);
+        cudaError_t e = cudaEventRecord(t_side.fork, st);
+        if (e != cudaSuccess) {
+            set_error("side stream fork: %s", cudaGetErrorString(e));
+            return TPMLP_ERR_CUDA;
+        }
+        GemmCall cc = c;
+        cc.g.tail_event = t_side.fork;
+        TP_TRY(run_call(cc, dt, dev, st));
+        e = cudaStreamWaitEvent(ss, t_side.fork, 0);
+        if (e != cudaSuccess) {
+            set_error("side stream fork: %s", cudaGetErrorString(e));
+            return TPMLP_ERR_CUDA;
+        }
+        if (mine2 && w.db2) TP_TRY(db2_sum(ss));
+        if (mine1 && w.db1) TP_TRY(db1_sum(ss));
+        return record_and_wait(t_side.join, ss, st, "side stream join");
+    };
+    // every sum is assigned to exactly one of the two GEMMs
+    TP_TRY(run_call(dy, dt, dev, st));
+    TP_TRY(gemm_with_sums(db, at_db, at_db && !at_da));
+    TP_TRY(gemm_with_sums(da, !at_db, at_da));
+    return run_call(dx, dt, dev, st);
+}
+
 // The block backward (GeLU' fused) from dZ.  With a side stream of the caller's registered
 // (tpmlp_set_side_stream) and a split that pays (side_by_side_sms), the two pairs of independent
 // GEMMs run side by side:
@@ -502,6 +561,13 @@ tpmlp_status block_bwd(const void* X, const void* A_sh, const void* B_sh, const 
         backward_splits(dy, db, da, dx, key, dev, &x1, &x2);
     }
     if (x1 == 0 && x2 == 0) {
+        if (side && (db1_sh || db2)) {
+            const int64_t fs = ffn / p;
+            const SumsBesideTails w{dZ, db2, dH_ws, db1_sh, M, h, fs, p, gf32};
+            bool done = false;
+            TP_TRY(sums_beside_tails(dy, db, da, dx, w, dt, dev, st, &done));
+            if (done) return TPMLP_OK;
+        }
         TP_TRY(do_row_bwd(Y_sh, B_sh, dZ, H_sh, dH_ws, dB_sh, nullptr, M, h, ffn, p, dt, gf32, TPMLP_ACT_GELU_ERF,
                           dev, st));
         return column_bwd_with_db2(X, A_sh, dH_ws, dX, dA_sh, db1_sh, dZ, db2, M, h, ffn, p, dt, gf32, dev, st,

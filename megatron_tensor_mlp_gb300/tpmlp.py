@@ -241,7 +241,8 @@ GEMM_AUTO, GEMM_SINGLE, GEMM_PAIR, GEMM_PAIR_DIRECT, GEMM_PAIR_STAGED = 0, 1, 2,
 def tpmlp_set_side_stream(side_stream, fork_event, join_event, check=True):
     """Register (or, with three Nones, clear) a side stream and two events of the caller's for the
     fused backwards: independent GEMMs side by side at small shapes, else the column sums beside a
-    GEMM that leaves SMs idle.  Torch objects or raw handles; the caller keeps them alive."""
+    weight-gradient GEMM's short last wave or a GEMM that leaves SMs idle.  Torch objects or raw
+    handles; the caller keeps them alive."""
     def handle(x):
         if x is None or isinstance(x, int):
             return x

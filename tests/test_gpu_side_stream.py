@@ -56,3 +56,39 @@ def test_side_stream_sums_are_bit_identical(shape):
     db2 = harness.to_host(buf.db2)
     want = synth.widen(buf.host["dZ"]).sum(axis=0)
     assert np.linalg.norm(db2 - want) / np.linalg.norm(want) < 1e-5
+
+
+def test_sums_beside_last_waves_are_bit_identical():
+    """At the fwd+bwd bench workload (s=2048 b=4 h=5120 ffn=20480 p=4) every GEMM spans many waves, so
+    the backward runs its GEMMs in line; dB_i and dA_i end on a split-K last wave of 4 tiles on 16
+    SMs, and with a side stream registered the column sums run beside those last waves (db2 beside
+    dB's, db1 beside dA's).  Every output keeps its bits, dX included; the outputs are poisoned
+    first and checked after a single call, so sums that read dH before it is complete would show."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from megatron_tensor_mlp_gb300 import harness, synth
+    from megatron_tensor_mlp_gb300 import tpmlp as T
+
+    wl = synth.custom(2048, 4, 5120, 20480, 4, dtype="bf16", sigma_w=0.02, sigma_bias=0.01, seed=67)
+    buf = harness.MLPBuffers(wl, backward=True)
+    buf.fwd()
+    buf.bwd()
+    torch.cuda.synchronize()
+    T.tpmlp_device_status()
+    names = ("db1", "db2", "dX", "dA", "dB", "dH")
+    outs = (buf.db1_sh, buf.db2, buf.dX, buf.dA_sh, buf.dB_sh, buf.dH)
+    ref = [t.clone() for t in outs]
+    side, fork, join = torch.cuda.Stream(), torch.cuda.Event(), torch.cuda.Event()
+    T.tpmlp_set_side_stream(side, fork, join)
+    try:
+        for rep in range(3):
+            for t in outs:
+                t.fill_(float("nan"))
+            buf.bwd()
+            torch.cuda.synchronize()
+            T.tpmlp_device_status()
+            for name, a, b in zip(names, ref, outs):
+                assert torch.equal(a, b), f"{name} (call {rep})"
+    finally:
+        T.tpmlp_set_side_stream(None, None, None)
