@@ -58,19 +58,22 @@ def test_side_stream_sums_are_bit_identical(shape):
     assert np.linalg.norm(db2 - want) / np.linalg.norm(want) < 1e-5
 
 
-def test_sums_beside_last_waves_are_bit_identical():
+@pytest.mark.parametrize("shape", [(2048, 4, 5120, 20480, 4), (2050, 4, 5120, 20480, 4)], ids=["bench", "ragged-M"])
+def test_sums_beside_last_waves_are_bit_identical(shape):
     """At the fwd+bwd bench workload (s=2048 b=4 h=5120 ffn=20480 p=4) every GEMM spans many waves, so
     the backward runs its GEMMs in line; dB_i and dA_i end on a split-K last wave of 4 tiles on 16
     SMs, and with a side stream registered the column sums run beside those last waves (db2 beside
     dB's, db1 beside dA's).  Every output keeps its bits, dX included; the outputs are poisoned
-    first and checked after a single call, so sums that read dH before it is complete would show."""
+    first and checked after a single call, so sums that read dH before it is complete would show.
+    The second shape has 8 tokens past a 256-row block (a ragged K for dB and dA, ragged rows for
+    the other GEMMs) and the same last waves."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from megatron_tensor_mlp_gb300 import harness, synth
     from megatron_tensor_mlp_gb300 import tpmlp as T
 
-    wl = synth.custom(2048, 4, 5120, 20480, 4, dtype="bf16", sigma_w=0.02, sigma_bias=0.01, seed=67)
+    wl = synth.custom(*shape, dtype="bf16", sigma_w=0.02, sigma_bias=0.01, seed=67)
     buf = harness.MLPBuffers(wl, backward=True)
     buf.fwd()
     buf.bwd()
