@@ -120,6 +120,11 @@ __device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsig
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
     return r;
 }
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
 __device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
     unsigned long long r;
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
@@ -158,13 +163,30 @@ __device__ __forceinline__ void normal_cdf_pair(float x0, float x1, float& cdf0,
     cdf1 = x1 >= 0.0f ? 1.0f - h1 : h1;
 }
 
-// v[j] <- GeLU(v[j]) for j in [0, 32)
+// v[j] <- GeLU(v[j]) for j in [0, 32), as max(x, 0) - |x| h with h = erfc(|x| / sqrt(2)) / 2,
+// which holds for either sign (x >= 0: x Phi(x) = x - x h; x < 0: x Phi(x) = x h = -|x| h): no
+// sign select, and a single rounding where x >= 0.  1/sqrt(2) is folded into p, and
+// -z^2 log2(e) is taken from x directly: about 14 operations per pair of elements besides the
+// four special-function ones, against 18 through normal_cdf_pair.
 __device__ __forceinline__ void gelu_inplace32(float* v) {
+    const float kP = 0.3275911f * 0.70710678118654752f;
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
-        float c0, c1, e0, e1;
-        normal_cdf_pair(v[j], v[j + 1], c0, c1, e0, e1);
-        f2_unpack(f2_mul(f2_pack(v[j], v[j + 1]), f2_pack(c0, c1)), v[j], v[j + 1]);
+        const float x0 = v[j], x1 = v[j + 1];
+        const unsigned long long t =
+            f2_pack(rcp_approx(fmaf(kP, fabsf(x0), 1.0f)), rcp_approx(fmaf(kP, fabsf(x1), 1.0f)));
+        unsigned long long q = f2_fma(t, f2_pack(0.5307027145f, 0.5307027145f), f2_pack(-0.7265760135f, -0.7265760135f));
+        q = f2_fma(t, q, f2_pack(0.7107068705f, 0.7107068705f));
+        q = f2_fma(t, q, f2_pack(-0.142248368f, -0.142248368f));
+        q = f2_fma(t, q, f2_pack(0.127414796f, 0.127414796f));
+        q = f2_mul(t, q);  // erfc(|x| / sqrt 2) / 2 without the exponential
+        const unsigned long long xx = f2_pack(x0, x1);
+        float w0, w1;  // -x^2 / 2 log2(e)
+        f2_unpack(f2_mul(f2_mul(xx, xx), f2_pack(-0.72134752044448170f, -0.72134752044448170f)), w0, w1);
+        float h0, h1;
+        f2_unpack(f2_mul(q, f2_pack(ex2_approx(w0), ex2_approx(w1))), h0, h1);
+        v[j] = fmaf(-fabsf(x0), h0, fmaxf(x0, 0.0f));
+        v[j + 1] = fmaf(-fabsf(x1), h1, fmaxf(x1, 0.0f));
     }
 }
 
@@ -392,7 +414,9 @@ __device__ __forceinline__ void epilogue_chunk(const KArgs& p, const uint32_t (&
                     float bf[8];
                     unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(bp + g * 8)), bf);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) v[g * 8 + i] += bf[i];
+                    for (int i = 0; i < 8; i += 2)
+                        f2_unpack(f2_add(f2_pack(v[g * 8 + i], v[g * 8 + i + 1]), f2_pack(bf[i], bf[i + 1])),
+                                  v[g * 8 + i], v[g * 8 + i + 1]);
                 }
             }
         }
@@ -875,7 +899,9 @@ __device__ __forceinline__ void epilogue_tile_staged(const KArgs& p, const CUten
                         float bf[8];
                         unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(bp + g * 8)), bf);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) v[g * 8 + i] += bf[i];
+                        for (int i = 0; i < 8; i += 2)
+                            f2_unpack(f2_add(f2_pack(v[g * 8 + i], v[g * 8 + i + 1]), f2_pack(bf[i], bf[i + 1])),
+                                      v[g * 8 + i], v[g * 8 + i + 1]);
                     }
                 }
             }
