@@ -805,18 +805,22 @@ def run_gpu(args):
                 break
         barrier()
         a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sampler.mark_start("e2e")
         a.record(stream)
         copy_stream.wait_event(a)  # no copy of the timed steps starts before the timed region
         run_pipeline(n_e2e)
         z.record(stream)
         torch.cuda.synchronize()
+        sampler.mark_end("e2e")
         e2e_ms = dist_max(a.elapsed_time(z) / n_e2e)
+        ce = sampler.summary("e2e")
         e2e = {"value": round(job_throughput(flops_step, ws, e2e_ms) / 1e12, 2), "unit": "TFLOP/s",
                "ms_per_step": round(e2e_ms, 4), "steps": n_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "note": "every step copies X, dZ in from pinned host memory and reads Z, dX back, on a copy "
                        "stream overlapped with the neighbouring steps' compute; weights stay resident; "
                        "timed in the device-timed region's clock regime (settled, or after the same idle "
-                       "start in a short run)"}
+                       "start in a short run)",
+               "clocks": {k: ce.get(k) for k in ("sm_mhz", "reasons", "samples", "window", "power_w_median")}}
     T.tpmlp_device_status()
 
     # the forward at the pages' sizing (the >= 60% of dense bf16 target)
