@@ -339,15 +339,15 @@ tpmlp_status tpmlp_debug_wait_timeout(uint32_t timeout_us, void* stream);
  *     the other (GEMMs of one or two waves of tiles, e.g. s=512 b=4 h=1024 ffn=4096 p=4):
  *     dH_i on `stream` beside dB_i (then db2) on the side stream, then dA_i (after db1) on
  *     `stream` beside dX on the side stream;
- *   - otherwise, in those two, where dB_i or dA_i runs its last partial wave as a second
- *     launch (split-K CTA pairs, four CTAs per tile) that leaves at least half the SMs idle
- *     (e.g. s=2048 b=4 h=5120 ffn=20480 p=4: 4 tiles on 16 SMs), the bias-gradient column
- *     sums (db1 = 1^T dH, db2 = 1^T dZ), which need no tensor cores, run on the side stream
- *     beside that last wave: db2 beside dB_i's and db1 beside dA_i's, or both beside the one
- *     there is; `stream` waits for them before its next GEMM;
- *   - otherwise (and in tpmlp_swiglu_mlp_bwd) the column sums run on the side stream beside
- *     the first of the dA and dX GEMMs whose grid leaves enough SMs idle for all of them;
- *     where no GEMM does, they run in line.
+ *   - otherwise (and in tpmlp_swiglu_mlp_bwd), where dB_i or dA_i (the packed dW_i) runs
+ *     its last partial wave as a second launch (split-K CTA pairs, four CTAs per tile) that
+ *     leaves at least half the SMs idle (e.g. s=2048 b=4 h=5120 ffn=20480 p=4: 4 tiles on 16
+ *     SMs), the bias-gradient column sums (db1 = 1^T dH, db2 = 1^T dZ), which need no tensor
+ *     cores, run on the side stream beside that last wave: db2 beside dB_i's and db1 beside
+ *     dA_i's, or both beside the one there is; `stream` waits for them before its next GEMM;
+ *   - otherwise the column sums run on the side stream beside the first of the dA and dX
+ *     GEMMs whose grid leaves enough SMs idle for all of them; where no GEMM does, they run
+ *     in line.
  * The side stream waits for an event recorded on `stream` before its first kernel (for dX,
  * after dH; for sums beside a last wave, between that GEMM's two launches), and `stream`
  * waits for an event recorded on the side stream after its last, so everything is

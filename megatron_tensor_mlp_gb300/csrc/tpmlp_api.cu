@@ -476,7 +476,8 @@ tpmlp_status record_and_wait(cudaEvent_t ev, cudaStream_t from, cudaStream_t to,
     return TPMLP_OK;
 }
 
-// The block backward's column sums beside the last waves of its weight-gradient GEMMs.  A GEMM
+// A block backward's column sums beside the last waves of its weight-gradient GEMMs (the GeLU
+// block's dB_i and dA_i; the SwiGLU block's dB_i and packed dW_i).  A GEMM
 // of several waves whose last wave is at most half full runs that wave as a second, short
 // launch on four CTAs per tile (split-K CTA pairs), which leaves most SMs idle while it runs
 // (at s=2048 b=4 h=5120 ffn=20480 p=4: dB_i and dA_i, 4 tiles on 16 of 152 SMs for ~25 us).
@@ -957,29 +958,25 @@ tpmlp_status tpmlp_swiglu_mlp_bwd(const void* X, const void* W_sh, const void* B
     if (M == 0) return TPMLP_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool gf32 = grad_dt == TPMLP_F32;
-    {
-        // dY = dZ B_i^T per feature; the epilogue writes the packed (dHg, dHu)
-        Operand a{dZ, h, 0, 1, false};
-        Operand bb{B_sh, h, fs * h, p, false};
-        GemmSpec g = spec_base();
-        g.M = M; g.N = fs; g.K = h; g.n_shards = p;
-        g.a_batched = false; g.b_batched = true;
-        g.epi = EPI_DSWIGLU;
-        g.aux = H_ws; g.aux_ld = 2 * fs; g.aux_ss = M * 2 * fs;
-        g.out = dH_ws; g.out_ld = 2 * fs; g.out_ss = M * 2 * fs;
-        TP_TRY(run_gemm(a, bb, g, dt, *dev, st));
-    }
-    {
-        Operand a{Y_ws, fs, M * fs, p, true};          // dB_i = Y_i^T dZ
-        Operand bb{dZ, h, 0, 1, true};
-        GemmSpec g = spec_base();
-        g.M = fs; g.N = h; g.K = M; g.n_shards = p;
-        g.a_batched = true; g.b_batched = false;
-        g.epi = EPI_STORE; g.out_f32 = gf32;
-        g.out = dB_sh; g.out_ld = h; g.out_ss = fs * h;
-        TP_TRY(run_gemm(a, bb, g, dt, *dev, st));
-    }
+    // dY = dZ B_i^T per feature; the epilogue writes the packed (dHg, dHu)
+    GemmCall dy{{dZ, h, 0, 1, false}, {B_sh, h, fs * h, p, false}, spec_base()};
+    dy.g.M = M; dy.g.N = fs; dy.g.K = h; dy.g.n_shards = p;
+    dy.g.a_batched = false; dy.g.b_batched = true;
+    dy.g.epi = EPI_DSWIGLU;
+    dy.g.aux = H_ws; dy.g.aux_ld = 2 * fs; dy.g.aux_ss = M * 2 * fs;
+    dy.g.out = dH_ws; dy.g.out_ld = 2 * fs; dy.g.out_ss = M * 2 * fs;
+    const GemmCall db = dB_call(Y_ws, dZ, dB_sh, M, h, ffn, p, gf32);  // dB_i = Y_i^T dZ
     // the packed gate/up layer is a column layer of width 2 ffn: dW = X^T dH, dX = sum_i dH_i W_i^T
+    if (t_side.s != nullptr && t_side.device == dev->device && (dbw_sh || db2)) {
+        const GemmCall dw = dA_call(X, dH_ws, dW_sh, M, h, 2 * ffn, p, gf32);
+        const GemmCall dx = dX_call(dH_ws, W_sh, dX, M, h, 2 * ffn, p, false);
+        const SumsBesideTails w{dZ, db2, dH_ws, dbw_sh, M, h, 2 * fs, p, gf32};
+        bool done = false;
+        TP_TRY(sums_beside_tails(dy, db, dw, dx, w, dt, *dev, st, &done));
+        if (done) return TPMLP_OK;
+    }
+    TP_TRY(run_call(dy, dt, *dev, st));
+    TP_TRY(run_call(db, dt, *dev, st));
     return column_bwd_with_db2(X, W_sh, dH_ws, dX, dW_sh, dbw_sh, dZ, db2, M, h, 2 * ffn, p, dt, gf32, *dev, st);
 }
 

@@ -95,3 +95,52 @@ def test_sums_beside_last_waves_are_bit_identical(shape):
                 assert torch.equal(a, b), f"{name} (call {rep})"
     finally:
         T.tpmlp_set_side_stream(None, None, None)
+
+
+def test_swiglu_sums_beside_last_waves_are_bit_identical():
+    """The SwiGLU block backward at the bench's sizes (s=2048 b=4 h=5120, ffn=20480 per branch, p=4):
+    dB_i and the packed dW_i end on split-K last waves (4 and 8 tiles), so with a side stream
+    registered db2 runs beside dB's and the packed bias gradient beside dW's.  Every output keeps
+    its bits against the in-line run, after single calls on poisoned buffers."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from megatron_tensor_mlp_gb300 import tpmlp as T
+
+    s, b, h, f, p = 2048, 4, 5120, 20480, 4
+    M, fs, bf = s * b, f // p, torch.bfloat16
+    g = torch.Generator(device="cuda").manual_seed(68)
+    rnd = lambda shape, sig: (torch.randn(shape, generator=g, device="cuda") * sig).to(bf)  # noqa: E731
+    X, dZ = rnd((M, h), 1.0), rnd((M, h), 1.0)
+    W, bw, B = rnd((p, h, 2 * fs), 0.02), rnd((p, 2 * fs), 0.01), rnd((p, fs, h), 0.02)
+    Z, Y = torch.empty((M, h), dtype=bf, device="cuda"), torch.empty((p, M, fs), dtype=bf, device="cuda")
+    H = torch.empty((p, M, 2 * fs), dtype=torch.float32, device="cuda")
+    T.tpmlp_swiglu_mlp_fwd(X, W, bw, B, None, Z, Y, H, s, b, h, f, p)
+    dX, dH = torch.empty((M, h), dtype=bf, device="cuda"), torch.empty((p, M, 2 * fs), dtype=bf, device="cuda")
+    dW = torch.empty((p, h, 2 * fs), dtype=torch.float32, device="cuda")
+    dB = torch.empty((p, fs, h), dtype=torch.float32, device="cuda")
+    dbw, db2 = torch.empty((p, 2 * fs), dtype=torch.float32, device="cuda"), torch.empty(h, dtype=torch.float32,
+                                                                                            device="cuda")
+    outs = (dX, dW, dB, dbw, db2, dH)
+    names = ("dX", "dW", "dB", "dbw", "db2", "dH")
+
+    def bwd():
+        T.tpmlp_swiglu_mlp_bwd(X, W, B, H, Y, dZ, dX, dW, dB, dbw, db2, dH, s, b, h, f, p)
+
+    bwd()
+    torch.cuda.synchronize()
+    T.tpmlp_device_status()
+    ref = [t.clone() for t in outs]
+    side, fork, join = torch.cuda.Stream(), torch.cuda.Event(), torch.cuda.Event()
+    T.tpmlp_set_side_stream(side, fork, join)
+    try:
+        for rep in range(2):
+            for t in outs:
+                t.fill_(float("nan"))
+            bwd()
+            torch.cuda.synchronize()
+            T.tpmlp_device_status()
+            for name, a, c in zip(names, ref, outs):
+                assert torch.equal(a, c), f"{name} (call {rep})"
+    finally:
+        T.tpmlp_set_side_stream(None, None, None)
