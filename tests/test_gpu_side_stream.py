@@ -7,7 +7,9 @@ share of the SMs; with nothing registered everything runs in line on one stream.
 on the smaller grids, so dH, dB, dA and the column sums db1, db2 have the same bits both ways.
 dX runs on CTA pairs over its whole K loop in its share, rather than on split-K pairs that add
 two fp32 halves, so a few of its bf16 values round the other way: it is checked against the
-in-line result to one bf16 step, and against the unsharded sum.
+in-line result to one bf16 step, and against the unsharded sum.  At the bench's sizes (GEMMs of
+many waves) the side stream instead takes the column sums beside the weight-gradient GEMMs'
+split-K last waves, in the GeLU and the SwiGLU block: there every output keeps its bits.
 """
 import numpy as np
 import pytest
