@@ -32,7 +32,10 @@ sys.path.insert(0, ROOT)
 METRIC = "TP-MLP fwd/bwd TFLOP/s & tokens/s on 1 GB300; % of dense BF16 tensor peak"
 NOMINAL_BF16_TFLOPS = 2250.0
 WARMUP_SECONDS = 2.0  # default warm-up of the GPU arm (see run_gpu)
-E2E_IDLE_SECONDS = 1.0  # short runs: idle time before the end-to-end leg, as before the device-timed region
+# short runs: the end-to-end leg starts after as long an idle as the device-timed region did
+# (the buffer set-up), at least E2E_IDLE_SECONDS and at most E2E_IDLE_MAX_SECONDS
+E2E_IDLE_SECONDS = 1.0
+E2E_IDLE_MAX_SECONDS = 5.0
 MAIN_WORKLOAD = 5      # fwd + bwd
 FWD_WORKLOAD = 4       # forward at the pages' sizing
 
@@ -256,6 +259,12 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside), "window": window, "source": self.source,
                 "seconds": round(t1 - t0, 4) if (t0 is not None and t1 is not None) else None,
                 "power_w_median": med([r[3] for r in inside if r[3] is not None])}
+
+
+def e2e_idle_seconds(setup_s):
+    """Idle before a short run's end-to-end leg: as long as the buffer set-up that preceded the
+    device-timed region, within [E2E_IDLE_SECONDS, E2E_IDLE_MAX_SECONDS]."""
+    return min(max(float(setup_s), E2E_IDLE_SECONDS), E2E_IDLE_MAX_SECONDS)
 
 
 def e2e_step_count(args):
@@ -622,7 +631,10 @@ def run_gpu(args):
     if args.bwd and not wl.backward:
         import dataclasses
         wl = dataclasses.replace(wl, backward=True, name=wl.name.replace("-fwd ", "-fwd-bwd "))
+    t_setup = time.time()
     buf = harness.MLPBuffers(wl)
+    torch.cuda.synchronize()
+    setup_s = time.time() - t_setup  # the GPU idles (but for the input copies) before the timed leg
     s, b, h, f, p = buf.dims()
     M = wl.M
     stream = torch.cuda.current_stream()
@@ -788,12 +800,14 @@ def run_gpu(args):
             stream.wait_stream(copy_stream)
 
         # The same clock regime as the device-timed region: by default a settled warm-up; in a
-        # short run (explicit --warmup) W pipelined steps after the GPU has been idle, as the
-        # device-timed region starts after the idle buffer set-up, so that the power controller
-        # has raised the clock again and neither leg inherits the other's power-capped tail.
+        # short run (explicit --warmup) W pipelined steps after the GPU has been idle as long as
+        # before the device-timed region (the buffer set-up), so that the power controller has
+        # raised the clock again and neither leg inherits the other's power-capped tail.
+        idle_s = 0.0
         if args.warmup is not None:
             torch.cuda.synchronize()
-            time.sleep(E2E_IDLE_SECONDS)
+            idle_s = e2e_idle_seconds(setup_s)
+            time.sleep(idle_s)
         t_w = time.time()
         n_w = 0
         while True:
@@ -820,7 +834,8 @@ def run_gpu(args):
                        "stream overlapped with the neighbouring steps' compute; weights stay resident; "
                        "timed in the device-timed region's clock regime (settled, or after the same idle "
                        "start in a short run)",
-               "clocks": {k: ce.get(k) for k in ("sm_mhz", "reasons", "samples", "window", "power_w_median")}}
+               "clocks": {k: ce.get(k) for k in ("sm_mhz", "reasons", "samples", "window", "power_w_median")},
+               "idle_before_s": round(idle_s, 2)}
     T.tpmlp_device_status()
 
     # the forward at the pages' sizing (the >= 60% of dense bf16 target)

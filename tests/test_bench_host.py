@@ -89,3 +89,11 @@ def test_e2e_leg_times_as_many_steps_as_the_device_region(monkeypatch):
                        (["bench.py", "--e2e-steps", "0"], 0)):
         monkeypatch.setattr(sys, "argv", argv)
         assert bench.e2e_step_count(bench.parse()) == want
+
+
+def test_e2e_leg_idles_as_long_as_the_set_up():
+    """A short run's end-to-end leg starts after as long an idle as the buffer set-up gave the
+    device-timed region, bounded on both sides."""
+    assert bench.e2e_idle_seconds(3.2) == 3.2
+    assert bench.e2e_idle_seconds(0.1) == bench.E2E_IDLE_SECONDS
+    assert bench.e2e_idle_seconds(60.0) == bench.E2E_IDLE_MAX_SECONDS
